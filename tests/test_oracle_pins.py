@@ -1,0 +1,459 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+Each test ties one oracle function to something other than itself: published
+known-answer vectors, a library routine (scipy's Sylvester Hadamard matrix,
+Triton's Philox), brute-force enumeration, exhaustive round trips, closed
+forms, or textbook constants.  Sources: HyperQuant summary, Method 1-4.
+"""
+import os
+
+import numpy as np
+import pytest
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ Philox
+def test_philox_known_answers(oracle):
+    rows = _read_table("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(h, 16) for h in r]
+        out = oracle.philox(v[0:4], v[4:6])
+        assert [int(o) for o in out] == v[6:10]
+
+
+def test_philox_matches_triton_interpreter(oracle):
+    """Triton's Philox (an independent implementation) on random counters/keys."""
+    pytest.importorskip("triton")
+    import subprocess, sys, json
+    rng = np.random.default_rng(7)
+    ctrs = rng.integers(0, 2**32, size=(8, 4), dtype=np.uint64)
+    seed = int(rng.integers(0, 2**63))
+    code = r'''
+import os, sys, json
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+@triton.jit
+def k(o, seed, c0p, c1p, c2p, c3p):
+    i = tl.arange(0, 8)
+    a, b, c, d = tl.philox(seed, tl.load(c0p + i), tl.load(c1p + i), tl.load(c2p + i), tl.load(c3p + i))
+    tl.store(o + i * 4 + 0, a); tl.store(o + i * 4 + 1, b)
+    tl.store(o + i * 4 + 2, c); tl.store(o + i * 4 + 3, d)
+ctrs, seed = json.loads(sys.argv[1])
+t = lambda col: torch.tensor([x - (1 << 32) if x >= (1 << 31) else x for x in col], dtype=torch.int32)
+cols = [t([c[j] for c in ctrs]) for j in range(4)]
+out = torch.zeros(32, dtype=torch.int32)
+k[(1,)](out, seed, *cols)
+print(json.dumps([int(v) & 0xFFFFFFFF for v in out]))
+'''
+    arg = json.dumps([ctrs.tolist(), seed])
+    try:
+        res = subprocess.run([sys.executable, "-c", code, arg], capture_output=True, text=True,
+                             timeout=240)
+    except subprocess.TimeoutExpired:
+        pytest.skip("triton interpreter too slow here")
+    if res.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + res.stderr.strip().splitlines()[-1][:120])
+    got = json.loads(res.stdout.strip().splitlines()[-1])
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for i in range(8):
+        assert [int(x) for x in oracle.philox(ctrs[i], key)] == got[4 * i:4 * i + 4]
+
+
+def test_sign_masks_are_philox_words(oracle):
+    # make_signs = one Philox call with counter (segment lo, hi, 0, 'SIGN').
+    m = oracle.make_signs(0x0123456789ABCDEF, 5)
+    ref = oracle.philox([5, 0, 0, 0x5349474E], [0x89ABCDEF, 0x01234567])
+    assert (m == ref).all()
+    # masks of different segments/seeds differ and are balanced on average
+    bits = np.unpackbits(np.stack([oracle.make_signs(3, s) for s in range(256)]).view(np.uint8))
+    assert abs(bits.mean() - 0.5) < 0.01
+
+
+# ------------------------------------------------------------------ FWHT
+def _hadamard_from_oracle(oracle):
+    H = np.zeros((128, 128))
+    for j in range(128):
+        e = np.zeros(128, np.float32)
+        e[j] = 1.0
+        H[:, j] = oracle.fwht128(e)
+    return H
+
+
+def test_fwht_is_sylvester_hadamard(oracle):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    H = _hadamard_from_oracle(oracle)
+    assert set(np.unique(H)) == {-1.0, 1.0}
+    assert (H == H.T).all()
+    assert (H @ H.T == 128 * np.eye(128)).all()
+    assert (H == scipy_linalg.hadamard(128)).all()
+
+
+def test_fwht_preserves_l2_and_rounds_per_stage(oracle):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    Hs = scipy_linalg.hadamard(128).astype(np.float64)
+    rng = np.random.default_rng(1)
+    for scale in (1e-3, 1.0, 37.0):
+        x = (rng.standard_normal(128) * scale).astype(np.float32)
+        z = oracle.fwht128(x).astype(np.float64)
+        x64 = x.astype(np.float64)
+        assert abs((z @ z) / 128.0 / (x64 @ x64) - 1.0) < 1e-6
+        # 7 rounded stages: each output within 7 * 2^-24 * sum|x| of the exact value
+        exact = Hs @ x64
+        assert np.max(np.abs(z - exact)) <= 7 * 2.0**-24 * np.abs(x64).sum() * 1.01
+
+
+# ------------------------------------------------------------ nearest points
+def _brute_coset(y, odd):
+    """All points of 2D8 (odd=False) or 2D8+1 (odd=True) whose coordinates are
+    one of the two integers of that parity bracketing y_i.  The nearest point
+    of the coset is among them (moving a coordinate by 4 keeps membership)."""
+    N = y.shape[0]
+    if odd:
+        lo = 2 * np.floor((y - 1) / 2) + 1
+    else:
+        lo = 2 * np.floor(y / 2)
+    combos = ((np.arange(256)[:, None] >> np.arange(8)[None, :]) & 1).astype(np.float64)
+    pts = lo[:, None, :] + 2 * combos[None, :, :]              # N x 256 x 8
+    half = (pts - (1 if odd else 0)) / 2
+    ok = (np.round(half.sum(-1)).astype(np.int64) % 2) == 0
+    return pts, ok
+
+
+def _brute_e8_min(y):
+    best = np.full(y.shape[0], np.inf)
+    for odd in (False, True):
+        pts, ok = _brute_coset(y, odd)
+        d = ((pts - y[:, None, :]) ** 2).sum(-1)
+        d[~ok] = np.inf
+        best = np.minimum(best, d.min(-1))
+    return best
+
+
+def _in_2e8(v):
+    v = np.asarray(v, dtype=np.int64)
+    par = v & 1
+    return (par == par[..., :1]).all(-1) & ((v.sum(-1) % 4) == 0)
+
+
+def _e8_codes(oracle, ys):
+    return np.stack([oracle.nearest_e8(y) for y in ys.astype(np.float32)])
+
+
+def test_e8_nearest_point_brute_force(oracle):
+    rng = np.random.default_rng(2)
+    ys = []
+    for scale in (0.3, 1.0, 3.0, 30.0):
+        ys.append(rng.standard_normal((2500, 8)) * scale)
+    y = np.concatenate(ys).astype(np.float32).astype(np.float64)
+    v = _e8_codes(oracle, y)
+    assert _in_2e8(v).all()
+    d_or = ((v - y) ** 2).sum(-1)
+    d_min = _brute_e8_min(y)
+    assert np.all(d_or <= d_min + 1e-4)                      # fp32 decision slack only
+    assert np.mean(np.abs(d_or - d_min) < 1e-12) > 0.999
+
+
+def test_e8_ties_and_translation(oracle):
+    # exact ties: equidistant from 0 and a minimal vector, or all-integer inputs
+    ties = np.array([[1, 1, 0, 0, 0, 0, 0, 0], [0.5] * 8, [1] * 8, [-1, 1, -1, 1, 0, 0, 0, 0],
+                     [0, 0, 0, 0, 0, 0, 0, 0], [2, 0, 0, 0, 0, 0, 0, 0], [1, 0, 0, 0, 0, 0, 0, 0],
+                     [-0.0] * 8, [3, 1, 1, 1, 1, 1, 1, 1]], dtype=np.float64)
+    v = _e8_codes(oracle, ties)
+    assert _in_2e8(v).all()
+    assert np.all(((v - ties) ** 2).sum(-1) <= _brute_e8_min(ties) + 1e-12)
+    # Q(y + lam) = Q(y) + lam for lattice vectors lam (inputs kept exact in fp32)
+    rng = np.random.default_rng(3)
+    y = np.round(rng.standard_normal((2000, 8)) * 4 * 1024) / 1024
+    base = _e8_codes(oracle, y)
+    lam = 2 * rng.integers(-3, 4, size=(2000, 8))
+    odd = rng.integers(0, 2, size=2000)[:, None]
+    lam = lam + odd
+    lam[:, 7] += (-(lam.sum(-1)) % 4)                        # make sum = 0 mod 4
+    assert _in_2e8(lam).all()
+    moved = _e8_codes(oracle, y + lam)
+    same = (moved == base + lam).all(-1)
+    d1 = ((moved - (y + lam)) ** 2).sum(-1)
+    assert np.all(d1 <= _brute_e8_min(y + lam) + 1e-4)
+    assert same.mean() > 0.999
+
+
+def test_d4_and_z_nearest_point_brute_force(oracle):
+    rng = np.random.default_rng(4)
+    y = (rng.standard_normal((5000, 4)) * 3).astype(np.float32).astype(np.float64)
+    v = np.stack([oracle.nearest_d4(r) for r in y])
+    assert (v.sum(-1) % 2 == 0).all()
+    combos = ((np.arange(16)[:, None] >> np.arange(4)[None, :]) & 1)
+    pts = np.floor(y)[:, None, :] + combos[None]
+    d = ((pts - y[:, None, :]) ** 2).sum(-1)
+    d[(pts.sum(-1) % 2) != 0] = np.inf
+    assert np.allclose(((v - y) ** 2).sum(-1), d.min(-1), atol=0, rtol=0)
+    for t in (-2.5, -1.5, -0.5, 0.5, 1.5, 2.5, 0.49999997, 7.3):
+        assert oracle.nearest_z(t) == int(np.round(t))       # numpy rounds half to even
+
+
+# ------------------------------------------------------------------ dither
+def _voronoi_check_e8(u):
+    """u must be at least as close to 0 as to any lattice point."""
+    d0 = (u.astype(np.float64) ** 2).sum(-1)
+    return d0 <= _brute_e8_min(u.astype(np.float64)) + 1e-9
+
+
+@pytest.mark.parametrize("lat", [8, 4, 1])
+def test_dither_in_voronoi_cell_with_right_second_moment(oracle, lat):
+    gold = {r[0]: float(r[3]) for r in _read_table("lattice_nsm.txt")}
+    target = {8: gold["E8"], 4: gold["D4"], 1: gold["Z"]}[lat]
+    u = np.stack([oracle.dither(lat, 99, t) for t in range(600)]).reshape(-1, lat if lat > 1 else 1)
+    if lat == 8:
+        assert _voronoi_check_e8(u).all()
+    elif lat == 4:
+        assert (np.stack([oracle.nearest_d4(r) for r in u[:4000]]) == 0).all()
+    else:
+        assert (np.abs(u) < 0.5).all()
+    m = (u.astype(np.float64) ** 2).mean()
+    se = (u.astype(np.float64) ** 2).mean(-1).std() / np.sqrt(u.shape[0]) / 1.0
+    assert abs(m - target) < 4 * se + 1e-4
+    # the dither is deterministic in (seed, tile) and differs across tiles
+    assert (oracle.dither(lat, 99, 5) == oracle.dither(lat, 99, 5)).all()
+    assert not (oracle.dither(lat, 99, 5) == oracle.dither(lat, 99, 6)).all()
+
+
+@pytest.mark.parametrize("lat,name", [(8, "E8"), (4, "D4"), (1, "Z")])
+def test_dithered_error_second_moment(oracle, lat, name):
+    """With subtractive dither the error v - u - y is uniform on the Voronoi
+    cell, so its per-dimension mean square is G(Lambda) det^(2/n)."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    gold = {r[0]: float(r[3]) for r in _read_table("lattice_nsm.txt")}
+    rng = np.random.default_rng(5)
+    n_tiles = 400
+    xf = rng.standard_normal((n_tiles, 128)).astype(np.float32)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)       # truncate to bf16 bits
+    xb = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    signs = np.zeros((1, 4), np.uint32)                     # D = I for this check
+    alpha = 5.0
+    P = oracle.make_params(lat, 4, alpha, 1, 1234, signs, 1 << 40)
+    enc = oracle.encode(P, x, want_codes=True)
+    H = scipy_linalg.hadamard(128).astype(np.float64)
+    y = (xb @ H.T) * (alpha / np.sqrt(128.0))
+    u = np.stack([oracle.dither(lat, 1234, t) for t in range(n_tiles)]).astype(np.float64)
+    e = enc["codes"] - u - y
+    dim = lat if lat > 1 else 1
+    per_vec = (e.reshape(-1, dim) ** 2).mean(-1)
+    m, se = per_vec.mean(), per_vec.std() / np.sqrt(per_vec.size)
+    assert abs(m - gold[name]) < 4 * se, (m, gold[name], se)
+
+
+def test_nsm_ordering(oracle):
+    gold = {r[0]: float(r[1]) for r in _read_table("lattice_nsm.txt")}
+    assert gold["E8"] < gold["D4"] < gold["Z"]
+
+
+# ------------------------------------------------------------ fold / strip
+def _all_2e8(limit):
+    ev = np.arange(-limit, limit + 1, 2) if limit % 2 == 0 else np.arange(-limit + 1, limit + 1, 2)
+    od = np.arange(-limit + (limit % 2 == 0), limit + 1, 2)
+    out = []
+    for vals in (ev, od):
+        g = np.stack(np.meshgrid(*[vals] * 8, indexing="ij"), -1).reshape(-1, 8)
+        out.append(g[(g.sum(-1) % 4) == 0])
+    return np.concatenate(out).astype(np.int32)
+
+
+def _strip(lattice, s, k, oracle):
+    dim = {8: 8, 4: 4, 1: 1}[lattice]
+    s = s.copy().reshape(-1, dim)
+    for c in range(dim):
+        for b in range(k):
+            if oracle.bit_stripped(lattice, c, b, k):
+                s[:, c] &= ~np.uint32(1 << b)
+    return s.reshape(-1)
+
+
+def test_e8_fold_round_trip_exhaustive(oracle):
+    v = _all_2e8(4)
+    assert _in_2e8(v).all() and v.shape[0] > 200000
+    s = oracle.fold(8, v.reshape(-1))
+    assert (s < 64).all()
+    for k in range(0, 6):
+        back, rc = oracle.unfold(8, k, _strip(8, s, k, oracle))
+        assert rc == 0 and (back.reshape(-1, 8) == v).all()
+    # stripped bits per vector: 0, 7, 8 for k = 0, 1, >= 2 (= log2 [Z^8 : 2E8])
+    for k, want in ((0, 0), (1, 7), (2, 8), (5, 8)):
+        n = sum(oracle.bit_stripped(8, c, b, k) for c in range(8) for b in range(k))
+        assert n == want
+    assert 128 * 3 - oracle.tile_rbits(8, 3) == 16 * 8
+
+
+def test_fold_large_values_and_magnitudes(oracle):
+    rng = np.random.default_rng(6)
+    w = rng.integers(-(1 << 19), 1 << 19, size=(5000, 8))
+    w[:, 7] += (w[:, :7].sum(-1) - w[:, 7]) % 2                 # w in D8
+    p = rng.integers(0, 2, size=(5000, 1))
+    v = (2 * w + p).astype(np.int32)
+    assert _in_2e8(v).all()
+    s = oracle.fold(8, v.reshape(-1)).reshape(-1, 8)
+    assert (s < (1 << 22)).all()
+    ratio = s[np.abs(v) > 1000] / (2.0 * np.abs(v[np.abs(v) > 1000]))
+    assert np.all(np.abs(ratio - 1) < 0.01)                      # symbols ~ 2|v|
+    for k in (0, 1, 2, 7):
+        back, rc = oracle.unfold(8, k, _strip(8, s.reshape(-1), k, oracle))
+        assert rc == 0 and (back.reshape(-1, 8) == v).all()
+
+
+def test_d4_and_z_fold_round_trip(oracle):
+    vals = np.arange(-6, 7)
+    g = np.stack(np.meshgrid(*[vals] * 4, indexing="ij"), -1).reshape(-1, 4)
+    v = g[(g.sum(-1) % 2) == 0].astype(np.int32)
+    s = oracle.fold(4, v.reshape(-1))
+    for k in range(0, 4):
+        back, rc = oracle.unfold(4, k, _strip(4, s, k, oracle))
+        assert rc == 0 and (back.reshape(-1, 4) == v).all()
+    z = np.arange(-70000, 70000, dtype=np.int32)
+    sz = oracle.fold(1, z)
+    assert set(oracle.fold(1, np.array([0, -1, 1, -2, 2], np.int32)).tolist()) == {0, 1, 2, 3, 4}
+    back, rc = oracle.unfold(1, 0, sz)
+    assert rc == 0 and (back == z).all()
+
+
+def test_unstripped_parity_copies_are_checked(oracle):
+    v = np.array([1, 1, 1, 1, 1, 1, 1, 1], np.int32)            # odd coset point
+    s = oracle.fold(8, v)
+    bad = s.copy()
+    bad[3] ^= 1                                                # break a copy of p
+    assert oracle.unfold(8, 0, bad)[1] == oracle.ERR_CORRUPT
+    bad = s.copy()
+    bad[7] ^= 2                                                # break r
+    assert oracle.unfold(8, 1, bad)[1] == oracle.ERR_CORRUPT
+    vd = np.array([1, 0, 0, 1], np.int32)
+    sd = oracle.fold(4, vd)
+    sd[3] ^= 1
+    assert oracle.unfold(4, 0, sd)[1] == oracle.ERR_CORRUPT
+
+
+# ------------------------------------------------------------ stream layout
+def _parse_stream_py(stream, offsets, n_tiles, lattice, k, oracle):
+    """Independent reader of the documented layout (pure Python)."""
+    dim = {8: 8, 4: 4, 1: 1}[lattice]
+    syms = np.zeros((n_tiles, 128), np.int64)
+    words = [int(w) for w in stream]
+
+    def bit(base, b):
+        return (words[base + (b >> 5)] >> (31 - (b & 31))) & 1
+
+    for g in range(len(offsets) - 1):
+        base = int(offsets[g])
+        t0, t1 = 32 * g, min(32 * g + 32, n_tiles)
+        b = 0
+        for t in range(t0, t1):
+            for j in range(128):
+                s = 0
+                for bb in range(k - 1, -1, -1):
+                    if not oracle.bit_stripped(lattice, j % dim, bb, k):
+                        s |= bit(base, b) << bb
+                        b += 1
+                syms[t, j] = s
+        for t in range(t0, t1):
+            for j in range(128):
+                q = 0
+                while bit(base, b) == 0:
+                    q += 1
+                    b += 1
+                b += 1
+                syms[t, j] |= q << k
+        assert (b + 31) // 32 == int(offsets[g + 1]) - base
+    return syms
+
+
+@pytest.mark.parametrize("lat,k", [(8, 2), (8, 0), (4, 1), (1, 3)])
+def test_stream_layout_and_tile_length_closed_form(oracle, lat, k):
+    from weights_hq_encode_gb300 import inputs as I
+    x = I.bf16_bits(I.tiny_kv())[:70]                          # 3 groups, ragged tail
+    P = oracle.make_params(lat, k, 2.5, 1, 0, oracle.make_signs(0, 0), 1 << 40)
+    enc = oracle.encode(P, x, want_codes=True)
+    assert enc["status"] == 0
+    s = oracle.fold(lat, enc["codes"].reshape(-1)).reshape(-1, 128).astype(np.int64)
+    dim = {8: 8, 4: 4, 1: 1}[lat]
+    stripped = sum(oracle.bit_stripped(lat, c, b, k) for c in range(dim) for b in range(k))
+    closed = ((s >> k) + 1 + k).sum(-1) - (128 // dim) * stripped
+    assert (enc["tile_bits"] == closed).all()
+    got = _parse_stream_py(enc["stream"], enc["offsets"], x.shape[0], lat, k, oracle)
+    dims = np.arange(128) % dim
+    mask = np.zeros(128, np.int64)
+    for c in range(dim):
+        for b in range(k):
+            if oracle.bit_stripped(lat, c, b, k):
+                mask[dims == c] |= 1 << b
+    assert (got == (s & ~mask[None, :])).all()
+    dec = oracle.decode(P, enc["stream"], enc["offsets"], x.shape[0], want_codes=True)
+    assert dec["status"] == 0 and (dec["codes"] == enc["codes"]).all()
+
+
+def test_capacity_and_corruption(oracle):
+    from weights_hq_encode_gb300 import inputs as I
+    x = I.bf16_bits(I.tiny_kv())
+    P = oracle.make_params(8, 2, 2.5, 1, 0, oracle.make_signs(0, 0), 1 << 40)
+    full = oracle.encode(P, x)
+    cap = full["total_words"] // 2
+    part = oracle.encode(P, x, cap_words=cap)
+    assert part["status"] & oracle.ERR_CAPACITY
+    assert (part["offsets"] == full["offsets"]).all()
+    assert (part["stream"][:cap] == full["stream"][:cap]).all()
+    # flipping bits inside group 1 corrupts group 1 only
+    bad = full["stream"].copy()
+    w = int(full["offsets"][1]) + 3
+    bad[w] ^= 0x00F00000
+    dec = oracle.decode(P, bad, full["offsets"], x.shape[0], want_codes=True)
+    ok = oracle.decode(P, full["stream"], full["offsets"], x.shape[0], want_codes=True)
+    changed = (dec["codes"] != ok["codes"]).any(-1)
+    assert changed[32:64].any() and not changed[:32].any() and not changed[64:].any()
+    if dec["status"] & oracle.ERR_CORRUPT:
+        assert (dec["out"][32:64] == 0).all()
+    # truncated index: the last group loses a word
+    off = full["offsets"].copy()
+    off[-1] -= 1
+    dec = oracle.decode(P, full["stream"], off, x.shape[0])
+    assert dec["status"] & oracle.ERR_CORRUPT and (dec["out"][224:] == 0).all()
+
+
+def test_range_guard(oracle):
+    x = np.zeros((3, 128), np.uint16)
+    x[1, 5] = 0x7F00                                           # bf16 1.7e38
+    x[2, 0] = 0x7FC0                                           # NaN
+    P = oracle.make_params(8, 2, 4.0, 1, 9, np.zeros(4, np.uint32), 1 << 40)
+    enc = oracle.encode(P, x, want_codes=True)
+    assert enc["status"] & oracle.ERR_RANGE
+    zero = oracle.encode(P, np.zeros((3, 128), np.uint16), want_codes=True)
+    assert (enc["codes"] == zero["codes"]).all()
+
+
+def test_scalar_special_case_is_textbook_uniform_quantizer(oracle):
+    """Z lattice, dither off: codes are rint(alpha * RHT(x)) (orthonormal RHT)."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    from weights_hq_encode_gb300 import inputs as I
+    x = I.bf16_bits(I.tiny_kv())
+    signs = oracle.make_signs(11, 0)
+    alpha = 3.7
+    P = oracle.make_params(1, 8, alpha, 0, 0, signs, 1 << 40)
+    enc = oracle.encode(P, x, want_codes=True)
+    d = np.where(np.unpackbits(signs.view(np.uint8), bitorder="little")[:128] == 1, -1.0, 1.0)
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    H = scipy_linalg.hadamard(128).astype(np.float64)
+    y = (xf * d) @ H.T * (alpha / np.sqrt(128.0))
+    ref = np.round(y)
+    near_tie = np.abs(np.abs(y - np.floor(y)) - 0.5) < 1e-4
+    assert (enc["codes"][~near_tie] == ref[~near_tie]).all()
+    dec = oracle.decode(P, enc["stream"], enc["offsets"], x.shape[0])
+    # reconstruction error bounded by the cell: |H^T(v - y)| / (alpha sqrt128) per coord
+    err = dec["out"] - xf
+    assert np.sqrt((err ** 2).mean()) < 0.5 / alpha * 1.05
