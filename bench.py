@@ -1,0 +1,412 @@
+"""Benchmark of the HyperQuant tile codec on GB300 (E8, 2 and 3 bps).
+
+One step = the whole hot path on the Llama-3.1-8B-shaped KV cache
+(32 layers x {K,V} x 8 heads x 8192 tokens x 128, bf16, 1 GiB): encode at
+2 bps, decode at 2 bps, encode at 3 bps, decode at 3 bps.  `value` is the
+bf16-equivalent throughput of the step (4 x 1 GiB of bf16 per step / time)
+with inputs resident in HBM; `e2e` repeats the step through the C ABI with
+host (pinned) buffers and the host<->device copies inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), every rank codes its own cache (weak scaling, no
+data-path collective; the barrier and the max over ranks of the time use the
+process group only for timing).  `--impl reference` times the CPU oracle on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "E8 encode/decode GB/s (bf16-equiv) on 1 GB300 at 2/3 bps; % of HBM roofline"
+UNIT = "GB/s"
+WORKLOAD = ("kv_cache_8b: Llama-3.1-8B-shaped KV cache, 32 layers x {K,V} x 8 kv heads x "
+            "8192 tokens x 128, bf16 (Student-t nu=5 x lognormal channel scales, 4 outlier "
+            "channels/head x10), per-layer sign rotation + dither, E8 at 2.0 and 3.0 bps")
+RATES = ("2.0", "3.0")
+
+
+def load_json(path):
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def hbm_peak():
+    m = load_json(os.path.join(ROOT, "MEASURED_PEAKS.json"))
+    if m and m.get("hbm_gbs"):
+        return float(m["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def oracle_sample_time(budget_s: float = 12.0, max_s: float = 30.0):
+    """Times the oracle (as it stands) on a bounded sample of the workload:
+    encode + decode at 2 and 3 bps of whole (layer, K/V) slabs, repeated
+    until `budget_s` of CPU work.  Returns (GB/s bf16-equiv, cores, sample text)."""
+    import numpy as np
+    from oracle import oracle as O
+    from weights_hq_encode_gb300 import inputs as I
+    cal = load_json(os.path.join(ROOT, "weights_hq_encode_gb300", "calibration.json"))
+    C = I.KV8B
+    x = I.bf16_bits(I.kv_slab(I.slab_seed(C["data_seed"], 0, 0), C["kv_heads"], 2048)).reshape(-1, 128)
+    mask = (O.make_signs(C["sign_seed"], 0) ^ O.make_signs(C["layer_sign_seed"], 0)).reshape(1, 4)
+    threads = O.default_threads()
+    elems, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for r in RATES:
+            c = cal["kv_cache_8b"]["E8"][r]
+            P = O.make_params(8, c["k"], c["alpha"], 1, C["dither_seed"], mask, 1 << 40)
+            enc = O.encode(P, x, threads=threads)
+            O.decode(P, enc["stream"], enc["offsets"], x.shape[0], out="bf16", threads=threads)
+            elems += 2 * x.size
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or dt >= max_s:
+            break
+    gbs = 2.0 * elems / dt / 1e9
+    sample = (f"{reps} x (encode+decode at 2 and 3 bps) of {x.shape[0]} tiles "
+              f"(layer 0 K, 8 heads x 2048 tokens) in {dt:.1f} s")
+    return gbs, threads, sample, dt / reps
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    gbs, cores, sample, _ = oracle_sample_time()
+    out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic", "config": {"workload": WORKLOAD},
+           "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "weights_hq_encode_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from weights_hq_encode_gb300 import build
+    build.build()
+    from weights_hq_encode_gb300 import hq, inputs as I
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cal = load_json(os.path.join(ROOT, "weights_hq_encode_gb300", "calibration.json"))
+    C = I.KV8B
+    x = I.kv_cache_8b(dev)
+    xt = hq.as_tiles(x)
+    n = xt.shape[0]
+    n_elem = n * 128
+    masks = hq.kv_layer_masks(C["sign_seed"], C["layer_sign_seed"], C["layers"])
+    seg = np.array([masks[l] for l in range(C["layers"]) for _ in (0, 1)], np.uint32)
+    signs = torch.from_numpy(seg.view(np.int32).copy()).to(dev)
+    tps = C["kv_heads"] * C["tokens"]
+    base = rank * n                                  # distinct dither counters per rank
+    params = {r: hq.make_params(8, cal["kv_cache_8b"]["E8"][r]["k"],
+                                cal["kv_cache_8b"]["E8"][r]["alpha"], 1, C["dither_seed"], signs,
+                                tps, tile_base=base) for r in RATES}
+    ng = hq.hq_num_groups(n)
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    offsets = {r: torch.zeros(ng + 1, dtype=torch.int64, device=dev) for r in RATES}
+    total = {}
+    for r in RATES:                                  # size query (outside the timed region)
+        assert hq.hq_encode(params[r], xt, n, None, 0, offsets[r], ws, status) == 0
+        total[r] = int(offsets[r][-1].item())
+    streams = {r: torch.empty(total[r] + 1, dtype=torch.int32, device=dev) for r in RATES}
+    out = torch.empty((n, 128), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    order = []
+    for r in RATES:
+        order += [("encode", r), ("decode", r)]
+
+    def launch(kind, r):
+        if kind == "encode":
+            return hq.hq_encode(params[r], xt, n, streams[r], total[r], offsets[r], ws, status,
+                                stream)
+        return hq.hq_decode(params[r], streams[r], total[r], offsets[r], n, out, hq.HQ_OUT_BF16,
+                            status, stream)
+
+    def step(events=None):
+        for i, (kind, r) in enumerate(order):
+            if events is not None:
+                events[i][0].record(stream)
+            rc = launch(kind, r)
+            if rc != 0:
+                raise RuntimeError(f"{kind} {r}: {hq.hq_status_string(rc)}")
+            if events is not None:
+                events[i][1].record(stream)
+
+    status.zero_()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = int(status.item())
+    if st:
+        raise RuntimeError(f"codec status {hq.hq_status_string(st)} ({st})")
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in order]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.4)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    per = {}
+    for i, (kind, r) in enumerate(order):
+        d = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+        per[f"{kind}_{r}bps"] = sum(d) / len(d)
+    bytes_bf16 = 2.0 * n_elem
+    value = world * len(order) * bytes_bf16 / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    op_report = {}
+    for (kind, r) in order:
+        t = per[f"{kind}_{r}bps"]
+        alg = bytes_bf16 + 4.0 * total[r] + 8.0 * (ng + 1)
+        op_report[f"{kind}_{r}bps"] = {
+            "ms": round(t, 4), "GBps_bf16eq": round(bytes_bf16 / (t * 1e-3) / 1e9, 1),
+            "alg_bytes": int(alg), "achieved_GBps": round(alg / (t * 1e-3) / 1e9, 1),
+            "roofline_frac": round(alg / (t * 1e-3) / 1e9 / peak, 4),
+            "realized_bps": round(total[r] * 32.0 / n_elem, 4)}
+    dom = max(op_report, key=lambda k: op_report[k]["ms"])
+    traffic = None
+    tr = load_json(os.path.join(ROOT, "profiles", "traffic.json"))
+    if tr and tr.get("source_hash") == source_hash() and dom in tr.get("kernels", {}):
+        traffic = tr["kernels"][dom]
+    roof = {"bound": "hbm", "kernel": dom, "achieved": op_report[dom]["achieved_GBps"],
+            "peak": peak, "unit": "GB/s", "frac": op_report[dom]["roofline_frac"],
+            "traffic": traffic, "peak_kind": peak_kind}
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(args, hq, params, xt, n, ng, total, dev, world)
+
+    # ---- fused scores on compressed K (reported beside the step, not in `value`)
+    fused = run_fused(hq, I, cal, dev, args) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, sample, _ = oracle_sample_time()
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample}
+    if rank == 0:
+        res = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+               "data": "synthetic (seeded; shapes and distributions of the Llama-3.1-8B KV cache)",
+               "config": {"workload": WORKLOAD, "lattice": "E8", "rates_bps": [2.0, 3.0],
+                          "tiles": n, "l2": "inputs (1 GiB) larger than L2 (129 MB); no flush",
+                          "parallelism": f"{world} independent replicas (tile shards)"},
+               "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
+               "gpu_launches": len(order) * args.steps, "fused_scores": fused,
+               "cpu_baseline": cpu, "source_hash": source_hash()}
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(args, hq, params, xt, n, ng, total, dev, world):
+    import torch
+    import torch.distributed as dist
+    stream = torch.cuda.current_stream(dev)
+    host_x = torch.empty(xt.shape, dtype=xt.dtype, pin_memory=True)
+    host_x.copy_(xt)
+    xd = torch.empty_like(xt)
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    offs = {r: torch.zeros(ng + 1, dtype=torch.int64, device=dev) for r in RATES}
+    sd = {r: torch.empty(total[r] + 1, dtype=torch.int32, device=dev) for r in RATES}
+    outd = torch.empty((n, 128), dtype=torch.bfloat16, device=dev)
+    hs = {r: torch.empty(total[r] + 1, dtype=torch.int32, pin_memory=True) for r in RATES}
+    ho = {r: torch.empty(ng + 1, dtype=torch.int64, pin_memory=True) for r in RATES}
+    hout = {r: torch.empty((n, 128), dtype=torch.bfloat16, pin_memory=True) for r in RATES}
+    h2d = xt.numel() * 2
+    d2h = sum((total[r] + 1) * 4 + (ng + 1) * 8 + n * 256 for r in RATES)
+
+    def step():
+        xd.copy_(host_x, non_blocking=True)
+        for r in RATES:
+            assert hq.hq_encode(params[r], xd, n, sd[r], total[r], offs[r], ws, status, stream) == 0
+            hs[r].copy_(sd[r], non_blocking=True)
+            ho[r].copy_(offs[r], non_blocking=True)
+            assert hq.hq_decode(params[r], sd[r], total[r], offs[r], n, outd, hq.HQ_OUT_BF16,
+                                status, stream) == 0
+            hout[r].copy_(outd, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * 2 * len(RATES) * 2.0 * n * 128 / (ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4)}
+
+
+def run_fused(hq, I, cal, dev, args):
+    import numpy as np
+    import torch
+    C = I.SCORES
+    c = cal["kv_cache_8b"]["E8"]["3.0"]
+    K = I.scores_keys(dev)
+    q = I.scores_queries(dev)
+    n = C["kv_heads"] * C["tokens"]
+    m = [a ^ b for a, b in zip(hq.hq_make_signs(C["sign_seed"], 0),
+                                hq.hq_make_signs(C["layer_sign_seed"], 0))]
+    signs = torch.from_numpy(np.asarray(m, np.uint32).view(np.int32).reshape(1, 4)).to(dev)
+    p = hq.make_params(8, c["k"], c["alpha"], 1, C["dither_seeds"][0], signs, n)
+    enc = hq.encode(K, p)
+    B, Hq, T = C["batch"], C["q_heads"], C["tokens"]
+    scores = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(hq.hq_decode_qk_workspace_bytes(B, Hq), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    qi = q.view(torch.int16)
+    for _ in range(3):
+        hq.hq_decode_qk(p, enc.stream, enc.total_words, enc.offsets, C["kv_heads"], T, qi, B, Hq,
+                        scores, ws, st)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    a.record()
+    for _ in range(reps):
+        hq.hq_decode_qk(p, enc.stream, enc.total_words, enc.offsets, C["kv_heads"], T, qi, B, Hq,
+                        scores, ws, st)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    alg = enc.total_words * 4 + enc.offsets.numel() * 8 + q.numel() * 2 + scores.numel() * 4
+    peak, _ = hbm_peak()
+    flops = 2.0 * B * Hq * T * 128
+    return {"workload": "K 8 heads x 32768 tokens E8 3 bps; q 16 x 32 heads; fp32 scores",
+            "ms": round(ms, 4), "alg_bytes": int(alg),
+            "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
+            "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+            "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2), "status": int(st.item())}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

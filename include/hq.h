@@ -1,0 +1,168 @@
+/*
+ * hq.h -- C ABI of the GB300 (sm_103a) HyperQuant tile codec.
+ *
+ * The codec follows the HyperQuant technical summary, Method sections 1-4:
+ *   1 "Per-tile randomized Hadamard transform": 128-wide tiles, RHT = H D x;
+ *   2 "Lattice quantization": alpha scaling, nearest point of E8 (integer
+ *     embedding 2E8 in Z^8), D4 or Z;
+ *   3 "Bit stripping and Rice coding": membership-fixed bits removed, the
+ *     remaining symbols Rice coded with parameter k;
+ *   4 "Bias correction for the KV cache": per-layer +-1 sign rotation (folded
+ *     into the per-segment sign masks) and subtractive dither
+ *     U ~ Uniform(V(Lambda)), regenerated from a seed by the decoder.
+ * and, for hq_decode_qk, the closing section's "fused decode + MMA" (attention
+ * scores computed from compressed K without materialising K).
+ *
+ * Conventions for every entry point:
+ *   - All pointers named d_* are device pointers (CUDA global memory); the
+ *     caller allocates, owns and frees every buffer.  The library allocates
+ *     nothing, never synchronises the stream, and keeps no state between
+ *     calls, so calls on different streams are independent.
+ *   - The return value reports synchronous errors only: HQ_ERR_INVALID for a
+ *     bad argument (nothing is launched), HQ_ERR_CUDA for a failed launch.
+ *   - Data-dependent errors are OR-ed into *d_status (a device uint32 the
+ *     caller zeroes beforehand and reads after its own synchronisation):
+ *     HQ_ERR_CAPACITY, HQ_ERR_CORRUPT, HQ_ERR_TIMEOUT, HQ_ERR_RANGE.
+ *   - bf16 data is passed as raw 16-bit patterns (uint16_t); fp32 as float.
+ *   - The stream argument is a cudaStream_t (0 = legacy default stream).
+ *
+ * Stream format (one encode call):
+ *   tiles are indexed in groups of HQ_GROUP_TILES = 32 consecutive tiles; each
+ *   group starts on a 32-bit word boundary and holds
+ *     R-area: for each tile, the kept remainder bits of its 128 Rice symbols
+ *             (bits k-1..0 of each symbol, membership-fixed bits skipped);
+ *     U-area: for each tile, for each symbol, q = s >> k zeros then a one;
+ *     zero padding to the next word.
+ *   Bit b of a group is bit 31 - (b % 32) of word b / 32 (MSB first).
+ *   offsets[g] = word index of group g, offsets[n_groups] = total words.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *hq_stream_t;   /* same type as cudaStream_t */
+
+/* Status bits (return values and *d_status). */
+enum {
+  HQ_OK = 0,
+  HQ_ERR_INVALID = 1,   /* bad argument; nothing launched */
+  HQ_ERR_CUDA = 2,      /* kernel launch or memset failed */
+  HQ_ERR_CAPACITY = 4,  /* stream larger than cap_words: words past the cap
+                           were not written; offsets are still complete */
+  HQ_ERR_CORRUPT = 8,   /* a group failed a format check: its tiles decode to 0 */
+  HQ_ERR_TIMEOUT = 16,  /* a cross-block wait ran out (encode look-back) */
+  HQ_ERR_RANGE = 32     /* non-finite input or |alpha * RHT(x)| > 2^20: the tile
+                           was coded as an all-zero tile */
+};
+
+enum { HQ_Z = 1, HQ_D4 = 4, HQ_E8 = 8 };      /* lattice = its dimension */
+enum { HQ_OUT_BF16 = 0, HQ_OUT_F32 = 1 };
+
+#define HQ_TILE 128
+#define HQ_GROUP_TILES 32
+
+/* Codec parameters, identical for the encode and decode of one stream.
+ *   lattice            HQ_E8 (2E8 in Z^8), HQ_D4 or HQ_Z.
+ *   rice_k             Rice parameter, 0..15.
+ *   alpha              > 0: lattice units per unit of the orthonormal RHT
+ *                      (H / sqrt(128)) output.
+ *   dither             0 or 1 (subtractive dither, Method 4).
+ *   dither_seed        Philox key of the dither.
+ *   tile_base          global index of the call's first tile; the dither of
+ *                      tile t of the call uses counter tile_base + t, so a
+ *                      tensor split over several calls codes identically.
+ *   d_signs            device [n_segments][4] uint32 sign masks (bit i of the
+ *                      128-bit mask set = coordinate i negated before H), e.g.
+ *                      hq_make_signs(seedD, 0) XOR hq_make_signs(seedS, layer).
+ *   tiles_per_segment  > 0: tile t of the call uses mask t / tiles_per_segment.
+ *   lookback_spins     0 = default; otherwise the bound on polls of one
+ *                      predecessor in the encoder's cross-block scan, after
+ *                      which HQ_ERR_TIMEOUT is raised.
+ *   flags              bit 0 (HQ_FLAG_WORKSPACE_READY): the caller has zeroed
+ *                      the encode workspace itself; hq_encode skips its memset. */
+typedef struct hq_params {
+  int32_t lattice;
+  int32_t rice_k;
+  float alpha;
+  int32_t dither;
+  uint64_t dither_seed;
+  uint64_t tile_base;
+  const uint32_t *d_signs;
+  int64_t tiles_per_segment;
+  uint32_t lookback_spins;
+  uint32_t flags;
+} hq_params;
+
+#define HQ_FLAG_WORKSPACE_READY 1u
+
+/* Number of index groups for n_tiles tiles: ceil(n_tiles / 32). */
+int64_t hq_num_groups(int64_t n_tiles);
+
+/* Bytes of device workspace hq_encode needs for n_tiles tiles (look-back
+ * state of the cross-block scan; 8 bytes per 128 tiles plus a header). */
+size_t hq_encode_workspace_bytes(int64_t n_tiles);
+
+/* Encode n_tiles bf16 tiles (Method 1-4).
+ *   d_x        [n_tiles][128] bf16 bit patterns, device.
+ *   d_stream   device output words, capacity cap_words; NULL = size query
+ *              (only d_offsets is written).
+ *   d_offsets  device [hq_num_groups(n_tiles) + 1] uint64 word offsets;
+ *              always written completely (last entry = total words).
+ *   d_ws       device workspace of ws_bytes >= hq_encode_workspace_bytes();
+ *              zeroed by hq_encode with cudaMemsetAsync unless
+ *              HQ_FLAG_WORKSPACE_READY is set.
+ *   d_status   device uint32, OR-ed with HQ_ERR_{CAPACITY,TIMEOUT,RANGE}.
+ * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
+int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
+              uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
+              uint32_t *d_status, hq_stream_t stream);
+
+/* Decode n_tiles tiles from a stream written by hq_encode with the same
+ * params (Method 1-4 inverted: unpack, Rice decode, restore stripped bits,
+ * subtract dither, inverse RHT).
+ *   d_stream   device words [stream_words]; a group whose index entries
+ *              point outside [0, stream_words] is treated as corrupt, so a
+ *              damaged index never causes a read past the buffer.
+ *   d_out      [n_tiles][128], bf16 (out_kind HQ_OUT_BF16, round to nearest
+ *              even) or fp32 (HQ_OUT_F32).
+ * A group failing a format check decodes to zeros and sets HQ_ERR_CORRUPT.
+ * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
+int hq_decode(const hq_params *p, const uint32_t *d_stream, uint64_t stream_words,
+              const uint64_t *d_offsets, int64_t n_tiles, void *d_out, int out_kind,
+              uint32_t *d_status, hq_stream_t stream);
+
+/* Bytes of device workspace hq_decode_qk needs (rotated queries, fp32). */
+size_t hq_decode_qk_workspace_bytes(int B, int Hq);
+
+/* Attention scores from compressed K (closing section, fused decode + MMA):
+ *   scores[b][hq][t] = sum_d q[b][hq][d] * Khat[h][t][d],  h = hq / (Hq / n_kv_heads),
+ * with Khat the decode of K tile h * n_tokens + t; K itself is never written.
+ *   d_q        [B][Hq][128] bf16, device.
+ *   d_scores   [B][Hq][n_tokens] fp32, device.
+ *   d_ws       >= hq_decode_qk_workspace_bytes(B, Hq) bytes, device.
+ * Requires Hq % n_kv_heads == 0 and every head's tiles in one sign segment
+ * (tiles_per_segment a multiple of n_tokens).  Returns HQ_OK, HQ_ERR_INVALID
+ * or HQ_ERR_CUDA.  Asynchronous. */
+int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream_words,
+                 const uint64_t *d_k_offsets, int n_kv_heads, int64_t n_tokens, const uint16_t *d_q, int B, int Hq,
+                 float *d_scores, void *d_ws, size_t ws_bytes, uint32_t *d_status,
+                 hq_stream_t stream);
+
+/* Host: the 128-bit sign mask of (seed, segment) -- one Philox4x32-10 call
+ * (Salmon et al., SC'11) with key (seed lo, seed hi) and counter
+ * (segment lo, segment hi, 0, 0x5349474E).  out[4] is host memory. */
+void hq_make_signs(uint64_t seed, uint64_t segment, uint32_t out[4]);
+
+/* Host: a static, human-readable name for a status value or bit set. */
+const char *hq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif  /* HQ_H_ */

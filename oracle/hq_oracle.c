@@ -627,6 +627,7 @@ static int get_bit(const uint32_t *words, uint64_t base, uint64_t b) {
 typedef struct {
   const ora_params *P;
   const uint32_t *stream;
+  uint64_t stream_words;
   const uint64_t *offsets;
   int64_t n_tiles;
   float *out_f32;
@@ -640,7 +641,7 @@ static int parse_group(const dec_ctx *C, int64_t g, uint32_t *sym /*[32][128]*/)
   const ora_params *P = C->P;
   int k = P->rice_k, dim = lattice_dim(P->lattice);
   uint64_t base = C->offsets[g];
-  if (C->offsets[g + 1] < base) return ORA_ERR_CORRUPT;
+  if (C->offsets[g + 1] < base || C->offsets[g + 1] > C->stream_words) return ORA_ERR_CORRUPT;
   uint64_t nbits = (C->offsets[g + 1] - base) * 32u;
   int64_t t0 = g * GROUP_TILES;
   int64_t t1 = t0 + GROUP_TILES < C->n_tiles ? t0 + GROUP_TILES : C->n_tiles;
@@ -702,16 +703,19 @@ static void dec_groups(void *c, int64_t gb, int64_t ge) {
   free(sym);
 }
 
-/* Decode n_tiles tiles.  Either output may be NULL.  A group that fails any
- * check decodes to zeros and sets ORA_ERR_CORRUPT.  Returns 0, or -1 for
+/* Decode n_tiles tiles from stream[0 .. stream_words).  Either output may be
+ * NULL.  A group that fails any check (including index entries outside the
+ * stream) decodes to zeros and sets ORA_ERR_CORRUPT.  Returns 0, or -1 for
  * invalid arguments. */
-int oracle_decode(const ora_params *P, const uint32_t *stream, const uint64_t *offsets,
+int oracle_decode(const ora_params *P, const uint32_t *stream, uint64_t stream_words,
+                  const uint64_t *offsets,
                   int64_t n_tiles, float *out_f32, uint16_t *out_bf16, int32_t *v_out,
                   uint32_t *status, int nthreads) {
   if (!params_ok(P) || n_tiles < 0 || !offsets || !status || (!stream && n_tiles > 0)) return -1;
   int64_t ng = oracle_n_groups(n_tiles);
   dec_ctx C;
-  C.P = P; C.stream = stream; C.offsets = offsets; C.n_tiles = n_tiles;
+  C.P = P; C.stream = stream; C.stream_words = stream_words; C.offsets = offsets;
+  C.n_tiles = n_tiles;
   C.out_f32 = out_f32; C.out_bf16 = out_bf16; C.v_out = v_out;
   C.gflags = (uint32_t *)calloc((size_t)(ng > 0 ? ng : 1), sizeof(uint32_t));
   if (!C.gflags) return -1;

@@ -63,7 +63,7 @@ def lib():
             L.oracle_payload_bits.restype = i64
             L.oracle_payload_bits.argtypes = [vp, vp, i64, ctypes.c_int]
             L.oracle_decode.restype = ctypes.c_int
-            L.oracle_decode.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int]
+            L.oracle_decode.argtypes = [vp, vp, u64, vp, i64, vp, vp, vp, vp, ctypes.c_int]
             L.oracle_scores.restype = ctypes.c_int
             L.oracle_scores.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, ctypes.c_int,
                                         vp, ctypes.c_int]
@@ -238,7 +238,7 @@ def decode(P: Params, stream: np.ndarray, offsets: np.ndarray, n_tiles: int,
     b = np.zeros((n_tiles, 128), np.uint16) if out == "bf16" else None
     codes = np.zeros((n_tiles, 128), np.int32) if want_codes else None
     st = np.zeros(1, np.uint32)
-    rc = lib().oracle_decode(ctypes.byref(P), _p(s), _p(o), n_tiles, _p(f), _p(b), _p(codes),
+    rc = lib().oracle_decode(ctypes.byref(P), _p(s), s.size, _p(o), n_tiles, _p(f), _p(b), _p(codes),
                              _p(st), threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_decode: invalid arguments")

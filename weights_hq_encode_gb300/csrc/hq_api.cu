@@ -1,0 +1,210 @@
+// hq_api.cu -- host entry points of the C ABI declared in include/hq.h.
+// Argument checking, launch geometry and workspace layout; all arithmetic of
+// the codec runs in the kernels.
+#include <cmath>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "hq_internal.h"
+
+namespace {
+
+using namespace hq;
+
+constexpr uint32_t kDefaultSpins = 1u << 20;   // ~0.3 s of polling per predecessor
+
+bool lattice_ok(int l) { return l == HQ_Z || l == HQ_D4 || l == HQ_E8; }
+
+int rbits_of(int lattice, int k) {
+  // kept remainder bits per tile: 128 k minus the membership-fixed low bits
+  int per8 = 0;
+  for (int c = 0; c < 8; ++c) {
+    int strip = 0;
+    if (lattice == HQ_E8) strip = (c == 0) ? 0 : (c == 7 ? (k < 2 ? k : 2) : (k < 1 ? k : 1));
+    else if (lattice == HQ_D4) strip = ((c & 3) == 3) ? (k < 1 ? k : 1) : 0;
+    per8 += k - strip;
+  }
+  return per8 * 16;
+}
+
+bool params_ok(const hq_params *p) {
+  if (!p || !lattice_ok(p->lattice)) return false;
+  if (p->rice_k < 0 || p->rice_k > 15) return false;
+  if (!(p->alpha > 0.0f) || !std::isfinite(p->alpha)) return false;
+  if (p->dither != 0 && p->dither != 1) return false;
+  if (!p->d_signs || p->tiles_per_segment <= 0) return false;
+  return true;
+}
+
+bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Scales of the orthonormal RHT in lattice units, formed in double and
+// rounded once (alpha / sqrt(128) forward, 1 / (alpha sqrt(128)) back).
+float enc_scale(float alpha) { return (float)((double)alpha / std::sqrt(128.0)); }
+float dec_scale(float alpha) { return (float)(1.0 / ((double)alpha * std::sqrt(128.0))); }
+
+uint32_t host_philox_word_mul_hi(uint32_t a, uint32_t b) {
+  return (uint32_t)(((uint64_t)a * b) >> 32);
+}
+
+DecodeArgs make_decode_args(const hq_params *p, const uint32_t *stream, uint64_t stream_words,
+                            const uint64_t *offsets, int64_t n_tiles, uint32_t *status) {
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.stream = stream;
+  a.stream_words = stream_words;
+  a.offsets = offsets;
+  a.n_tiles = n_tiles;
+  a.n_groups = (n_tiles + HQ_GROUP_TILES - 1) / HQ_GROUP_TILES;
+  a.status = status;
+  a.signs = p->d_signs;
+  a.tiles_per_segment = p->tiles_per_segment;
+  a.tile_base = p->tile_base;
+  a.dither_seed = p->dither_seed;
+  a.s_dec = dec_scale(p->alpha);
+  a.rice_k = p->rice_k;
+  a.rbits = rbits_of(p->lattice, p->rice_k);
+  a.dither = p->dither;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t hq_num_groups(int64_t n_tiles) {
+  return n_tiles <= 0 ? 0 : (n_tiles + HQ_GROUP_TILES - 1) / HQ_GROUP_TILES;
+}
+
+size_t hq_encode_workspace_bytes(int64_t n_tiles) {
+  int64_t tpb = hq::encode_tiles_per_block();
+  int64_t blocks = n_tiles <= 0 ? 0 : (n_tiles + tpb - 1) / tpb;
+  return 8 + 8 * (size_t)blocks;
+}
+
+int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
+              uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
+              uint32_t *d_status, hq_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!params_ok(p) || n_tiles < 0 || !d_offsets || !d_status) return HQ_ERR_INVALID;
+  if (n_tiles == 0) {
+    return cudaMemsetAsync(d_offsets, 0, sizeof(uint64_t), st) == cudaSuccess ? HQ_OK
+                                                                             : HQ_ERR_CUDA;
+  }
+  if (!d_x || !aligned(d_x, 16) || !d_ws || !aligned(d_ws, 8) ||
+      ws_bytes < hq_encode_workspace_bytes(n_tiles) || !aligned(d_offsets, 8))
+    return HQ_ERR_INVALID;
+  EncodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.x = d_x;
+  a.n_tiles = n_tiles;
+  a.n_groups = hq_num_groups(n_tiles);
+  int64_t tpb = hq::encode_tiles_per_block();
+  int64_t blocks = (n_tiles + tpb - 1) / tpb;
+  if (blocks > 0x7FFFFFFF) return HQ_ERR_INVALID;
+  a.n_blocks = (uint32_t)blocks;
+  a.stream = d_stream;
+  a.cap_words = d_stream ? cap_words : 0;
+  a.offsets = d_offsets;
+  a.ws = d_ws;
+  a.status = d_status;
+  a.signs = p->d_signs;
+  a.tiles_per_segment = p->tiles_per_segment;
+  a.tile_base = p->tile_base;
+  a.dither_seed = p->dither_seed;
+  a.s_enc = enc_scale(p->alpha);
+  a.rice_k = p->rice_k;
+  a.rbits = rbits_of(p->lattice, p->rice_k);
+  a.dither = p->dither;
+  a.spins = p->lookback_spins ? p->lookback_spins : kDefaultSpins;
+  if (!(p->flags & HQ_FLAG_WORKSPACE_READY)) {
+    if (cudaMemsetAsync(d_ws, 0, hq_encode_workspace_bytes(n_tiles), st) != cudaSuccess)
+      return HQ_ERR_CUDA;
+  }
+  return hq::launch_encode(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int hq_decode(const hq_params *p, const uint32_t *d_stream, uint64_t stream_words,
+              const uint64_t *d_offsets, int64_t n_tiles, void *d_out, int out_kind,
+              uint32_t *d_status, hq_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!params_ok(p) || n_tiles < 0 || !d_status) return HQ_ERR_INVALID;
+  if (out_kind != HQ_OUT_BF16 && out_kind != HQ_OUT_F32) return HQ_ERR_INVALID;
+  if (n_tiles == 0) return HQ_OK;
+  if (!d_stream || !d_offsets || !d_out || !aligned(d_out, 16) || !aligned(d_offsets, 8))
+    return HQ_ERR_INVALID;
+  DecodeArgs a = make_decode_args(p, d_stream, stream_words, d_offsets, n_tiles, d_status);
+  a.out = d_out;
+  a.out_kind = out_kind;
+  return hq::launch_decode(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
+size_t hq_decode_qk_workspace_bytes(int B, int Hq) {
+  if (B <= 0 || Hq <= 0) return 0;
+  return (size_t)B * (size_t)Hq * HQ_TILE * sizeof(float);
+}
+
+int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream_words,
+                 const uint64_t *d_k_offsets, int n_kv_heads, int64_t n_tokens,
+                 const uint16_t *d_q, int B, int Hq, float *d_scores, void *d_ws,
+                 size_t ws_bytes, uint32_t *d_status, hq_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!params_ok(p) || !d_status || n_kv_heads <= 0 || n_tokens < 0 || B < 0 || Hq <= 0)
+    return HQ_ERR_INVALID;
+  if (Hq % n_kv_heads != 0) return HQ_ERR_INVALID;
+  if (n_tokens == 0 || B == 0) return HQ_OK;
+  if (p->tiles_per_segment % n_tokens != 0) return HQ_ERR_INVALID;
+  if (!d_k_stream || !d_k_offsets || !d_q || !d_scores || !d_ws ||
+      ws_bytes < hq_decode_qk_workspace_bytes(B, Hq) || !aligned(d_ws, 16) ||
+      !aligned(d_k_offsets, 8))
+    return HQ_ERR_INVALID;
+  QkArgs a;
+  a.dec = make_decode_args(p, d_k_stream, stream_words, d_k_offsets,
+                           (int64_t)n_kv_heads * n_tokens, d_status);
+  a.dec.out_kind = -1;
+  a.n_kv = n_kv_heads;
+  a.n_tokens = n_tokens;
+  a.q = d_q;
+  a.B = B;
+  a.Hq = Hq;
+  a.qrot = reinterpret_cast<float *>(d_ws);
+  a.scores = d_scores;
+  return hq::launch_decode_qk(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
+// Philox4x32-10 on the host (Salmon et al., SC'11), used for the sign masks.
+void hq_make_signs(uint64_t seed, uint64_t segment, uint32_t out[4]) {
+  uint32_t c0 = (uint32_t)segment, c1 = (uint32_t)(segment >> 32), c2 = 0u, c3 = 0x5349474Eu;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    uint32_t hi0 = host_philox_word_mul_hi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    uint32_t hi1 = host_philox_word_mul_hi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+const char *hq_status_string(int status) {
+  switch (status) {
+    case HQ_OK: return "ok";
+    case HQ_ERR_INVALID: return "invalid argument";
+    case HQ_ERR_CUDA: return "CUDA launch failed";
+    case HQ_ERR_CAPACITY: return "stream capacity exceeded";
+    case HQ_ERR_CORRUPT: return "corrupt stream";
+    case HQ_ERR_TIMEOUT: return "cross-block wait timed out";
+    case HQ_ERR_RANGE: return "input out of range";
+    default: return status < 0 ? "unknown status" : "several errors";
+  }
+}
+
+}  // extern "C"

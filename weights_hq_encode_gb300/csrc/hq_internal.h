@@ -1,0 +1,68 @@
+// hq_internal.h -- argument blocks shared by the host entry points and the
+// kernels of the codec library (not part of the public C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/hq.h"
+
+namespace hq {
+
+struct EncodeArgs {
+  const uint16_t *x;
+  int64_t n_tiles;
+  int64_t n_groups;
+  uint32_t n_blocks;
+  uint32_t *stream;         // nullptr: size query
+  uint64_t cap_words;
+  uint64_t *offsets;
+  void *ws;                 // [0]: ticket counter (uint32), then uint64 state[n_blocks]
+  uint32_t *status;
+  const uint32_t *signs;
+  int64_t tiles_per_segment;
+  uint64_t tile_base;
+  uint64_t dither_seed;
+  float s_enc;
+  int rice_k;
+  int rbits;
+  int dither;
+  uint32_t spins;
+};
+
+struct DecodeArgs {
+  const uint32_t *stream;
+  uint64_t stream_words;
+  const uint64_t *offsets;
+  int64_t n_tiles;
+  int64_t n_groups;
+  void *out;
+  int out_kind;             // HQ_OUT_BF16 / HQ_OUT_F32; -1: lattice-domain e = v - u (fp32)
+  uint32_t *status;
+  const uint32_t *signs;
+  int64_t tiles_per_segment;
+  uint64_t tile_base;
+  uint64_t dither_seed;
+  float s_dec;
+  int rice_k;
+  int rbits;
+  int dither;
+};
+
+struct QkArgs {
+  DecodeArgs dec;           // K stream
+  int n_kv;
+  int64_t n_tokens;
+  const uint16_t *q;        // [B][Hq][128] bf16
+  int B, Hq;
+  float *qrot;              // [B][Hq][128] fp32 workspace: s_dec * H * D_h * q
+  float *scores;            // [B][Hq][n_tokens]
+};
+
+int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st);
+int encode_tiles_per_block();
+int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st);
+int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);
+
+}  // namespace hq

@@ -53,9 +53,22 @@ def tiny_kv(device="cpu") -> torch.Tensor:
     return x.to(torch.bfloat16).reshape(TINY["n_tokens"], TILE)
 
 
+def kv_scales(seed: int, kv_heads: int) -> torch.Tensor:
+    """Per-channel scales [kv_heads, 1, 128] of one slab: lognormal(0, 1), with 4
+    random outlier channels per head x10.  Always drawn on the CPU, so a slab
+    drawn on any device has the same scales (only the bulk noise differs)."""
+    g = _gen(seed, "cpu")
+    scale = torch.exp(torch.randn((kv_heads, 1, TILE), generator=g))
+    for h in range(kv_heads):
+        ch = torch.randperm(TILE, generator=g)[:4]
+        scale[h, 0, ch] *= 10.0
+    return scale
+
+
 def kv_slab(seed: int, kv_heads: int, tokens: int, device="cpu") -> torch.Tensor:
-    """One (layer, K-or-V) slab [kv_heads, tokens, 128] bf16."""
-    g = _gen(seed, device)
+    """One (layer, K-or-V) slab [kv_heads, tokens, 128] bf16: Student-t (nu = 5)
+    noise times the slab's per-channel scales."""
+    g = _gen(seed + 7919, device)
     shape = (kv_heads, tokens, TILE)
     num = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     chi2 = torch.zeros(shape, device=device, dtype=torch.float32)
@@ -64,11 +77,7 @@ def kv_slab(seed: int, kv_heads: int, tokens: int, device="cpu") -> torch.Tensor
         chi2.addcmul_(n, n)
     t = num / torch.sqrt(chi2 / 5.0)
     del chi2, num
-    scale = torch.exp(torch.randn((kv_heads, 1, TILE), generator=g, device=device))
-    for h in range(kv_heads):
-        ch = torch.randperm(TILE, generator=g, device=device)[:4]
-        scale[h, 0, ch] *= 10.0
-    return (t * scale).to(torch.bfloat16)
+    return (t * kv_scales(seed, kv_heads).to(device)).to(torch.bfloat16)
 
 
 def slab_seed(data_seed: int, layer: int, kv: int) -> int:
