@@ -201,7 +201,9 @@ def test_invalid_arguments(hq, oracle):
             setattr(p, kk, vv)
         assert hq.hq_encode(p, x, 4, None, 0, offsets, ws, status) == hq.HQ_ERR_INVALID
     p = c.gpu_params(hq)
-    xm = x.view(torch.uint8)[2:2 + 4 * 256].view(torch.int16)      # misaligned input
+    big = torch.zeros(5 * 128, dtype=torch.int16, device="cuda")
+    xm = big[1:1 + 4 * 128]                                  # 2-byte offset: misaligned input
+    assert xm.data_ptr() % 16 == 2
     assert hq.hq_encode(p, xm, 4, None, 0, offsets, ws, status) == hq.HQ_ERR_INVALID
     small_ws = torch.zeros(8, dtype=torch.uint8, device="cuda")
     assert hq.hq_encode(p, x, 4, None, 0, offsets, small_ws, status) == hq.HQ_ERR_INVALID
