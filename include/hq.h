@@ -154,6 +154,36 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
                  float *d_scores, void *d_ws, size_t ws_bytes, uint32_t *d_status,
                  hq_stream_t stream);
 
+/* Largest n_tiles accepted by hq_encode_noalloc: 2^24 tiles (2^31 elements,
+ * 4 GiB of bf16 per call). */
+#define HQ_NOALLOC_MAX_TILES (1LL << 24)
+
+/* hq_encode for callers that cannot allocate device memory.  The summary has
+ * no counterpart to this entry point; it exists for deployment.  Some callers
+ * may not call cudaMalloc at the point where they encode: a serving engine
+ * that hands all free device memory to its own cache pool at start-up (a new
+ * allocation would fail or fragment that pool), a latency-critical path where
+ * cudaMalloc / cudaFree may synchronise the device, or a plugin inside a host
+ * framework that owns every allocation and offers the plugin no allocator.
+ * Such callers cannot provide the encoder's workspace, so this variant uses a
+ * fixed scratch array compiled into the library instead (about 1 MiB, held in
+ * every GPU that loads the library until the process exits).
+ *   Arguments, outputs and status bits are those of hq_encode without d_ws /
+ *   ws_bytes; the caller still passes (and owns) the input, the output words,
+ *   the offsets and the status word.  Neither this function nor anything it
+ *   calls allocates: the scratch is cleared with cudaMemsetAsync on `stream`.
+ *   n_tiles > HQ_NOALLOC_MAX_TILES returns HQ_ERR_INVALID, nothing launched.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ *   All calls on a device share the one scratch array: calls that may overlap
+ *   on the GPU (different streams without ordering between them) race and
+ *   corrupt each other's scan; serialise them (one stream, or events).
+ * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
+int hq_encode_noalloc(const hq_params *p, const uint16_t *d_x, int64_t n_tiles,
+                      uint32_t *d_stream, uint64_t cap_words, uint64_t *d_offsets,
+                      uint32_t *d_status, hq_stream_t stream);
+
 /* Host: the 128-bit sign mask of (seed, segment) -- one Philox4x32-10 call
  * (Salmon et al., SC'11) with key (seed lo, seed hi) and counter
  * (segment lo, segment hi, 0, 0x5349474E).  out[4] is host memory. */

@@ -23,7 +23,9 @@ HQ_TILE, HQ_GROUP_TILES = 128, 32
 HQ_FLAG_WORKSPACE_READY = 1
 
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
-            "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string")
+            "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
+            "hq_encode_noalloc")
+HQ_NOALLOC_MAX_TILES = 1 << 24
 
 
 class hq_params(ctypes.Structure):
@@ -50,6 +52,8 @@ def _load():
     L.hq_encode_workspace_bytes.argtypes = [i64]
     L.hq_encode.restype = ctypes.c_int
     L.hq_encode.argtypes = [vp, vp, i64, vp, u64, vp, vp, sz, vp, vp]
+    L.hq_encode_noalloc.restype = ctypes.c_int
+    L.hq_encode_noalloc.argtypes = [vp, vp, i64, vp, u64, vp, vp, vp]
     L.hq_decode.restype = ctypes.c_int
     L.hq_decode.argtypes = [vp, vp, u64, vp, i64, vp, ctypes.c_int, vp, vp]
     L.hq_decode_qk_workspace_bytes.restype = sz
@@ -121,6 +125,13 @@ def hq_encode(p: hq_params, x: torch.Tensor, n_tiles: int, stream_buf, cap_words
     return int(_lib.hq_encode(ctypes.byref(p), _ptr(x), n_tiles, _ptr(stream_buf), cap_words,
                               _ptr(offsets), _ptr(ws), ws.numel() * ws.element_size(),
                               _ptr(status), _stream(stream)))
+
+
+def hq_encode_noalloc(p: hq_params, x: torch.Tensor, n_tiles: int, stream_buf, cap_words: int,
+                      offsets: torch.Tensor, status: torch.Tensor, stream=None) -> int:
+    """hq_encode with the library's built-in scratch (no workspace argument)."""
+    return int(_lib.hq_encode_noalloc(ctypes.byref(p), _ptr(x), n_tiles, _ptr(stream_buf),
+                                      cap_words, _ptr(offsets), _ptr(status), _stream(stream)))
 
 
 def hq_decode(p: hq_params, stream_buf: torch.Tensor, stream_words: int, offsets: torch.Tensor,
