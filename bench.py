@@ -169,14 +169,14 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     cal = load_json(os.path.join(ROOT, "weights_hq_encode_gb300", "calibration.json"))
     C = I.KV8B
-    x = I.kv_cache_8b(dev)
+    x = I.kv_cache_8b(dev, tokens=args.tokens)
     xt = hq.as_tiles(x)
     n = xt.shape[0]
     n_elem = n * 128
     masks = hq.kv_layer_masks(C["sign_seed"], C["layer_sign_seed"], C["layers"])
     seg = np.array([masks[l] for l in range(C["layers"]) for _ in (0, 1)], np.uint32)
     signs = torch.from_numpy(seg.view(np.int32).copy()).to(dev)
-    tps = C["kv_heads"] * C["tokens"]
+    tps = C["kv_heads"] * args.tokens
     base = rank * n                                  # distinct dither counters per rank
     params = {r: hq.make_params(8, cal["kv_cache_8b"]["E8"][r]["k"],
                                 cal["kv_cache_8b"]["E8"][r]["alpha"], 1, C["dither_seed"], signs,
@@ -269,10 +269,10 @@ def run_ours(args, rank, world):
             "traffic": traffic, "peak_kind": peak_kind}
 
     # ---- end to end through the C ABI with host buffers
-    e2e = run_e2e(args, hq, params, xt, n, ng, total, dev, world)
+    e2e = None if args.skip_e2e else run_e2e(args, hq, params, xt, n, ng, total, dev, world)
 
     # ---- fused scores on compressed K (reported beside the step, not in `value`)
-    fused = run_fused(hq, I, cal, dev, args) if rank == 0 else None
+    fused = run_fused(hq, I, cal, dev, args) if rank == 0 and not args.skip_fused else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -284,7 +284,9 @@ def run_ours(args, rank, world):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                "data": "synthetic (seeded; shapes and distributions of the Llama-3.1-8B KV cache)",
-               "config": {"workload": WORKLOAD, "lattice": "E8", "rates_bps": [2.0, 3.0],
+               "config": {"workload": WORKLOAD if args.tokens == C["tokens"] else
+                          WORKLOAD.replace("8192 tokens", f"{args.tokens} tokens (reduced)"),
+                          "lattice": "E8", "rates_bps": [2.0, 3.0],
                           "tiles": n, "l2": "inputs (1 GiB) larger than L2 (129 MB); no flush",
                           "parallelism": f"{world} independent replicas (tile shards)"},
                "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
@@ -390,6 +392,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="tokens per head (8192 = the full workload; smaller only for profiling)")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-fused", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
