@@ -105,7 +105,8 @@ typedef struct hq_params {
 int64_t hq_num_groups(int64_t n_tiles);
 
 /* Bytes of device workspace hq_encode needs for n_tiles tiles (look-back
- * state of the cross-block scan; 8 bytes per 128 tiles plus a header). */
+ * state of the cross-block scan: an 8-byte header plus 8 bytes per index
+ * group of 32 tiles). */
 size_t hq_encode_workspace_bytes(int64_t n_tiles);
 
 /* Encode n_tiles bf16 tiles (Method 1-4).
@@ -154,9 +155,9 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
                  float *d_scores, void *d_ws, size_t ws_bytes, uint32_t *d_status,
                  hq_stream_t stream);
 
-/* Largest n_tiles accepted by hq_encode_noalloc: 2^24 tiles (2^31 elements,
- * 4 GiB of bf16 per call). */
-#define HQ_NOALLOC_MAX_TILES (1LL << 24)
+/* Largest n_tiles accepted by hq_encode_noalloc: 2^22 tiles (2^29 elements,
+ * 1 GiB of bf16 per call). */
+#define HQ_NOALLOC_MAX_TILES (1LL << 22)
 
 /* hq_encode for callers that cannot allocate device memory.  The summary has
  * no counterpart to this entry point; it exists for deployment.  Some callers

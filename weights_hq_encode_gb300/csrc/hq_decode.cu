@@ -1,18 +1,21 @@
 // hq_decode.cu -- decoder and fused score kernel of the HyperQuant tile codec.
 //
-// One warp per index group of 32 tiles, one lane per tile.  The warp finds
-// the start of every tile's unary section by a popcount scan of the group's
-// U-area (every one bit there terminates a symbol, 128 per tile), then each
-// lane reads its remainders at their fixed position, its unary codes with
-// count-leading-zeros, restores the stripped bits, regenerates the dither and
-// inverts the transform (HyperQuant summary, Method 1-4 in reverse).  Every
-// loop is bounded by the group's own word count from the index, and a group
-// that fails any check is written as zeros with HQ_ERR_CORRUPT.
+// A block of 256 threads decodes one index group of 32 tiles; lane r of a
+// tile handles symbols 16r .. 16r+15 (two 8-vectors).  The block stages the
+// group's words in shared memory, then finds where every lane's unary codes
+// start by a block-wide popcount scan of the U-area (every one bit there ends
+// a symbol: 16 per lane).  Each lane reads its remainders at their fixed
+// position and its unary codes with count-leading-zeros, restores the
+// stripped bits, regenerates the dither and inverts the transform
+// (HyperQuant summary, Method 1-4 in reverse); outputs are stored with
+// contiguous 32-byte (bf16) / 64-byte (fp32) writes per lane.  Every loop is
+// bounded by the group's word count from the index, and a group that fails
+// any check is written as zeros with HQ_ERR_CORRUPT.
 //
 // hq_decode_qk (the summary's closing section, fused decode + MMA) decodes K
-// tiles only to the lattice domain e = v - u and dots them with queries that
-// were rotated once into the same domain, q' = s_dec H D q, so K is never
-// written and no inverse transform is run per key.
+// only to the lattice domain e = v - u and dots it with queries rotated once
+// into that domain, q' = s_dec H D q, so K is never written and no inverse
+// transform is run per key.
 #include <cuda_runtime.h>
 
 #include "hq_device.cuh"
@@ -20,15 +23,20 @@
 
 namespace hq {
 
-constexpr int kDecThreads = 128;
-constexpr int kDecGroups = kDecThreads / 32;
+constexpr int kDecThreads = 256;
+constexpr int kDecStageWords = 4096;       // groups up to 16 KiB are read from shared memory
 
-__device__ __forceinline__ uint32_t get_bits(const uint32_t *p, uint64_t pos, int nb) {
-  uint64_t w = pos >> 5;
-  int sh = (int)(pos & 31);
-  uint32_t hi = __ldg(p + w);
-  uint32_t lo = (sh + nb > 32) ? __ldg(p + w + 1) : 0u;
-  return __funnelshift_l(lo, hi, sh) >> (32 - nb);
+// nb (1..64) bits starting at bit `pos` of W, MSB-first, right-aligned.
+__device__ __forceinline__ uint64_t read_bits(const uint32_t *W, uint64_t pos, int nb) {
+  const uint64_t w = pos >> 5;
+  const int sh = (int)(pos & 31);
+  const int need = (sh + nb + 31) >> 5;         // words touched (1..3)
+  const uint32_t a0 = W[w];
+  const uint32_t a1 = need > 1 ? W[w + 1] : 0u;
+  const uint32_t a2 = need > 2 ? W[w + 2] : 0u;
+  const uint64_t hi = ((uint64_t)a0 << 32) | a1;
+  const uint64_t v = (hi << sh) | (sh ? ((uint64_t)a2 >> (32 - sh)) : 0ull);
+  return nb >= 64 ? v : (v >> (64 - nb));
 }
 
 // MSB-first position (0..31) of the n-th (1-based) set bit of x.
@@ -37,94 +45,124 @@ __device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
   return __clz(x);
 }
 
-// Decodes the tile of this lane to the lattice-domain values e = v - u.
-// Returns false (for the whole warp) when the group is corrupt.
-template <int LAT>
-__device__ bool decode_group_lane(const DecodeArgs &a, int64_t g, int lane, float e[128],
-                                  uint64_t (*s_start)[kGroupTiles + 1]) {
+// Block-wide exclusive sum of v over 256 threads; *total gets the sum.
+__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t *s_warp,
+                                                   uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kDecThreads / 32; ++i) {
+    const uint32_t ws = s_warp[i];
+    if (i < warp) before += ws;
+    all += ws;
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
+// Stages group g, finds every lane's unary start, parses this lane's 16
+// symbols and returns e = v - u for them (lattice domain).  The return value
+// is block-uniform: false when the group is corrupt (e is then all zeros).
+template <int LAT, int K>
+__device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_t *s_words,
+                            uint64_t *s_start, uint32_t *s_warp) {
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+  const int k = K >= 0 ? K : a.rice_k;
   const int64_t t0 = g * kGroupTiles;
   const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
   const uint64_t base = a.offsets[g], end = a.offsets[g + 1];
-  const int k = a.rice_k;
-  const uint64_t R = (uint64_t)a.rbits;
   bool bad = end < base || end > a.stream_words;
   const uint64_t nwords = bad ? 0 : end - base;
-  const uint64_t nbits = nwords * 32;
+  const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
   const uint64_t ustart = (uint64_t)nt * R;
-  if (ustart > nbits) bad = true;
-  const uint32_t *p = a.stream + base;
-  uint64_t *starts = s_start[threadIdx.x >> 5];
+  if (ustart > nwords * 32) bad = true;
+  const bool staged = nwords <= (uint64_t)kDecStageWords;
+  const uint32_t *W = staged ? s_words : a.stream + base;
+  if (!bad && staged)
+    for (uint64_t i = tid; i < nwords; i += kDecThreads) s_words[i] = __ldg(a.stream + base + i);
+  if (tid == 0) s_start[0] = ustart;
+  __syncthreads();
 
-  // ---- tile boundaries: popcount scan of the U-area
-  uint64_t ones = 0, uend = 0;
+  // ---- unary starts: the 16m-th one of the U-area ends lane m-1's codes
   const uint64_t want = 128ull * (uint64_t)nt;
+  uint64_t ones = 0;
   if (!bad) {
-    if (lane == 0) starts[0] = ustart;
-    for (uint64_t wb = ustart >> 5; wb < nwords; wb += 32) {
-      uint64_t w = wb + lane;
-      uint32_t word = w < nwords ? __ldg(p + w) : 0u;
+    for (uint64_t wb = ustart >> 5; wb < nwords; wb += kDecThreads) {
+      const uint64_t w = wb + tid;
+      uint32_t word = w < nwords ? W[w] : 0u;
       if (w == (ustart >> 5)) word &= 0xFFFFFFFFu >> (ustart & 31);
-      uint32_t pc = __popc(word);
-      uint32_t incl = pc;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
+      const uint32_t pc = __popc(word);
+      uint32_t total;
+      const uint64_t before = ones + block_excl_sum(pc, s_warp, &total);
+      uint64_t m = (before / 16 + 1) * 16;
+      while (m <= before + pc && m <= want) {
+        s_start[m / 16] = w * 32 + (uint64_t)nth_set_bit_msb(word, (int)(m - before)) + 1;
+        m += 16;
       }
-      uint64_t before = ones + incl - pc;
-      uint64_t m = (before / 128 + 1) * 128;       // next tile boundary (in ones)
-      if (pc && m <= before + pc && m <= want) {
-        int pos = nth_set_bit_msb(word, (int)(m - before));
-        uint64_t bit = w * 32 + (uint64_t)pos + 1;
-        int ti = (int)(m / 128);
-        if (ti < nt) starts[ti] = bit;
-        else uend = bit;
-      }
-      ones += __shfl_sync(0xffffffffu, incl, 31);
+      ones += total;
     }
-    // the lane that found the end of the last tile shares it
-    uint64_t ue = uend;
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) ue = max(ue, __shfl_xor_sync(0xffffffffu, ue, d));
-    uend = ue;
-    if (ones != want || ((uend + 31) >> 5) != nwords) bad = true;
   }
-  __syncwarp();
+  __syncthreads();
+  if (!bad && (ones != want || ((s_start[8 * nt] + 31) >> 5) != nwords)) bad = true;
 
-  // ---- per-lane parse
-  uint32_t sym[128];
+  // ---- this lane's symbols
+  uint32_t sym[16];
   bool lbad = false;
-  if (!bad && lane < nt) {
-    if (R > 0) {
-      uint64_t pos = (uint64_t)lane * R;
+  const bool valid = tl < nt;
+  if (!bad && valid) {
+    const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
+    uint64_t rpos = (uint64_t)tl * R + (uint64_t)r * 2 * rb8;
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        int lowb = stripped_low_bits<LAT>(j & 7, k);
-        int nb = k - lowb;
-        sym[j] = nb > 0 ? (get_bits(p, pos, nb) << lowb) : 0u;
-        pos += (uint64_t)max(nb, 0);
+    for (int jj = 0; jj < 2; ++jj) {
+      if (K >= 0) {
+        constexpr int KK = K >= 0 ? K : 0;
+        const uint64_t rv = rb8 > 0 ? read_bits(W, rpos, rb8) : 0ull;
+        int off = rb8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int lowb = stripped_low_bits<LAT>(c, KK);
+          const int nb = KK - lowb;
+          off -= nb;
+          sym[8 * jj + c] = nb > 0 ? (uint32_t)((rv >> off) & ((1ull << nb) - 1ull)) << lowb : 0u;
+        }
+      } else {
+        uint64_t p = rpos;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int lowb = stripped_low_bits<LAT>(c, k);
+          const int nb = k - lowb;
+          sym[8 * jj + c] = nb > 0 ? (uint32_t)read_bits(W, p, nb) << lowb : 0u;
+          p += (uint64_t)(nb > 0 ? nb : 0);
+        }
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 128; ++j) sym[j] = 0u;
+      rpos += (uint64_t)rb8;
     }
-    uint64_t pos = starts[lane];
-    const uint64_t stop = (lane + 1 < nt) ? starts[lane + 1] : uend;
+    uint64_t pos = s_start[tid];
+    const uint64_t stop = s_start[tid + 1];
     const uint32_t qmax = (kSymbolLimit - 1u) >> k;
 #pragma unroll
-    for (int j = 0; j < 128; ++j) {
+    for (int j = 0; j < 16; ++j) {
       uint32_t q = 0;
       bool done = lbad;
       while (!done) {
         if (pos >= stop) { lbad = true; break; }
-        uint32_t x = __ldg(p + (pos >> 5)) << (pos & 31);
-        uint32_t avail = 32u - (uint32_t)(pos & 31);
+        const uint32_t x = W[pos >> 5] << (pos & 31);
         if (x) {
-          uint32_t z = __clz(x);
+          const uint32_t z = __clz(x);
           q += z;
           pos += z + 1;
           done = true;
         } else {
+          const uint32_t avail = 32u - (uint32_t)(pos & 31);
           q += avail;
           pos += avail;
           if (q > qmax) { lbad = true; break; }
@@ -135,68 +173,74 @@ __device__ bool decode_group_lane(const DecodeArgs &a, int64_t g, int lane, floa
     }
     if (!lbad && pos != stop) lbad = true;
   }
-  // ---- unfold, dither, e = v - u
-  if (!bad && !lbad && lane < nt) {
-    const uint64_t gt = a.tile_base + (uint64_t)(t0 + lane);
+
+  // ---- restore stripped bits, subtract the dither
+  if (!bad && valid && !lbad) {
+    const uint64_t gt = a.tile_base + (uint64_t)(t0 + tl);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int jj = 0; jj < 2; ++jj) {
       int32_t v[8];
-      unfold8<LAT>(sym + 8 * j, k, v, &lbad);
+      unfold8<LAT>(sym + 8 * jj, k, v, &lbad);
       float u[8];
       if (a.dither) {
-        dither8<LAT>(a.dither_seed, gt, (uint32_t)j, u);
+        dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[i] = 0.0f;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) e[8 * j + i] = __fsub_rn((float)v[i], u[i]);
+      for (int i = 0; i < 8; ++i) {
+        // exact int -> float for |v| < 2^22 (magic-number conversion)
+        const float fv = __fsub_rn(__int_as_float(0x4B400000 + v[i]), kMagic1);
+        e[8 * jj + i] = __fsub_rn(fv, u[i]);
+      }
     }
   }
-  bad = bad || __any_sync(0xffffffffu, lbad);
-  return !bad;
+  const int any_bad = __syncthreads_or((bad || lbad) ? 1 : 0);
+  if (any_bad || !valid) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) e[i] = 0.0f;
+  }
+  return !any_bad;
 }
 
-template <int LAT>
+template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(DecodeArgs a) {
-  __shared__ uint64_t s_start[kDecGroups][kGroupTiles + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t g = (int64_t)blockIdx.x * kDecGroups + warp;
-  if (g >= a.n_groups) return;
-  float e[128];
-  bool ok = decode_group_lane<LAT>(a, g, lane, e, s_start);
-  const int64_t t = g * kGroupTiles + lane;
+  __shared__ uint32_t s_words[kDecStageWords];
+  __shared__ uint64_t s_start[kDecThreads + 1];
+  __shared__ uint32_t s_warp[kDecThreads / 32];
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+  const int64_t g = blockIdx.x;
+  float e[16];
+  const bool ok = decode_lane<LAT, K>(a, g, e, s_words, s_start, s_warp);
+  const int64_t t = g * kGroupTiles + tl;
+  if (!ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
+  // the transform runs on every lane of the block (shuffles need full warps)
+  fwht128_x8(e, r);
   if (t >= a.n_tiles) return;
-  if (!ok) {
-    if (lane == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
-#pragma unroll
-    for (int i = 0; i < 128; ++i) e[i] = 0.0f;
-  } else {
-    fwht128(e);
+  if (ok) {
     const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
-    uint32_t m[4] = {__ldg(mask), __ldg(mask + 1), __ldg(mask + 2), __ldg(mask + 3)};
+    const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      float r = __fmul_rn(e[i], a.s_dec);
-      e[i] = ((m[i >> 5] >> (i & 31)) & 1u) ? -r : r;
+    for (int i = 0; i < 16; ++i) {
+      const float v = __fmul_rn(e[i], a.s_dec);
+      e[i] = __uint_as_float(__float_as_uint(v) ^ (((mw >> i) & 1u) << 31));
     }
   }
   if (a.out_kind == HQ_OUT_F32) {
-    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + t * kTile);
+    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + t * kTile + 16 * r);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) dst[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    for (int c = 0; c < 4; ++c)
+      dst[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
   } else {
-    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + t * kTile);
+    uint32_t w[8];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h)
-        w[h] = (uint32_t)f32_to_bf16_rn(e[8 * c + 2 * h]) |
-               ((uint32_t)f32_to_bf16_rn(e[8 * c + 2 * h + 1]) << 16);
-      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    for (int h = 0; h < 8; ++h)
+      w[h] = (uint32_t)f32_to_bf16_rn(e[2 * h]) | ((uint32_t)f32_to_bf16_rn(e[2 * h + 1]) << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + t * kTile + 16 * r);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -211,7 +255,7 @@ __global__ void rotate_queries_kernel(QkArgs a) {
   const uint16_t *q = a.q + (int64_t)row * kTile;
 #pragma unroll
   for (int i = 0; i < 128; ++i) {
-    float f = __uint_as_float((uint32_t)q[i] << 16);
+    const float f = __uint_as_float((uint32_t)q[i] << 16);
     x[i] = ((mask[i >> 5] >> (i & 31)) & 1u) ? -f : f;
   }
   fwht128(x);
@@ -219,49 +263,102 @@ __global__ void rotate_queries_kernel(QkArgs a) {
   for (int i = 0; i < 128; ++i) a.qrot[(int64_t)row * kTile + i] = __fmul_rn(x[i], a.dec.s_dec);
 }
 
-template <int LAT>
+// Scores of one group of K tiles.  Lane r holds 16 lattice-domain values of
+// its tile; partial dots with 8 query rows at a time are reduced over the
+// tile's 8 lanes by a butterfly that leaves one finished row on each lane.
+template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads)
 scores_kernel(QkArgs a) {
-  __shared__ uint64_t s_start[kDecGroups][kGroupTiles + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t g = (int64_t)blockIdx.x * kDecGroups + warp;
-  if (g >= a.dec.n_groups) return;
-  float e[128];
-  bool ok = decode_group_lane<LAT>(a.dec, g, lane, e, s_start);
-  const int64_t tile = g * kGroupTiles + lane;
-  if (tile >= a.dec.n_tiles) return;
-  if (!ok) {
-    if (lane == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-#pragma unroll
-    for (int i = 0; i < 128; ++i) e[i] = 0.0f;
-  }
-  const int h = (int)(tile / a.n_tokens);
-  const int64_t tok = tile - (int64_t)h * a.n_tokens;
+  __shared__ uint32_t s_words[kDecStageWords];
+  __shared__ uint64_t s_start[kDecThreads + 1];
+  __shared__ uint32_t s_warp[kDecThreads / 32];
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+  const int64_t g = blockIdx.x;
+  float e[16];
+  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_words, s_start, s_warp);
+  if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
+  const int64_t tile = g * kGroupTiles + tl;
+  const bool valid = tile < a.dec.n_tiles;
+  const int h = valid ? (int)(tile / a.n_tokens) : 0;
+  const int64_t tok = valid ? tile - (int64_t)h * a.n_tokens : 0;
   const int G = a.Hq / a.n_kv;
-  for (int b = 0; b < a.B; ++b) {
-    for (int gq = 0; gq < G; ++gq) {
-      const int64_t row = (int64_t)b * a.Hq + (int64_t)h * G + gq;
-      const float4 *qr = reinterpret_cast<const float4 *>(a.qrot + row * kTile);
-      float acc = 0.0f;
+  const int rows = a.B * G;                     // query rows that read this head
+  for (int r0 = 0; r0 < rows; r0 += 8) {
+    float p[8];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float4 v = __ldg(qr + c);
-        acc = __fmaf_rn(v.x, e[4 * c], acc);
-        acc = __fmaf_rn(v.y, e[4 * c + 1], acc);
-        acc = __fmaf_rn(v.z, e[4 * c + 2], acc);
-        acc = __fmaf_rn(v.w, e[4 * c + 3], acc);
+    for (int i = 0; i < 8; ++i) {
+      const int rr = r0 + i;
+      p[i] = 0.0f;
+      if (rr < rows) {
+        const int b = rr / G, gq = rr - b * G;
+        const float4 *qr = reinterpret_cast<const float4 *>(
+            a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile + 16 * r);
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 qv = __ldg(qr + c);
+          acc = __fmaf_rn(qv.x, e[4 * c], acc);
+          acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
+          acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
+          acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
+        }
+        p[i] = acc;
       }
-      a.scores[row * a.n_tokens + tok] = acc;
+    }
+    // reduce-scatter over the 8 lanes: after the step with mask m a lane keeps
+    // the half of its slots whose bit m matches its own lane bit
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+#pragma unroll
+      for (int i = 0; i < m; ++i) {
+        const bool upper = (r & m) != 0;
+        const float send = upper ? p[i] : p[i + m];
+        const float keep = upper ? p[i + m] : p[i];
+        const float got = __shfl_xor_sync(0xffffffffu, send, m);
+        p[i] = __fadd_rn(keep, got);
+      }
+    }
+    const int rr = r0 + r;                       // slot kept by lane r is row r0 + r
+    if (valid && rr < rows) {
+      const int b = rr / G, gq = rr - b * G;
+      a.scores[((int64_t)b * a.Hq + (int64_t)h * G + gq) * a.n_tokens + tok] = p[0];
     }
   }
 }
 
+template <int LAT>
+static void launch_dec_lat(const DecodeArgs &a, cudaStream_t st) {
+  dim3 grid((unsigned)a.n_groups), block(kDecThreads);
+  switch (a.rice_k) {
+    case 0: decode_kernel<LAT, 0><<<grid, block, 0, st>>>(a); break;
+    case 1: decode_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
+    case 2: decode_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
+    case 3: decode_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
+    case 4: decode_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
+    case 5: decode_kernel<LAT, 5><<<grid, block, 0, st>>>(a); break;
+    case 6: decode_kernel<LAT, 6><<<grid, block, 0, st>>>(a); break;
+    case 7: decode_kernel<LAT, 7><<<grid, block, 0, st>>>(a); break;
+    case 8: decode_kernel<LAT, 8><<<grid, block, 0, st>>>(a); break;
+    default: decode_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+  }
+}
+
+template <int LAT>
+static void launch_qk_lat(const QkArgs &a, cudaStream_t st) {
+  dim3 grid((unsigned)a.dec.n_groups), block(kDecThreads);
+  switch (a.dec.rice_k) {
+    case 1: scores_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
+    case 2: scores_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
+    case 3: scores_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
+    default: scores_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+  }
+}
+
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st) {
-  dim3 grid((unsigned)((a.n_groups + kDecGroups - 1) / kDecGroups)), block(kDecThreads);
   switch (lattice) {
-    case 8: decode_kernel<8><<<grid, block, 0, st>>>(a); break;
-    case 4: decode_kernel<4><<<grid, block, 0, st>>>(a); break;
-    default: decode_kernel<1><<<grid, block, 0, st>>>(a); break;
+    case 8: launch_dec_lat<8>(a, st); break;
+    case 4: launch_dec_lat<4>(a, st); break;
+    default: launch_dec_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
@@ -270,11 +367,10 @@ int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
   const int rows = a.B * a.Hq;
   rotate_queries_kernel<<<(rows + 127) / 128, 128, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return 1;
-  dim3 grid((unsigned)((a.dec.n_groups + kDecGroups - 1) / kDecGroups)), block(kDecThreads);
   switch (lattice) {
-    case 8: scores_kernel<8><<<grid, block, 0, st>>>(a); break;
-    case 4: scores_kernel<4><<<grid, block, 0, st>>>(a); break;
-    default: scores_kernel<1><<<grid, block, 0, st>>>(a); break;
+    case 8: launch_qk_lat<8>(a, st); break;
+    case 4: launch_qk_lat<4>(a, st); break;
+    default: launch_qk_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }

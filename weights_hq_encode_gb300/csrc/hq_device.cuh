@@ -64,6 +64,40 @@ __device__ __forceinline__ void fwht128(float x[128]) {
   }
 }
 
+// The same transform with a tile spread over 8 consecutive lanes, lane r of
+// the tile holding coordinates 16r .. 16r+15: stages h = 1, 2, 4, 8 stay in
+// registers, stages 16, 32, 64 pair lane r with lane r ^ 1, r ^ 2, r ^ 4.
+// The lower coordinate of a pair gets fl(a + b), the upper fl(a - b), exactly
+// as in the single-thread order (one rounding each, same stage order).
+__device__ __forceinline__ void fwht128_x8(float x[16], int r) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      float a = x[i], b = x[i + h];
+      x[i] = __fadd_rn(a, b);
+      x[i + h] = __fsub_rn(a, b);
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    const float sg = (r & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = __fmaf_rn(x[i], sg, o);        // lower: mine + other; upper: other - mine
+    }
+  }
+}
+
+// 1 << n for n < 32, and 0 for n >= 32 (PTX shl clamps the shift amount).
+__device__ __forceinline__ uint32_t bit_at(uint32_t n) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(1u), "r"(n));
+  return r;
+}
+
 // ---------------------------------------------------------------- lattices
 __device__ __forceinline__ uint32_t fbits(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ uint32_t zigzag(int32_t n) {
@@ -239,7 +273,7 @@ __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) 
 // Number of low remainder bits of coordinate c (within its 8-group) fixed by
 // membership and not written, for Rice parameter k.
 template <int LAT>
-__device__ __host__ __forceinline__ int stripped_low_bits(int c, int k) {
+__device__ __host__ __forceinline__ constexpr int stripped_low_bits(int c, int k) {
   if (LAT == 8) {
     if (c == 0) return 0;
     if (c == 7) return k < 2 ? k : 2;
@@ -291,11 +325,17 @@ __device__ __forceinline__ void unfold8(uint32_t s[8], int k, int32_t v[8], bool
 }
 
 // Remainder bits written per tile.
+// Remainder bits written per 8 coordinates and per tile.
 template <int LAT>
-__device__ __host__ __forceinline__ int tile_rbits(int k) {
-  int bits = 0;
-  for (int c = 0; c < 8; ++c) bits += k - stripped_low_bits<LAT>(c, k);
-  return bits * 16;
+__device__ __host__ __forceinline__ constexpr int rbits8(int k) {
+  return 8 * k - stripped_low_bits<LAT>(0, k) - stripped_low_bits<LAT>(1, k) -
+         stripped_low_bits<LAT>(2, k) - stripped_low_bits<LAT>(3, k) -
+         stripped_low_bits<LAT>(4, k) - stripped_low_bits<LAT>(5, k) -
+         stripped_low_bits<LAT>(6, k) - stripped_low_bits<LAT>(7, k);
+}
+template <int LAT>
+__device__ __host__ __forceinline__ constexpr int tile_rbits(int k) {
+  return 16 * rbits8<LAT>(k);
 }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {

@@ -1,14 +1,16 @@
 // hq_encode.cu -- single-pass encoder of the HyperQuant tile codec.
 //
-// One thread per 128-wide tile, one warp per index group of 32 tiles, one
-// block of 128 threads per 4 groups.  Per tile (HyperQuant summary, Method
-// 1-4): load bf16, apply the segment's sign mask, FWHT-128 in registers, scale
-// by alpha/sqrt(128) and add the subtractive dither in one fused multiply-add,
-// snap every 8-vector to the nearest lattice point, fold to Rice symbols.
-// Bit lengths are scanned within the warp (group layout), across the block,
-// and across blocks by a decoupled look-back (Merrill & Garland 2016) whose
-// waits are bounded; the block then assembles its words in shared memory and
-// stores them with coalesced 32-bit writes.
+// A block of 256 threads codes one index group of 32 tiles; the 8 lanes
+// r = 0..7 of a tile hold coordinates 16r .. 16r+15 (two 8-vectors), so the
+// 32-byte loads of a warp are contiguous.  Per tile (HyperQuant summary,
+// Method 1-4): apply the segment's sign mask to the bf16 input, FWHT-128
+// (stages 1-8 in registers, 16-64 by warp shuffles), scale by alpha/sqrt(128)
+// and add the subtractive dither in one fused multiply-add, snap each
+// 8-vector to the nearest lattice point and fold it into Rice symbols.
+// Bit lengths are scanned across the 8 lanes of a tile and the 32 tiles of
+// the group; groups are chained by a decoupled look-back (Merrill & Garland
+// 2016) with bounded waits.  The group's words are assembled in shared memory
+// and stored with coalesced 32-bit writes.
 #include <cuda_runtime.h>
 
 #include "hq_device.cuh"
@@ -16,13 +18,12 @@
 
 namespace hq {
 
-constexpr int kEncThreads = 128;                 // tiles per block
-constexpr int kEncGroups = kEncThreads / 32;     // groups per block
-constexpr int kStageWords = 6144;                // 24 KiB output staging per pass
+constexpr int kEncThreads = 256;                 // one group of 32 tiles
+constexpr int kStageWords = 4096;                // 16 KiB of output per window
+constexpr int kKmaxTemplated = 8;                // Rice k specialised at compile time
 
-// Look-back state word: [63:62] flag, [61:0] inclusive/aggregate word count.
-constexpr uint64_t kFlagAgg = 1ull << 62;
-constexpr uint64_t kFlagPrefix = 2ull << 62;
+constexpr uint64_t kFlagAgg = 1ull << 62;        // look-back state: [63:62] flag
+constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] words
 constexpr uint64_t kFlagPoison = 3ull << 62;
 constexpr uint64_t kValueMask = (1ull << 62) - 1;
 
@@ -72,219 +73,292 @@ __device__ bool lookback(uint64_t *state, uint32_t blk, uint64_t agg, uint32_t s
   return true;
 }
 
-// Appends bits MSB-first into a shared-memory window of words [cb, cb + kStageWords).
-struct BitSink {
-  uint32_t *sm;
-  int64_t cb;
-  int64_t cw;
-  uint32_t cur;
-  __device__ void flush() {
-    if (cur != 0u && cw >= cb && cw < cb + kStageWords) atomicOr(sm + (cw - cb), cur);
-    cur = 0u;
+// MSB-first bit writer into the shared-memory window [lo, lo + kStageWords)
+// of group words.  Whole words are OR-ed in (the first and last word of a
+// writer's range may be shared with neighbouring lanes).
+struct BitOut {
+  uint32_t *stage;
+  int64_t lo;
+  int64_t w;       // word receiving the next completed 32 bits
+  uint64_t acc;    // pending bits, right-aligned
+  int n;           // number of pending bits (< 32 between calls)
+
+  __device__ void begin(uint32_t *sm, int64_t window_lo, int64_t bitpos) {
+    stage = sm;
+    lo = window_lo;
+    w = bitpos >> 5;
+    n = (int)(bitpos & 31);
+    acc = 0;
   }
-  __device__ void or_word(int64_t w, uint32_t bits) {
-    if (w != cw) { flush(); cw = w; }
-    cur |= bits;
+  __device__ void emit(int64_t wi, uint32_t word) {
+    if (word != 0u && wi >= lo && wi < lo + kStageWords) atomicOr(stage + (wi - lo), word);
   }
-  // nb (1..31) bits of val at bit position pos.
-  __device__ void put(int64_t pos, uint32_t val, int nb) {
-    int64_t w = pos >> 5;
-    int sh = (int)(pos & 31);
-    if (sh + nb <= 32) {
-      or_word(w, val << (32 - sh - nb));
-    } else {
-      int lo = sh + nb - 32;                  // bits that spill into word w + 1
-      or_word(w, val >> lo);
-      or_word(w + 1, val << (32 - lo));
+  // nb (0..32) bits, right-aligned in val with zeros above.
+  __device__ void put(uint32_t val, int nb) {
+    acc = (acc << nb) | val;
+    n += nb;
+    if (n >= 32) {
+      n -= 32;
+      emit(w++, (uint32_t)(acc >> n));
     }
   }
-  __device__ void one(int64_t pos) { or_word(pos >> 5, 0x80000000u >> (pos & 31)); }
+  __device__ void zeros(uint32_t count) {
+    while (count >= 32u) { put(0u, 32); count -= 32u; }
+    put(0u, (int)count);
+  }
+  __device__ void finish() {
+    if (n > 0) emit(w, (uint32_t)(acc << (32 - n)));
+  }
 };
 
-template <int LAT>
+// Kept remainder bits of one 8-group of symbols, MSB-first, right-aligned
+// (rbits8<LAT>(K) bits, at most 64).
+template <int LAT, int K>
+__device__ __forceinline__ uint64_t r_bits_of(const uint32_t s[8]) {
+  uint64_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int lowb = stripped_low_bits<LAT>(c, K);
+    const int nb = K - lowb;
+    if (nb > 0) acc = (acc << nb) | (uint64_t)((s[c] >> lowb) & ((1u << nb) - 1u));
+  }
+  return acc;
+}
+
+// Unary codes (q zeros then a one) of one 8-group.
+template <int K>
+__device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int kk) {
+  const int k = K >= 0 ? K : kk;
+  uint32_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = s[i] >> k;
+  // terminator positions (LSB-first) in one word when the 8 codes fit in 32 bits
+  uint32_t T = q[0], pat = bit_at(q[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    T = T + 1u + q[i];
+    pat |= bit_at(T);
+  }
+  const uint32_t L = T + 1u;
+  if (L <= 32u) {
+    o.put(__brev(pat) >> (32u - L), (int)L);
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      o.zeros(q[i]);
+      o.put(1u, 1);
+    }
+  }
+}
+
+template <int LAT, int K>
 __global__ void __launch_bounds__(kEncThreads)
 encode_kernel(EncodeArgs a) {
   __shared__ uint32_t s_stage[kStageWords];
-  __shared__ uint64_t s_group_words[kEncGroups];
-  __shared__ uint64_t s_base;
-  __shared__ uint32_t s_ticket;
+  __shared__ uint32_t s_tile_u[kGroupTiles];
+  __shared__ uint64_t s_tile_uoff[kGroupTiles];
+  __shared__ uint64_t s_base, s_words;
+  __shared__ uint32_t s_ticket, s_flags;
   __shared__ int s_ok;
-  __shared__ uint32_t s_flags;
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
   uint64_t *state = reinterpret_cast<uint64_t *>(a.ws) + 1;
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
     s_flags = 0u;
   }
   __syncthreads();
-  const uint32_t blk = s_ticket;
-  if (blk >= a.n_blocks) return;               // only with a pre-filled ticket
+  const uint32_t g = s_ticket;                   // this block's group
+  if (g >= a.n_blocks) return;                   // only with a pre-filled ticket
+  const int k = K >= 0 ? K : a.rice_k;
+  const int64_t t0 = (int64_t)g * kGroupTiles;
+  const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
+  const int64_t t = t0 + tl;
+  const bool valid = tl < nt;
 
-  const int64_t t = (int64_t)blk * kEncThreads + threadIdx.x;
-  const bool valid = t < a.n_tiles;
-  const int k = a.rice_k;
-  uint32_t sym[128];
-  uint64_t ubits = 0;
-
+  // ---- load 16 bf16 coordinates, sign mask, FWHT
+  float x[16];
   if (valid) {
-    // ---- load, sign, FWHT
-    float x[128];
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile);
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
     const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
-    uint32_t m[4] = {__ldg(mask), __ldg(mask + 1), __ldg(mask + 2), __ldg(mask + 3)};
+    const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      uint4 v = __ldg(src + c);
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        int i = 8 * c + 2 * h;
-        uint32_t lo = w[h] << 16, hi = w[h] & 0xFFFF0000u;
-        lo ^= ((m[i >> 5] >> (i & 31)) & 1u) << 31;
-        hi ^= ((m[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u) << 31;
-        x[i] = __uint_as_float(lo);
-        x[i + 1] = __uint_as_float(hi);
-      }
+    for (int q = 0; q < 8; ++q) {
+      // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of the pair
+      const uint32_t sw = (((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u;
+      const uint32_t ww = w[q] ^ sw;
+      x[2 * q] = __uint_as_float(ww << 16);
+      x[2 * q + 1] = __uint_as_float(ww & 0xFFFF0000u);
     }
-    fwht128(x);
-    // ---- scale + dither (one rounding), range rule
-    const uint64_t gt = a.tile_base + (uint64_t)t;
-    bool bad = false;
+  } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+  }
+  fwht128_x8(x, r);
+
+  // ---- scale + dither (one rounding), range rule for the whole tile
+  const uint64_t gt = a.tile_base + (uint64_t)t;
+  bool bad = false;
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    float u[8];
+    if (a.dither) {
+      dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = __fmaf_rn(x[8 * jj + i], a.s_enc, u[i]);
+      bad |= !(fabsf(y) <= kRangeLimit);
+      x[8 * jj + i] = y;
+    }
+  }
+  const uint32_t bal = __ballot_sync(0xffffffffu, valid && bad);
+  if ((bal >> (lane & 24)) & 0xFFu) {            // some lane of this tile is out of range
+    if (r == 0) atomicOr(&s_flags, (uint32_t)HQ_ERR_RANGE);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
       float u[8];
-      if (a.dither) dither8<LAT>(a.dither_seed, gt, (uint32_t)j, u);
+      if (a.dither) {
+        dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float y = __fmaf_rn(x[8 * j + i], a.s_enc, a.dither ? u[i] : 0.0f);
-        bad |= !(fabsf(y) <= kRangeLimit);
-        x[8 * j + i] = y;
+        for (int i = 0; i < 8; ++i) u[i] = 0.0f;
       }
-    }
-    if (bad) {
-      atomicOr(&s_flags, (uint32_t)HQ_ERR_RANGE);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float u[8];
-        if (a.dither) dither8<LAT>(a.dither_seed, gt, (uint32_t)j, u);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          x[8 * j + i] = __fmaf_rn(0.0f, a.s_enc, a.dither ? u[i] : 0.0f);
-      }
-    }
-    // ---- nearest point, fold, unary lengths
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      uint32_t s8[8];
-      quantize_fold8<LAT>(x + 8 * j, s8);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        sym[8 * j + i] = s8[i];
-        ubits += (uint64_t)(s8[i] >> k) + 1u;
-      }
+      for (int i = 0; i < 8; ++i) x[8 * jj + i] = __fmaf_rn(0.0f, a.s_enc, u[i]);
     }
   }
 
-  // ---- group layout: warp scan of unary lengths
-  const int64_t g = (int64_t)blk * kEncGroups + warp;
-  const int64_t gt0 = g * kGroupTiles;
-  const int nt = (int)max((int64_t)0, min((int64_t)kGroupTiles, a.n_tiles - gt0));
-  const uint64_t R = (uint64_t)a.rbits;
-  uint64_t incl = ubits;
+  // ---- nearest point, fold, unary lengths
+  uint32_t sym[16];
+  quantize_fold8<LAT>(x, sym);
+  quantize_fold8<LAT>(x + 8, sym + 8);
+  uint32_t ubits = 0;
+  if (valid) {
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    uint64_t o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += o;
+    for (int i = 0; i < 16; ++i) ubits += (sym[i] >> k) + 1u;
   }
-  const uint64_t u_excl = incl - ubits;
-  const uint64_t group_bits = (uint64_t)nt * R + __shfl_sync(0xffffffffu, incl, 31);
-  if (lane == 0) s_group_words[warp] = (group_bits + 31) >> 5;
+  // prefix over the 8 lanes of the tile
+  uint32_t incl = ubits;
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d, 8);
+    if (r >= d) incl += o;
+  }
+  const uint32_t u_in_tile = incl - ubits;
+  if (r == 7) s_tile_u[tl] = incl;
   __syncthreads();
 
-  // ---- block scan + look-back
-  if (threadIdx.x == 0) {
-    uint64_t agg = 0;
-    for (int w = 0; w < kEncGroups; ++w) agg += s_group_words[w];
-    uint64_t excl = 0;
-    bool ok = lookback(state, blk, agg, a.spins, &excl);
-    if (!ok) atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
-    s_base = excl;
-    s_ok = ok ? 1 : 0;
+  // ---- group layout, index, look-back (warp 0)
+  const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
+  if (tid < 32) {
+    const uint64_t tu = s_tile_u[tid];
+    uint64_t ui = tu;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t o = __shfl_up_sync(0xffffffffu, ui, d);
+      if (lane >= d) ui += o;
+    }
+    s_tile_uoff[tid] = ui - tu;
+    const uint64_t total = __shfl_sync(0xffffffffu, ui, 31);
+    if (tid == 0) {
+      const uint64_t words = ((uint64_t)nt * R + total + 31) >> 5;
+      uint64_t excl = 0;
+      const bool ok = lookback(state, g, words, a.spins, &excl);
+      if (!ok) atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
+      s_ok = ok ? 1 : 0;
+      s_base = excl;
+      s_words = words;
+      if (ok) {
+        a.offsets[g] = excl;
+        if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + words;
+        if (excl + words > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
+      }
+    }
   }
   __syncthreads();
   if (!s_ok) return;
-  const uint64_t base = s_base;
-  uint64_t gprefix = 0;
-  for (int w = 0; w < warp; ++w) gprefix += s_group_words[w];
-  uint64_t block_words = 0;
-  for (int w = 0; w < kEncGroups; ++w) block_words += s_group_words[w];
-
-  // ---- index
-  if (lane == 0 && nt > 0) {
-    a.offsets[g] = base + gprefix;
-    if (g == a.n_groups - 1) a.offsets[a.n_groups] = base + gprefix + s_group_words[warp];
-  }
-  if (threadIdx.x == 0) {
-    if (s_flags) atomicOr(a.status, s_flags);
-    if (base + block_words > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
-  }
+  if (tid == 0 && s_flags) atomicOr(a.status, s_flags);
   if (a.stream == nullptr) return;
+  const uint64_t base = s_base, gwords = s_words;
 
-  // ---- assemble words in shared memory, one window of kStageWords at a time
-  const int64_t r_pos = (int64_t)(gprefix * 32 + (uint64_t)lane * R);
-  const int64_t u_pos0 = (int64_t)(gprefix * 32 + (uint64_t)nt * R + u_excl);
-  for (int64_t cb = 0; cb < (int64_t)block_words; cb += kStageWords) {
-    for (int i = threadIdx.x; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
-    __syncthreads();
-    const int64_t lo_bit = cb * 32, hi_bit = (cb + kStageWords) * 32;
-    if (valid) {
-      BitSink sink{s_stage, cb, -1, 0u};
-      // R-section (skipped when it lies outside the window)
-      if (r_pos < hi_bit && r_pos + (int64_t)R > lo_bit && R > 0) {
-        int64_t pos = r_pos;
+  // ---- bits: R-section of this lane's two vectors, then its unary codes
+  const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
+  const int64_t r_pos = (int64_t)tl * (int64_t)R + (int64_t)r * 2 * rb8;
+  const int64_t u_pos = (int64_t)nt * (int64_t)R + (int64_t)s_tile_uoff[tl] + u_in_tile;
+  for (int64_t cb = 0; cb < (int64_t)gwords; cb += kStageWords) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          int lowb = stripped_low_bits<LAT>(j & 7, k);
-          int nb = k - lowb;
-          if (nb > 0) {
-            sink.put(pos, (sym[j] >> lowb) & ((1u << nb) - 1u), nb);
-            pos += nb;
+    for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
+    __syncthreads();
+    if (valid) {
+      BitOut o;
+      if (rb8 > 0) {
+        o.begin(s_stage, cb, r_pos);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          if (K >= 0) {
+            const uint64_t rv = r_bits_of<LAT, (K >= 0 ? K : 0)>(sym + 8 * jj);
+            if (rb8 > 32) o.put((uint32_t)(rv >> 32), rb8 - 32);
+            o.put((uint32_t)rv & (rb8 >= 32 ? 0xFFFFFFFFu : ((1u << rb8) - 1u)),
+                  rb8 > 32 ? 32 : rb8);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int lowb = stripped_low_bits<LAT>(c, k);
+              const int nb = k - lowb;
+              if (nb > 0) o.put((sym[8 * jj + c] >> lowb) & ((1u << nb) - 1u), nb);
+            }
           }
         }
+        o.finish();
       }
-      // U-section
-      if (u_pos0 < hi_bit && u_pos0 + (int64_t)ubits > lo_bit) {
-        int64_t pos = u_pos0;
-#pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          pos += (int64_t)(sym[j] >> k);
-          if (pos >= lo_bit && pos < hi_bit) sink.one(pos);
-          ++pos;
-        }
-      }
-      sink.flush();
+      o.begin(s_stage, cb, u_pos);
+      put_unary8<K>(o, sym, k);
+      put_unary8<K>(o, sym + 8, k);
+      o.finish();
     }
     __syncthreads();
-    const int64_t nw = min((int64_t)kStageWords, (int64_t)block_words - cb);
-    for (int i = threadIdx.x; i < nw; i += kEncThreads) {
-      uint64_t gw = base + (uint64_t)(cb + i);
+    const int64_t nw = min((int64_t)kStageWords, (int64_t)gwords - cb);
+    for (int i = tid; i < nw; i += kEncThreads) {
+      const uint64_t gw = base + (uint64_t)(cb + i);
       if (gw < a.cap_words) a.stream[gw] = s_stage[i];
     }
     __syncthreads();
   }
 }
 
-int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st) {
+template <int LAT>
+static void launch_lat(const EncodeArgs &a, cudaStream_t st) {
   dim3 grid((unsigned)a.n_blocks), block(kEncThreads);
+  switch (a.rice_k) {
+    case 0: encode_kernel<LAT, 0><<<grid, block, 0, st>>>(a); break;
+    case 1: encode_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
+    case 2: encode_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
+    case 3: encode_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
+    case 4: encode_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
+    case 5: encode_kernel<LAT, 5><<<grid, block, 0, st>>>(a); break;
+    case 6: encode_kernel<LAT, 6><<<grid, block, 0, st>>>(a); break;
+    case 7: encode_kernel<LAT, 7><<<grid, block, 0, st>>>(a); break;
+    case 8: encode_kernel<LAT, 8><<<grid, block, 0, st>>>(a); break;
+    default: encode_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+  }
+}
+
+int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st) {
+  static_assert(kKmaxTemplated == 8, "dispatch covers k = 0..8");
   switch (lattice) {
-    case 8: encode_kernel<8><<<grid, block, 0, st>>>(a); break;
-    case 4: encode_kernel<4><<<grid, block, 0, st>>>(a); break;
-    default: encode_kernel<1><<<grid, block, 0, st>>>(a); break;
+    case 8: launch_lat<8>(a, st); break;
+    case 4: launch_lat<4>(a, st); break;
+    default: launch_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 
-int encode_tiles_per_block() { return kEncThreads; }
+int encode_tiles_per_block() { return kGroupTiles; }
 
 }  // namespace hq

@@ -2,7 +2,7 @@
 // allocate device memory.
 //
 // The encoder's only scratch is the look-back state of its cross-block scan
-// (a ticket counter plus 8 bytes per block of 128 tiles).  hq_encode takes
+// (a ticket counter plus 8 bytes per index group of 32 tiles).  hq_encode takes
 // that scratch from the caller; this entry point instead uses a fixed array
 // compiled into the library, so neither the library nor the caller allocates
 // anything.  The array lives in every GPU's memory from the moment the
@@ -15,10 +15,11 @@
 
 namespace {
 
-// 8-byte ticket header + 8 bytes per block of 128 tiles for HQ_NOALLOC_MAX_TILES
-// tiles, rounded up to 256 bytes.
+// 8-byte ticket header + 8 bytes of look-back state per index group (one
+// encoder block per group) for HQ_NOALLOC_MAX_TILES tiles, rounded up to 256
+// bytes.
 constexpr size_t kNoallocScratchBytes =
-    ((8 + 8 * (size_t)(HQ_NOALLOC_MAX_TILES / 128)) + 255) / 256 * 256;
+    ((8 + 8 * (size_t)(HQ_NOALLOC_MAX_TILES / HQ_GROUP_TILES)) + 255) / 256 * 256;
 
 static __device__ __align__(256) unsigned char g_encode_scratch[kNoallocScratchBytes];
 

@@ -25,7 +25,7 @@ HQ_FLAG_WORKSPACE_READY = 1
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
             "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
             "hq_encode_noalloc")
-HQ_NOALLOC_MAX_TILES = 1 << 24
+HQ_NOALLOC_MAX_TILES = 1 << 22
 
 
 class hq_params(ctypes.Structure):
