@@ -48,6 +48,18 @@ uint32_t host_philox_word_mul_hi(uint32_t a, uint32_t b) {
   return (uint32_t)(((uint64_t)a * b) >> 32);
 }
 
+PhiloxKeys round_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = k0;
+    k.k1[r] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return k;
+}
+
 DecodeArgs make_decode_args(const hq_params *p, const uint32_t *stream, uint64_t stream_words,
                             const uint64_t *offsets, int64_t n_tiles, uint32_t *status) {
   DecodeArgs a;
@@ -62,6 +74,7 @@ DecodeArgs make_decode_args(const hq_params *p, const uint32_t *stream, uint64_t
   a.tiles_per_segment = p->tiles_per_segment;
   a.tile_base = p->tile_base;
   a.dither_seed = p->dither_seed;
+  a.keys = round_keys(p->dither_seed);
   a.s_dec = dec_scale(p->alpha);
   a.rice_k = p->rice_k;
   a.rbits = rbits_of(p->lattice, p->rice_k);
@@ -113,6 +126,7 @@ int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t
   a.tiles_per_segment = p->tiles_per_segment;
   a.tile_base = p->tile_base;
   a.dither_seed = p->dither_seed;
+  a.keys = round_keys(p->dither_seed);
   a.s_enc = enc_scale(p->alpha);
   a.rice_k = p->rice_k;
   a.rbits = rbits_of(p->lattice, p->rice_k);

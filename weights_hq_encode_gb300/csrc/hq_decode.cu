@@ -16,6 +16,7 @@
 // only to the lattice domain e = v - u and dots it with queries rotated once
 // into that domain, q' = s_dec H D q, so K is never written and no inverse
 // transform is run per key.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "hq_device.cuh"
@@ -146,30 +147,51 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_
       }
       rpos += (uint64_t)rb8;
     }
+    // unary codes: a 64-bit window from the lane's start holds all 16 codes
+    // whenever they total at most 64 bits (the common case); longer sections
+    // take the word-by-word path
     uint64_t pos = s_start[tid];
     const uint64_t stop = s_start[tid + 1];
     const uint32_t qmax = (kSymbolLimit - 1u) >> k;
+    if (stop - pos <= 64 && stop >= pos) {
+      const uint64_t w = pos >> 5;
+      const int sh = (int)(pos & 31);
+      const uint32_t a0 = W[w];
+      const uint32_t a1 = w + 1 < nwords ? W[w + 1] : 0u;
+      const uint32_t a2 = w + 2 < nwords ? W[w + 2] : 0u;
+      uint64_t win = ((((uint64_t)a0 << 32) | a1) << sh) | (sh ? ((uint64_t)a2 >> (32 - sh)) : 0ull);
+      uint32_t used = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      uint32_t q = 0;
-      bool done = lbad;
-      while (!done) {
-        if (pos >= stop) { lbad = true; break; }
-        const uint32_t x = W[pos >> 5] << (pos & 31);
-        if (x) {
-          const uint32_t z = __clz(x);
-          q += z;
-          pos += z + 1;
-          done = true;
-        } else {
-          const uint32_t avail = 32u - (uint32_t)(pos & 31);
-          q += avail;
-          pos += avail;
-          if (q > qmax) { lbad = true; break; }
-        }
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t z = __clz((uint32_t)(win >> 32));   // 32 when no one is left: corrupt
+        sym[j] |= z << k;
+        win <<= (z + 1) & 63;
+        used += z + 1;
       }
-      if (q > qmax) lbad = true;
-      sym[j] |= q << k;
+      pos += used;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint32_t q = 0;
+        bool done = lbad;
+        while (!done) {
+          if (pos >= stop) { lbad = true; break; }
+          const uint32_t x = W[pos >> 5] << (pos & 31);
+          if (x) {
+            const uint32_t z = __clz(x);
+            q += z;
+            pos += z + 1;
+            done = true;
+          } else {
+            const uint32_t avail = 32u - (uint32_t)(pos & 31);
+            q += avail;
+            pos += avail;
+            if (q > qmax) { lbad = true; break; }
+          }
+        }
+        if (q > qmax) lbad = true;
+        sym[j] |= q << k;
+      }
     }
     if (!lbad && pos != stop) lbad = true;
   }
@@ -183,7 +205,7 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_
       unfold8<LAT>(sym + 8 * jj, k, v, &lbad);
       float u[8];
       if (a.dither) {
-        dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
+        dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + jj), u);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[i] = 0.0f;
@@ -210,8 +232,15 @@ decode_kernel(DecodeArgs a) {
   __shared__ uint32_t s_words[kDecStageWords];
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ uint32_t s_warp[kDecThreads / 32];
+  __shared__ float4 s_scale[kTile / 4];          // D_i * s_dec of the block's first segment
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
+  const int64_t seg0 = (g * kGroupTiles) / a.tiles_per_segment;
+  if (tid < kTile) {
+    const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 5));
+    reinterpret_cast<float *>(s_scale)[tid] =
+        __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
+  }
   float e[16];
   const bool ok = decode_lane<LAT, K>(a, g, e, s_words, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
@@ -220,12 +249,22 @@ decode_kernel(DecodeArgs a) {
   fwht128_x8(e, r);
   if (t >= a.n_tiles) return;
   if (ok) {
-    const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
-    const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
+    // x = D fl(z s_dec) = fl(z (D s_dec)): the sign commutes with rounding
+    if (t / a.tiles_per_segment == seg0) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float v = __fmul_rn(e[i], a.s_dec);
-      e[i] = __uint_as_float(__float_as_uint(v) ^ (((mw >> i) & 1u) << 31));
+      for (int c = 0; c < 4; ++c) {
+        const float4 sc = s_scale[4 * r + c];
+        e[4 * c] = __fmul_rn(e[4 * c], sc.x);
+        e[4 * c + 1] = __fmul_rn(e[4 * c + 1], sc.y);
+        e[4 * c + 2] = __fmul_rn(e[4 * c + 2], sc.z);
+        e[4 * c + 3] = __fmul_rn(e[4 * c + 3], sc.w);
+      }
+    } else {
+      const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
+      const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        e[i] = __fmul_rn(e[i], __uint_as_float(__float_as_uint(a.s_dec) ^ (((mw >> i) & 1u) << 31)));
     }
   }
   if (a.out_kind == HQ_OUT_F32) {
@@ -236,8 +275,10 @@ decode_kernel(DecodeArgs a) {
   } else {
     uint32_t w[8];
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
-      w[h] = (uint32_t)f32_to_bf16_rn(e[2 * h]) | ((uint32_t)f32_to_bf16_rn(e[2 * h + 1]) << 16);
+    for (int h = 0; h < 8; ++h) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(e[2 * h], e[2 * h + 1]);   // RNE
+      w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+    }
     uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + t * kTile + 16 * r);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);

@@ -20,33 +20,42 @@ constexpr float kMagic2 = 25165824.0f;           // 1.5 * 2^24: round to even in
 // ---------------------------------------------------------------- Philox4x32-10
 // Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
 // (SC'11): 10 rounds of the 4x32 bijection with multipliers D2511F53 and
-// CD9E8D57 and Weyl key increments 9E3779B9 and BB67AE85.
-__device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
+// CD9E8D57 and Weyl key increments 9E3779B9 and BB67AE85.  Each half-round
+// product is one 32x32->64 multiply.
+template <class Keys>
+__device__ __forceinline__ uint4 philox10(uint4 c, const Keys &key) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
+    const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key.k0[r], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ key.k1[r], (uint32_t)p0);
   }
   return c;
 }
 
 constexpr uint32_t kDitherTag = 0x44495448u;   // 'DITH'
 
-// 16-bit uniform b_i (i = 0..7) of one 8-coordinate group, as the float b + 1/2.
-__device__ __forceinline__ void dither_halves(uint64_t seed, uint64_t tile, uint32_t j,
-                                              float b[8]) {
-  uint4 w = philox10(make_uint4((uint32_t)tile, (uint32_t)(tile >> 32), j, kDitherTag),
-                     (uint32_t)seed, (uint32_t)(seed >> 32));
-  uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    b[2 * m] = __fadd_rn((float)(ws[m] & 0xFFFFu), 0.5f);
-    b[2 * m + 1] = __fadd_rn((float)(ws[m] >> 16), 0.5f);
-  }
+// The four Philox words of 8-coordinate group j of a tile: coordinate 2m
+// takes the low half of word m, coordinate 2m+1 the high half.
+template <class Keys>
+__device__ __forceinline__ uint4 dither_words(const Keys &key, uint64_t tile, uint32_t j) {
+  return philox10(make_uint4((uint32_t)tile, (uint32_t)(tile >> 32), j, kDitherTag), key);
 }
+// 1 + b 2^-16 for the 16-bit value b in the low / high half of w (exact).
+__device__ __forceinline__ float grid_lo(uint32_t w) {
+  return __uint_as_float(((w << 7) & 0x007FFF80u) | 0x3F800000u);
+}
+__device__ __forceinline__ float grid_hi(uint32_t w) {
+  return __uint_as_float(((w >> 9) & 0x007FFF80u) | 0x3F800000u);
+}
+// With f = 1 + b 2^-16 these give the grid midpoints exactly:
+//   -1   + (b + 1/2) 2^-15 = 2f + (-3 + 2^-16)
+//   -2   + (b + 1/2) 2^-14 = 4f + (-6 + 2^-15)
+//   -1/2 + (b + 1/2) 2^-16 =  f + (-3/2 + 2^-17)
+constexpr float kGrid15 = -3.0f + 0x1p-16f;
+constexpr float kGrid14 = -6.0f + 0x1p-15f;
+constexpr float kGrid16 = -1.5f + 0x1p-17f;
 
 // ---------------------------------------------------------------- FWHT-128
 // Unnormalised Walsh-Hadamard transform, natural (Sylvester) order, stages
@@ -107,64 +116,6 @@ __device__ __forceinline__ int32_t unzigzag(uint32_t m) {
   return (int32_t)(m >> 1) ^ -(int32_t)(m & 1u);
 }
 
-// Nearest point of 2E8 = 2D8 u (2D8 + 1) (Method 2): the even-coset point is
-// built from F = 2 rint(y/2), the odd one from F + sign(e); the nearer is
-// chosen by the exact identity
-//   d^2(odd) - d^2(even) = (8 - 4pA) - 2 S + 4 pB min|e| + 4 pA max|e|
-// evaluated in fp32 in a fixed order (S summed left to right).  The result is
-// returned as the coset flag `odd` plus, per coordinate, the even-coset half
-// k_i = F_i / 2, the error sign neg_i and the index of the one moved
-// coordinate (jfix, or -1).
-struct E8Point {
-  int32_t k[8];      // F_i / 2
-  uint32_t neg;      // bit i: e_i negative (sign bit set)
-  int jfix;          // coordinate moved by the parity fix of the chosen coset, or -1
-  bool odd;          // chosen coset is 2D8 + 1
-};
-
-__device__ __forceinline__ E8Point nearest_e8(const float y[8]) {
-  E8Point r;
-  float a[8];
-  uint32_t par = 0, neg = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float T = __fadd_rn(y[i], kMagic2);
-    float F = __fsub_rn(T, kMagic2);
-    float e = __fsub_rn(y[i], F);
-    a[i] = fabsf(e);
-    r.k[i] = (int32_t)(fbits(T) - fbits(kMagic2));
-    par ^= fbits(T);
-    neg |= (fbits(e) >> 31) << i;
-  }
-  uint32_t pA = par & 1u;
-  uint32_t pB = pA ^ (__popc(neg) & 1u);
-  float S = a[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) S = __fadd_rn(S, a[i]);
-  int jA = 0, jB = 0;
-  float mx = a[0], mn = a[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    if (a[i] > mx) { mx = a[i]; jA = i; }
-    if (a[i] < mn) { mn = a[i]; jB = i; }
-  }
-  float D = __fmaf_rn(-2.0f, S, pA ? 4.0f : 8.0f);
-  if (pB) D = __fmaf_rn(4.0f, mn, D);
-  if (pA) D = __fmaf_rn(4.0f, mx, D);
-  r.odd = D < 0.0f;
-  r.neg = neg;
-  r.jfix = r.odd ? (pB ? jB : -1) : (pA ? jA : -1);
-  return r;
-}
-
-// Lattice point (integers) of an E8Point.
-__device__ __forceinline__ int32_t e8_coord(const E8Point &p, int i) {
-  int32_t F = 2 * p.k[i];
-  int s = ((p.neg >> i) & 1u) ? -1 : 1;
-  if (p.odd) return (i == p.jfix) ? F - s : F + s;
-  return (i == p.jfix) ? F + 2 * s : F;
-}
-
 // D4 = {v : sum v even} (Conway & Sloane's D_n rule).
 __device__ __forceinline__ void nearest_d4(const float y[4], int32_t v[4]) {
   float a[4];
@@ -196,35 +147,85 @@ __device__ __forceinline__ int32_t nearest_z(float y) {
 }
 
 // ---------------------------------------------------------------- dither
+// a * sign(e): the sign bit of e flips a (e is never zero here).
+__device__ __forceinline__ float mulsign(float a, float e) {
+  return __uint_as_float(__float_as_uint(a) ^ (__float_as_uint(e) & 0x80000000u));
+}
+
 // U ~ Uniform(V(Lambda)) for the 8 coordinates of group j of a tile (Method 4):
 // a grid point u0 of a box that tiles space by the lattice, minus Q(u0).
-template <int LAT>
-__device__ __forceinline__ void dither8(uint64_t seed, uint64_t tile, uint32_t j, float u[8]) {
-  float b[8];
-  dither_halves(seed, tile, j, b);
+// The boxes are centred, so Q(u0) needs the general rounding on one
+// coordinate per vector only; the rest of the nearest-point rule is the same
+// as nearest_e8 / nearest_d4 (largest-error / smallest-error coordinate,
+// first index among equals, the odd E8 coset only when strictly nearer).
+template <int LAT, class Keys>
+__device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t j, float u[8]) {
+  const uint4 w4 = dither_words(key, tile, j);
+  const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
   if (LAT == 8) {
-    float u0[8];
+    float e[8];
 #pragma unroll
-    for (int i = 0; i < 7; ++i) u0[i] = __fadd_rn(-1.0f, __fmul_rn(b[i], 0x1p-15f));
-    u0[7] = __fadd_rn(-2.0f, __fmul_rn(b[7], 0x1p-14f));
-    E8Point p = nearest_e8(u0);
+    for (int m = 0; m < 3; ++m) {
+      e[2 * m] = __fmaf_rn(grid_lo(w[m]), 2.0f, kGrid15);
+      e[2 * m + 1] = __fmaf_rn(grid_hi(w[m]), 2.0f, kGrid15);
+    }
+    e[6] = __fmaf_rn(grid_lo(w[3]), 2.0f, kGrid15);
+    const float u07 = __fmaf_rn(grid_hi(w[3]), 4.0f, kGrid14);   // in (-2, 2)
+    // coordinates 0..6 lie in (-1, 1): nearest even integer 0, error = u0
+    const float T7 = __fadd_rn(u07, kMagic2);
+    const float F7 = __fsub_rn(T7, kMagic2);
+    e[7] = __fsub_rn(u07, F7);
+    uint32_t sx = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) u[i] = __fsub_rn(u0[i], (float)e8_coord(p, i));
+    for (int i = 0; i < 8; ++i) sx ^= __float_as_uint(e[i]);
+    const uint32_t pA = __float_as_uint(T7) & 1u;          // parity of F7 / 2
+    const uint32_t pB = pA ^ (sx >> 31);
+    float S = fabsf(e[0]), mx = fabsf(e[0]), mn = fabsf(e[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      const float ai = fabsf(e[i]);
+      S = __fadd_rn(S, ai);
+      mx = fmaxf(mx, ai);
+      mn = fminf(mn, ai);
+    }
+    float D = __fmaf_rn(-2.0f, S, pA ? 4.0f : 8.0f);
+    if (pB) D = __fmaf_rn(4.0f, mn, D);
+    if (pA) D = __fmaf_rn(4.0f, mx, D);
+    const bool odd = D < 0.0f;
+    const float m = odd ? mn : mx;
+    bool open = odd ? (pB != 0u) : (pA != 0u);   // a parity fix is still to place
+    const float wb = odd ? 1.0f : 0.0f, wh = odd ? -1.0f : 2.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool hit = open && fabsf(e[i]) == m;
+      open = open && !hit;
+      u[i] = __fsub_rn(e[i], mulsign(hit ? wh : wb, e[i]));
+    }
   } else if (LAT == 4) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float u0[4];
-      int32_t lam[4];
+      float e[4];
+      e[0] = __fadd_rn(grid_lo(w[2 * h]), kGrid16);
+      e[1] = __fadd_rn(grid_hi(w[2 * h]), kGrid16);
+      e[2] = __fadd_rn(grid_lo(w[2 * h + 1]), kGrid16);
+      const float u03 = __fmaf_rn(grid_hi(w[2 * h + 1]), 2.0f, kGrid15);   // in (-1, 1)
+      const float T3 = __fadd_rn(u03, kMagic1);
+      e[3] = __fsub_rn(u03, __fsub_rn(T3, kMagic1));
+      bool open = (__float_as_uint(T3) & 1u) != 0u;   // odd sum: move the worst coordinate
+      const float mx = fmaxf(fmaxf(fabsf(e[0]), fabsf(e[1])), fmaxf(fabsf(e[2]), fabsf(e[3])));
 #pragma unroll
-      for (int i = 0; i < 3; ++i) u0[i] = __fadd_rn(-0.5f, __fmul_rn(b[4 * h + i], 0x1p-16f));
-      u0[3] = __fadd_rn(-1.0f, __fmul_rn(b[4 * h + 3], 0x1p-15f));
-      nearest_d4(u0, lam);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) u[4 * h + i] = __fsub_rn(u0[i], (float)lam[i]);
+      for (int i = 0; i < 4; ++i) {
+        const bool hit = open && fabsf(e[i]) == mx;
+        open = open && !hit;
+        u[4 * h + i] = hit ? __fsub_rn(e[i], mulsign(1.0f, e[i])) : e[i];
+      }
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) u[i] = __fadd_rn(-0.5f, __fmul_rn(b[i], 0x1p-16f));
+    for (int m = 0; m < 4; ++m) {
+      u[2 * m] = __fadd_rn(grid_lo(w[m]), kGrid16);
+      u[2 * m + 1] = __fadd_rn(grid_hi(w[m]), kGrid16);
+    }
   }
 }
 
@@ -235,23 +236,61 @@ __device__ __forceinline__ void dither8(uint64_t seed, uint64_t tile, uint32_t j
 template <int LAT>
 __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) {
   if (LAT == 8) {
-    E8Point p = nearest_e8(y);
-    int32_t w[8];
+    // nearest point of 2E8 (nearest_e8 rule), kept as floats v_i = F_i + c_i
+    float F[8], e[8];
+    uint32_t par = 0, sx = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      int32_t ng = (int32_t)((p.neg >> i) & 1u);
-      int32_t fix = (i == p.jfix) ? 1 : 0;
-      // even coset: w = k (+ sign at the fixed coordinate); odd: w = k - neg
-      // (k - 1 + neg at the fixed coordinate).
-      w[i] = p.odd ? (fix ? p.k[i] - 1 + ng : p.k[i] - ng)
-                   : (fix ? p.k[i] + 1 - 2 * ng : p.k[i]);
+      const float T = __fadd_rn(y[i], kMagic2);
+      F[i] = __fsub_rn(T, kMagic2);
+      e[i] = __fsub_rn(y[i], F[i]);
+      par ^= __float_as_uint(T);
+      sx ^= __float_as_uint(e[i]);
     }
-    uint32_t pc = p.odd ? 1u : 0u;
-    int32_t r = (w[0] + w[1] + w[2] + w[3] + w[4] + w[5] + w[6]) & 1;
-    int32_t t = (w[7] - r) >> 1;
+    const uint32_t pA = par & 1u, pB = pA ^ (sx >> 31);
+    float S = fabsf(e[0]), mx = fabsf(e[0]), mn = fabsf(e[0]);
 #pragma unroll
-    for (int i = 0; i < 7; ++i) s[i] = 2u * zigzag(w[i]) + pc;
-    s[7] = 4u * zigzag(t) + 2u * (uint32_t)r + pc;
+    for (int i = 1; i < 8; ++i) {
+      const float ai = fabsf(e[i]);
+      S = __fadd_rn(S, ai);
+      mx = fmaxf(mx, ai);
+      mn = fminf(mn, ai);
+    }
+    float D = __fmaf_rn(-2.0f, S, pA ? 4.0f : 8.0f);
+    if (pB) D = __fmaf_rn(4.0f, mn, D);
+    if (pA) D = __fmaf_rn(4.0f, mx, D);
+    const bool odd = D < 0.0f;
+    const float m = odd ? mn : mx;
+    bool open = odd ? (pB != 0u) : (pA != 0u);
+    // even coset: c = 0, the fixed coordinate +2 sign(e); odd: c = sign(e),
+    // the fixed coordinate -sign(e) (an error of -0 counts as negative)
+    const float wb = odd ? 1.0f : 0.0f, wh = odd ? -1.0f : 2.0f;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool hit = open && fabsf(e[i]) == m;
+      open = open && !hit;
+      const float c = __uint_as_float(__float_as_uint(hit ? wh : wb) ^
+                                      (__float_as_uint(e[i]) & 0x80000000u));
+      v[i] = __fadd_rn(F[i], c);
+    }
+    // fold (p = coset): s_i = 2Z(w_i) + p with w_i = (v_i - p)/2 and
+    // 2Z(w) = |4w + 1| - 1, i.e. s_i = |2 v_i + 1 - 2p| - 1 + p (exact in fp32);
+    // r = parity of sum_{i<7} w_i, s_7 = |2 v_7 - 2p - 4r + 2| - 2 + 2r + p.
+    const float p = odd ? 1.0f : 0.0f;
+    const float c1 = odd ? -1.0f : 1.0f;             // 1 - 2p
+    const float cs = odd ? kMagic1 : kMagic1 - 1.0f; // p - 1 + magic
+    float sum7 = v[0];
+#pragma unroll
+    for (int i = 1; i < 7; ++i) sum7 = __fadd_rn(sum7, v[i]);
+    const float half = __fmaf_rn(sum7, 0.5f, odd ? -3.5f : 0.0f);     // (sum7 - 7p) / 2
+    const uint32_t r = __float_as_uint(__fadd_rn(half, kMagic1)) & 1u;
+#pragma unroll
+    for (int i = 0; i < 7; ++i)
+      s[i] = __float_as_uint(__fadd_rn(fabsf(__fmaf_rn(2.0f, v[i], c1)), cs)) - 0x4B400000u;
+    const float rf = r ? 1.0f : 0.0f;
+    const float a7 = fabsf(__fmaf_rn(2.0f, v[7], __fmaf_rn(-4.0f, rf, 2.0f - 2.0f * p)));
+    s[7] = __float_as_uint(__fadd_rn(a7, __fmaf_rn(2.0f, rf, p - 2.0f + kMagic1))) - 0x4B400000u;
   } else if (LAT == 4) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

@@ -36,41 +36,51 @@ __device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
   return v;
 }
 
-// Exclusive prefix (in words) of block `blk`, whose own total is `agg`.
-// Returns false when a wait ran out or a predecessor was poisoned.
-__device__ bool lookback(uint64_t *state, uint32_t blk, uint64_t agg, uint32_t spins,
-                         uint64_t *excl_out) {
-  if (blk == 0) {
-    st_release(state, kFlagPrefix | agg);
-    *excl_out = 0;
-    return true;
-  }
-  st_release(state + blk, kFlagAgg | agg);
+// Decoupled look-back, split in two so that a block publishes its own total
+// as early as possible and waits for its predecessors as late as possible.
+__device__ __forceinline__ void publish_total(uint64_t *state, uint32_t blk, uint64_t agg) {
+  st_release(state + blk, (blk == 0 ? kFlagPrefix : kFlagAgg) | agg);
+}
+
+// Exclusive prefix (in words) of block `blk`, whose own total is `agg`, read
+// by one full warp: each poll looks at 32 predecessors at once, sums the
+// totals back to the nearest one whose inclusive prefix is known, and repeats
+// further back when none is.  Every wait is bounded by `spins` polls; a block
+// that runs out, or sees a poisoned predecessor, poisons itself and returns
+// false.  Lane 0 returns the prefix.
+__device__ bool lookback_warp(uint64_t *state, uint32_t blk, uint64_t agg, uint32_t spins,
+                              uint64_t *excl_out) {
+  const int lane = threadIdx.x & 31;
   uint64_t excl = 0;
-  int64_t p = (int64_t)blk - 1;
+  bool ok = true;
+  int64_t p = (int64_t)blk - 1;                       // newest predecessor not yet summed
   while (p >= 0) {
-    uint64_t s;
+    const int64_t q = p - lane;
+    uint64_t s = kFlagPrefix;                         // before block 0: prefix 0
     uint32_t n = 0;
     for (;;) {
-      s = ld_acquire(state + p);
-      if (s >> 62) break;
-      if (++n > spins) {
-        st_release(state + blk, kFlagPoison);
-        return false;
-      }
+      if (q >= 0) s = ld_acquire(state + q);
+      const uint32_t waiting = __ballot_sync(0xffffffffu, (s >> 62) == 0);
+      if (waiting == 0u) break;
+      if (++n > spins) { ok = false; break; }
       __nanosleep(n < 64 ? 32 : 256);
     }
-    if ((s & ~kValueMask) == kFlagPoison) {
-      st_release(state + blk, kFlagPoison);
-      return false;
-    }
-    excl += s & kValueMask;
-    if ((s & ~kValueMask) == kFlagPrefix) break;
-    --p;
+    if (!ok) break;
+    if (__ballot_sync(0xffffffffu, (s & ~kValueMask) == kFlagPoison)) { ok = false; break; }
+    const uint32_t pre = __ballot_sync(0xffffffffu, (s & ~kValueMask) == kFlagPrefix);
+    const int first = pre ? __ffs(pre) - 1 : 32;      // nearest predecessor with a prefix
+    uint64_t v = lane <= first ? (s & kValueMask) : 0ull;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    excl += v;
+    if (pre) break;
+    p -= 32;
   }
-  st_release(state + blk, kFlagPrefix | ((excl + agg) & kValueMask));
-  *excl_out = excl;
-  return true;
+  if (lane == 0) {
+    st_release(state + blk, ok ? (kFlagPrefix | ((excl + agg) & kValueMask)) : kFlagPoison);
+    *excl_out = excl;
+  }
+  return ok;
 }
 
 // MSB-first bit writer into the shared-memory window [lo, lo + kStageWords)
@@ -125,6 +135,15 @@ __device__ __forceinline__ uint64_t r_bits_of(const uint32_t s[8]) {
   return acc;
 }
 
+// Unary codes of 8 symbols one by one (codes longer than 32 bits in total).
+__device__ __noinline__ void put_unary_slow(BitOut *o, uint4 qa, uint4 qb) {
+  const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+  for (int i = 0; i < 8; ++i) {
+    o->zeros(q[i]);
+    o->put(1u, 1);
+  }
+}
+
 // Unary codes (q zeros then a one) of one 8-group.
 template <int K>
 __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int kk) {
@@ -142,12 +161,23 @@ __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int k
   const uint32_t L = T + 1u;
   if (L <= 32u) {
     o.put(__brev(pat) >> (32u - L), (int)L);
-  } else {
-#pragma unroll 1
+  } else if (L <= 64u) {
+    // the same positions in a 64-bit pattern (bit_at returns 0 past 31)
+    uint32_t lo = 0, hi = 0, P = 0;
+#pragma unroll
     for (int i = 0; i < 8; ++i) {
-      o.zeros(q[i]);
-      o.put(1u, 1);
+      P += q[i];
+      lo |= bit_at(P);
+      hi |= bit_at(P - 32u);
+      P += 1u;
     }
+    const uint64_t msb_first = ((uint64_t)__brev(lo) << 32 | __brev(hi)) >> (64u - L);
+    if (L > 32u) o.put((uint32_t)(msb_first >> 32), (int)L - 32);
+    o.put((uint32_t)msb_first, 32);
+  } else {
+    BitOut tmp = o;               // only the copy's address escapes: o stays in registers
+    put_unary_slow(&tmp, make_uint4(q[0], q[1], q[2], q[3]), make_uint4(q[4], q[5], q[6], q[7]));
+    o = tmp;
   }
 }
 
@@ -160,6 +190,8 @@ encode_kernel(EncodeArgs a) {
   __shared__ uint64_t s_base, s_words;
   __shared__ uint32_t s_ticket, s_flags;
   __shared__ int s_ok;
+  __shared__ uint4 s_signx[kTile / 8];          // sign XOR words of the first segment
+
 
   const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
   uint64_t *state = reinterpret_cast<uint64_t *>(a.ws) + 1;
@@ -167,6 +199,8 @@ encode_kernel(EncodeArgs a) {
     s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
     s_flags = 0u;
   }
+#pragma unroll
+  for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
   __syncthreads();
   const uint32_t g = s_ticket;                   // this block's group
   if (g >= a.n_blocks) return;                   // only with a pre-filled ticket
@@ -175,20 +209,35 @@ encode_kernel(EncodeArgs a) {
   const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
   const int64_t t = t0 + tl;
   const bool valid = tl < nt;
+  // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
+  const int64_t seg0 = t0 / a.tiles_per_segment;
+  if (tid < kTile / 2) {
+    const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
+    reinterpret_cast<uint32_t *>(s_signx)[tid] =
+        (((mword >> (2 * (tid & 15))) & 3u) * 0x40008000u) & 0x80008000u;
+  }
+  __syncthreads();
 
   // ---- load 16 bf16 coordinates, sign mask, FWHT
   float x[16];
   if (valid) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
     const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-    const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
-    const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
+    uint32_t sw[8];
+    if (t / a.tiles_per_segment == seg0) {
+      const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
+      sw[0] = s0.x; sw[1] = s0.y; sw[2] = s0.z; sw[3] = s0.w;
+      sw[4] = s1.x; sw[5] = s1.y; sw[6] = s1.z; sw[7] = s1.w;
+    } else {
+      const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
+      const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sw[q] = (((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u;
+    }
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of the pair
-      const uint32_t sw = (((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u;
-      const uint32_t ww = w[q] ^ sw;
+      const uint32_t ww = w[q] ^ sw[q];
       x[2 * q] = __uint_as_float(ww << 16);
       x[2 * q + 1] = __uint_as_float(ww & 0xFFFF0000u);
     }
@@ -205,7 +254,7 @@ encode_kernel(EncodeArgs a) {
   for (int jj = 0; jj < 2; ++jj) {
     float u[8];
     if (a.dither) {
-      dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
+      dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + jj), u);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) u[i] = 0.0f;
@@ -224,7 +273,7 @@ encode_kernel(EncodeArgs a) {
     for (int jj = 0; jj < 2; ++jj) {
       float u[8];
       if (a.dither) {
-        dither8<LAT>(a.dither_seed, gt, (uint32_t)(2 * r + jj), u);
+        dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + jj), u);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[i] = 0.0f;
@@ -254,7 +303,7 @@ encode_kernel(EncodeArgs a) {
   if (r == 7) s_tile_u[tl] = incl;
   __syncthreads();
 
-  // ---- group layout, index, look-back (warp 0)
+  // ---- group layout (warp 0): tile offsets, group total, published at once
   const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
   if (tid < 32) {
     const uint64_t tu = s_tile_u[tid];
@@ -265,37 +314,43 @@ encode_kernel(EncodeArgs a) {
       if (lane >= d) ui += o;
     }
     s_tile_uoff[tid] = ui - tu;
-    const uint64_t total = __shfl_sync(0xffffffffu, ui, 31);
+    const uint64_t words = ((uint64_t)nt * R + __shfl_sync(0xffffffffu, ui, 31) + 31) >> 5;
     if (tid == 0) {
-      const uint64_t words = ((uint64_t)nt * R + total + 31) >> 5;
-      uint64_t excl = 0;
-      const bool ok = lookback(state, g, words, a.spins, &excl);
-      if (!ok) atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
-      s_ok = ok ? 1 : 0;
-      s_base = excl;
       s_words = words;
-      if (ok) {
-        a.offsets[g] = excl;
-        if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + words;
-        if (excl + words > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
-      }
+      publish_total(state, g, words);
     }
   }
   __syncthreads();
-  if (!s_ok) return;
-  if (tid == 0 && s_flags) atomicOr(a.status, s_flags);
-  if (a.stream == nullptr) return;
-  const uint64_t base = s_base, gwords = s_words;
-
-  // ---- bits: R-section of this lane's two vectors, then its unary codes
+  const uint64_t gwords = s_words;
   const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
   const int64_t r_pos = (int64_t)tl * (int64_t)R + (int64_t)r * 2 * rb8;
   const int64_t u_pos = (int64_t)nt * (int64_t)R + (int64_t)s_tile_uoff[tl] + u_in_tile;
-  for (int64_t cb = 0; cb < (int64_t)gwords; cb += kStageWords) {
-#pragma unroll
-    for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
-    __syncthreads();
-    if (valid) {
+  const bool one_window = gwords <= (uint64_t)kStageWords;
+
+  // ---- warp 0 waits for the predecessors while the other warps assemble
+  if (tid < 32) {
+    uint64_t excl = 0;
+    const bool ok = lookback_warp(state, g, gwords, a.spins, &excl);
+    if (tid == 0) {
+      s_ok = ok ? 1 : 0;
+      s_base = excl;
+      if (!ok) {
+        atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
+      } else {
+        a.offsets[g] = excl;
+        if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + gwords;
+        if (excl + gwords > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
+        if (s_flags) atomicOr(a.status, s_flags);
+      }
+    }
+  }
+  for (int64_t cb = 0; cb < (int64_t)gwords || cb == 0; cb += kStageWords) {
+    if (!one_window) {                          // rare: groups beyond 16 KiB
+      __syncthreads();
+      for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
+      __syncthreads();
+    }
+    if (valid && a.stream != nullptr) {
       BitOut o;
       if (rb8 > 0) {
         o.begin(s_stage, cb, r_pos);
@@ -323,12 +378,14 @@ encode_kernel(EncodeArgs a) {
       o.finish();
     }
     __syncthreads();
+    if (!s_ok || a.stream == nullptr) return;
+    const uint64_t base = s_base;
     const int64_t nw = min((int64_t)kStageWords, (int64_t)gwords - cb);
     for (int i = tid; i < nw; i += kEncThreads) {
       const uint64_t gw = base + (uint64_t)(cb + i);
       if (gw < a.cap_words) a.stream[gw] = s_stage[i];
     }
-    __syncthreads();
+    if (one_window) break;
   }
 }
 

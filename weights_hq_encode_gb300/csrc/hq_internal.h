@@ -10,6 +10,13 @@
 
 namespace hq {
 
+// Philox4x32-10 round keys of the dither seed (round r uses key + r * Weyl),
+// precomputed on the host so the kernels read them from the parameter bank.
+struct PhiloxKeys {
+  uint32_t k0[10];
+  uint32_t k1[10];
+};
+
 struct EncodeArgs {
   const uint16_t *x;
   int64_t n_tiles;
@@ -24,6 +31,7 @@ struct EncodeArgs {
   int64_t tiles_per_segment;
   uint64_t tile_base;
   uint64_t dither_seed;
+  PhiloxKeys keys;
   float s_enc;
   int rice_k;
   int rbits;
@@ -44,6 +52,7 @@ struct DecodeArgs {
   int64_t tiles_per_segment;
   uint64_t tile_base;
   uint64_t dither_seed;
+  PhiloxKeys keys;
   float s_dec;
   int rice_k;
   int rbits;
