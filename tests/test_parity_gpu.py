@@ -73,6 +73,8 @@ CASES = [
     (8, 2, 2.5, 1, 129, 4, 123456789),
     (8, 5, 40.0, 1, 300, 1, 0),
     (8, 1, 0.05, 1, 70, 1, 0),
+    (8, 0, 300.0, 1, 40, 1, 0),       # groups far beyond the encoder's shared staging
+    (8, 2, 60.0, 0, 520, 2, 3),       # several blocks of 4 groups, ragged tail
     (4, 0, 0.8, 1, 65, 2, 0),
     (4, 1, 1.3, 1, 200, 1, 7),
     (4, 3, 6.0, 0, 31, 1, 0),

@@ -27,57 +27,80 @@ constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] word
 constexpr uint64_t kFlagPoison = 3ull << 62;
 constexpr uint64_t kValueMask = (1ull << 62) - 1;
 
-__device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// The look-back state word packs a flag and a value into one 64-bit word
+// that is written and read whole; nothing else is published through it, so
+// relaxed GPU-scope accesses are enough (and polls do not order each other).
+__device__ __forceinline__ void st_state(uint64_t *p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
+__device__ __forceinline__ uint64_t ld_state(const uint64_t *p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 // Decoupled look-back, split in two so that a block publishes its own total
 // as early as possible and waits for its predecessors as late as possible.
 __device__ __forceinline__ void publish_total(uint64_t *state, uint32_t blk, uint64_t agg) {
-  st_release(state + blk, (blk == 0 ? kFlagPrefix : kFlagAgg) | agg);
+  st_state(state + blk, (blk == 0 ? kFlagPrefix : kFlagAgg) | agg);
 }
 
 // Exclusive prefix (in words) of block `blk`, whose own total is `agg`, read
-// by one full warp: each poll looks at 32 predecessors at once, sums the
-// totals back to the nearest one whose inclusive prefix is known, and repeats
-// further back when none is.  Every wait is bounded by `spins` polls; a block
-// that runs out, or sees a poisoned predecessor, poisons itself and returns
-// false.  Lane 0 returns the prefix.
+// by one full warp.  Each poll loads 32 * kPer predecessors (lane l holds
+// distances kPer*l+1 .. kPer*l+kPer), finds the nearest one whose inclusive prefix is known and
+// sums the totals up to it; when a closer predecessor has published nothing
+// yet the poll is repeated, and when no prefix is in the window the next
+// window is read (kPer = 1 measured fastest).  Every wait is bounded by `spins` polls; a block that runs out, or
+// meets a poisoned predecessor, poisons itself and returns false.  Lane 0
+// publishes the block's own prefix and returns it.
 __device__ bool lookback_warp(uint64_t *state, uint32_t blk, uint64_t agg, uint32_t spins,
                               uint64_t *excl_out) {
+  constexpr int kPer = 1;
   const int lane = threadIdx.x & 31;
   uint64_t excl = 0;
   bool ok = true;
-  int64_t p = (int64_t)blk - 1;                       // newest predecessor not yet summed
+  int64_t p = (int64_t)blk - 1;                       // nearest predecessor not yet summed
+  uint32_t n = 0;
   while (p >= 0) {
-    const int64_t q = p - lane;
-    uint64_t s = kFlagPrefix;                         // before block 0: prefix 0
-    uint32_t n = 0;
-    for (;;) {
-      if (q >= 0) s = ld_acquire(state + q);
-      const uint32_t waiting = __ballot_sync(0xffffffffu, (s >> 62) == 0);
-      if (waiting == 0u) break;
+    uint64_t v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int64_t q = p - (int64_t)(kPer * lane + i);
+      v[i] = q >= 0 ? ld_state(state + q) : kFlagPrefix;   // before block 0: prefix 0
+    }
+    // first prefix and first unpublished/poisoned entry of this lane, in distance order
+    int first_p = kPer, first_bad = kPer;
+    bool poison = false;
+#pragma unroll
+    for (int i = kPer - 1; i >= 0; --i) {
+      const uint64_t f = v[i] & ~kValueMask;
+      if (f == kFlagPrefix) first_p = i;
+      if (f == 0 || f == kFlagPoison) first_bad = i;
+      if (f == kFlagPoison) poison = true;
+    }
+    const uint32_t has_p = __ballot_sync(0xffffffffu, first_p < kPer);
+    const int pl = has_p ? __ffs(has_p) - 1 : 32;             // lane of the nearest prefix
+    // a gap (unpublished or poisoned) closer than the nearest prefix blocks progress
+    const bool gap = (lane < pl && first_bad < kPer) || (lane == pl && first_bad < first_p);
+    const uint32_t gaps = __ballot_sync(0xffffffffu, gap);
+    if (gaps) {
+      if (__ballot_sync(0xffffffffu, gap && poison)) { ok = false; break; }
       if (++n > spins) { ok = false; break; }
       __nanosleep(n < 64 ? 32 : 256);
+      continue;
     }
-    if (!ok) break;
-    if (__ballot_sync(0xffffffffu, (s & ~kValueMask) == kFlagPoison)) { ok = false; break; }
-    const uint32_t pre = __ballot_sync(0xffffffffu, (s & ~kValueMask) == kFlagPrefix);
-    const int first = pre ? __ffs(pre) - 1 : 32;      // nearest predecessor with a prefix
-    uint64_t v = lane <= first ? (s & kValueMask) : 0ull;
+    uint64_t sum = 0;
 #pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-    excl += v;
-    if (pre) break;
-    p -= 32;
+    for (int i = 0; i < kPer; ++i)
+      if (lane < pl || (lane == pl && i <= first_p)) sum += v[i] & kValueMask;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    excl += sum;
+    if (has_p) break;
+    p -= 32 * kPer;
   }
   if (lane == 0) {
-    st_release(state + blk, ok ? (kFlagPrefix | ((excl + agg) & kValueMask)) : kFlagPoison);
+    st_state(state + blk, ok ? (kFlagPrefix | ((excl + agg) & kValueMask)) : kFlagPoison);
     *excl_out = excl;
   }
   return ok;
