@@ -1,10 +1,9 @@
 // hq_decode.cu -- decoder and fused score kernel of the HyperQuant tile codec.
 //
 // A block of 256 threads decodes one index group of 32 tiles; lane r of a
-// tile handles symbols 16r .. 16r+15 (two 8-vectors).  The block stages the
-// group's words in shared memory, then finds where every lane's unary codes
-// start by a block-wide popcount scan of the U-area (every one bit there ends
-// a symbol: 16 per lane).  Each lane reads its remainders at their fixed
+// tile handles symbols 16r .. 16r+15 (two 8-vectors).  The block finds where
+// every lane's unary codes start by a block-wide popcount scan of the U-area
+// (every one bit there ends a symbol: 16 per lane).  Each lane reads its remainders at their fixed
 // position and its unary codes with count-leading-zeros, restores the
 // stripped bits, regenerates the dither and inverts the transform
 // (HyperQuant summary, Method 1-4 in reverse); outputs are stored with
@@ -25,7 +24,6 @@
 namespace hq {
 
 constexpr int kDecThreads = 256;
-constexpr int kDecStageWords = 4096;       // groups up to 16 KiB are read from shared memory
 
 // nb (1..64) bits starting at bit `pos` of W, MSB-first, right-aligned.
 __device__ __forceinline__ uint64_t read_bits(const uint32_t *W, uint64_t pos, int nb) {
@@ -40,43 +38,30 @@ __device__ __forceinline__ uint64_t read_bits(const uint32_t *W, uint64_t pos, i
   return nb >= 64 ? v : (v >> (64 - nb));
 }
 
-// MSB-first position (0..31) of the n-th (1-based) set bit of x.
+// MSB-first position (0..31) of the n-th (1-based, n <= popc(x)) set bit of
+// x: a branch-free binary search on population counts.
 __device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
-  for (int i = 1; i < n; ++i) x &= ~(0x80000000u >> __clz(x));
-  return __clz(x);
+  int p = 0;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const int c = __popc(x >> (32 - w));        // ones among the top w bits
+    const bool skip = c < n;
+    n -= skip ? c : 0;
+    x = skip ? (x << w) : x;
+    p += skip ? w : 0;
+  }
+  return p;
 }
 
-// Block-wide exclusive sum of v over 256 threads; *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t *s_warp,
-                                                   uint32_t *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  uint32_t before = 0, all = 0;
-#pragma unroll
-  for (int i = 0; i < kDecThreads / 32; ++i) {
-    const uint32_t ws = s_warp[i];
-    if (i < warp) before += ws;
-    all += ws;
-  }
-  __syncthreads();
-  *total = all;
-  return before + incl - v;
-}
-
-// Stages group g, finds every lane's unary start, parses this lane's 16
-// symbols and returns e = v - u for them (lattice domain).  The return value
-// is block-uniform: false when the group is corrupt (e is then all zeros).
+// Finds where every lane's unary codes start, parses this lane's 16 symbols
+// and returns e = v - u for them (lattice domain).  The group's words are read
+// straight from global memory (each is read by the scan first, so the parse
+// hits L1).  The return value is block-uniform: false when the group is
+// corrupt (e is then all zeros).
 template <int LAT, int K>
-__device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_t *s_words,
-                            uint64_t *s_start, uint32_t *s_warp) {
-  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+__device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_t *s_start,
+                            uint32_t (*s_warp)[kDecThreads / 32]) {
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7, lane = tid & 31, warp = tid >> 5;
   const int k = K >= 0 ? K : a.rice_k;
   const int64_t t0 = g * kGroupTiles;
   const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
@@ -86,32 +71,47 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_
   const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
   const uint64_t ustart = (uint64_t)nt * R;
   if (ustart > nwords * 32) bad = true;
-  const bool staged = nwords <= (uint64_t)kDecStageWords;
-  const uint32_t *W = staged ? s_words : a.stream + base;
-  if (!bad && staged)
-    for (uint64_t i = tid; i < nwords; i += kDecThreads) s_words[i] = __ldg(a.stream + base + i);
-  if (tid == 0) s_start[0] = ustart;
-  __syncthreads();
+  const uint32_t *W = a.stream + base;
 
-  // ---- unary starts: the 16m-th one of the U-area ends lane m-1's codes
+  // ---- unary starts: the 16m-th one of the U-area ends lane m-1's codes.
+  // One word per thread per window; a warp scan plus one barrier per window.
   const uint64_t want = 128ull * (uint64_t)nt;
   uint64_t ones = 0;
   if (!bad) {
+    int par = 0;
     for (uint64_t wb = ustart >> 5; wb < nwords; wb += kDecThreads) {
       const uint64_t w = wb + tid;
-      uint32_t word = w < nwords ? W[w] : 0u;
+      uint32_t word = w < nwords ? __ldg(W + w) : 0u;
       if (w == (ustart >> 5)) word &= 0xFFFFFFFFu >> (ustart & 31);
       const uint32_t pc = __popc(word);
-      uint32_t total;
-      const uint64_t before = ones + block_excl_sum(pc, s_warp, &total);
-      uint64_t m = (before / 16 + 1) * 16;
-      while (m <= before + pc && m <= want) {
-        s_start[m / 16] = w * 32 + (uint64_t)nth_set_bit_msb(word, (int)(m - before)) + 1;
+      uint32_t incl = pc;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      if (lane == 31) s_warp[par][warp] = incl;
+      __syncthreads();
+      uint32_t before_w = 0, total = 0;
+#pragma unroll
+      for (int i = 0; i < kDecThreads / 32; ++i) {
+        const uint32_t ws = s_warp[par][i];
+        before_w += i < warp ? ws : 0u;
+        total += ws;
+      }
+      const uint64_t before = ones + before_w + incl - pc;
+      uint64_t m = (before / 16 + 1) * 16;       // at most two boundaries per word
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        if (m <= before + pc && m <= want)
+          s_start[m / 16] = w * 32 + (uint64_t)nth_set_bit_msb(word, (int)(m - before)) + 1;
         m += 16;
       }
       ones += total;
+      par ^= 1;
     }
   }
+  if (tid == 0) s_start[0] = ustart;
   __syncthreads();
   if (!bad && (ones != want || ((s_start[8 * nt] + 31) >> 5) != nwords)) bad = true;
 
@@ -147,53 +147,45 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_
       }
       rpos += (uint64_t)rb8;
     }
-    // unary codes: a 64-bit window from the lane's start holds all 16 codes
-    // whenever they total at most 64 bits (the common case); longer sections
-    // take the word-by-word path
-    uint64_t pos = s_start[tid];
-    const uint64_t stop = s_start[tid + 1];
+    // unary codes from a 64-bit window refilled one word at a time; a run of
+    // 32 or more zeros (a quotient >= 32) takes the counting loop
+    const uint64_t pos = s_start[tid], stop = s_start[tid + 1];
     const uint32_t qmax = (kSymbolLimit - 1u) >> k;
-    if (stop - pos <= 64 && stop >= pos) {
-      const uint64_t w = pos >> 5;
-      const int sh = (int)(pos & 31);
-      const uint32_t a0 = W[w];
-      const uint32_t a1 = w + 1 < nwords ? W[w + 1] : 0u;
-      const uint32_t a2 = w + 2 < nwords ? W[w + 2] : 0u;
-      uint64_t win = ((((uint64_t)a0 << 32) | a1) << sh) | (sh ? ((uint64_t)a2 >> (32 - sh)) : 0ull);
-      uint32_t used = 0;
+    uint64_t nextw = (pos >> 5) + 2;
+    const uint32_t a0 = (pos >> 5) < nwords ? __ldg(W + (pos >> 5)) : 0u;
+    const uint32_t a1 = (pos >> 5) + 1 < nwords ? __ldg(W + (pos >> 5) + 1) : 0u;
+    const int sh = (int)(pos & 31);
+    uint64_t win = ((((uint64_t)a0) << 32) | a1) << sh;
+    int avail = 64 - sh;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t z = __clz((uint32_t)(win >> 32));   // 32 when no one is left: corrupt
-        sym[j] |= z << k;
-        win <<= (z + 1) & 63;
-        used += z + 1;
+    for (int j = 0; j < 16; ++j) {
+      if (avail < 32) {
+        const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
+        win |= (uint64_t)nw << (32 - avail);
+        avail += 32;
+        ++nextw;
       }
-      pos += used;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t q = 0;
-        bool done = lbad;
-        while (!done) {
-          if (pos >= stop) { lbad = true; break; }
-          const uint32_t x = W[pos >> 5] << (pos & 31);
-          if (x) {
-            const uint32_t z = __clz(x);
-            q += z;
-            pos += z + 1;
-            done = true;
-          } else {
-            const uint32_t avail = 32u - (uint32_t)(pos & 31);
-            q += avail;
-            pos += avail;
-            if (q > qmax) { lbad = true; break; }
-          }
-        }
-        if (q > qmax) lbad = true;
-        sym[j] |= q << k;
+      uint32_t z = __clz((uint32_t)(win >> 32));
+      uint32_t q = 0;
+      while (z == 32u) {                          // rare: a long run of zeros
+        q += 32u;
+        win <<= 32;
+        avail -= 32;
+        const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
+        win |= (uint64_t)nw << (32 - avail);
+        avail += 32;
+        ++nextw;
+        if (q > qmax || nextw > nwords + 2) { lbad = true; z = 0u; break; }
+        z = __clz((uint32_t)(win >> 32));
       }
+      q += z;
+      if (q > qmax) lbad = true;
+      sym[j] |= q << k;
+      win <<= z + 1;
+      avail -= (int)z + 1;
     }
-    if (!lbad && pos != stop) lbad = true;
+    const uint64_t consumed_end = nextw * 32 - (uint64_t)avail;   // bit after the last code
+    if (!lbad && consumed_end != stop) lbad = true;
   }
 
   // ---- restore stripped bits, subtract the dither
@@ -227,11 +219,10 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint32_
 }
 
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 8)
 decode_kernel(DecodeArgs a) {
-  __shared__ uint32_t s_words[kDecStageWords];
   __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ uint32_t s_warp[kDecThreads / 32];
+  __shared__ uint32_t s_warp[2][kDecThreads / 32];
   __shared__ float4 s_scale[kTile / 4];          // D_i * s_dec of the block's first segment
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
@@ -242,7 +233,7 @@ decode_kernel(DecodeArgs a) {
         __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
   }
   float e[16];
-  const bool ok = decode_lane<LAT, K>(a, g, e, s_words, s_start, s_warp);
+  const bool ok = decode_lane<LAT, K>(a, g, e, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
   if (!ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
   // the transform runs on every lane of the block (shuffles need full warps)
@@ -308,15 +299,14 @@ __global__ void rotate_queries_kernel(QkArgs a) {
 // its tile; partial dots with 8 query rows at a time are reduced over the
 // tile's 8 lanes by a butterfly that leaves one finished row on each lane.
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 8)
 scores_kernel(QkArgs a) {
-  __shared__ uint32_t s_words[kDecStageWords];
   __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ uint32_t s_warp[kDecThreads / 32];
+  __shared__ uint32_t s_warp[2][kDecThreads / 32];
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
   float e[16];
-  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_words, s_start, s_warp);
+  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);
   if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
   const int64_t tile = g * kGroupTiles + tl;
   const bool valid = tile < a.dec.n_tiles;

@@ -205,7 +205,7 @@ __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int k
 }
 
 template <int LAT, int K>
-__global__ void __launch_bounds__(kEncThreads)
+__global__ void __launch_bounds__(kEncThreads, 6)
 encode_kernel(EncodeArgs a) {
   __shared__ uint32_t s_stage[kStageWords];
   __shared__ uint32_t s_tile_u[kGroupTiles];
