@@ -72,6 +72,7 @@ DecodeArgs make_decode_args(const hq_params *p, const uint32_t *stream, uint64_t
   a.status = status;
   a.signs = p->d_signs;
   a.tiles_per_segment = p->tiles_per_segment;
+  a.seg_shift = pow2_shift(p->tiles_per_segment);
   a.tile_base = p->tile_base;
   a.dither_seed = p->dither_seed;
   a.keys = round_keys(p->dither_seed);
@@ -124,6 +125,7 @@ int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t
   a.status = d_status;
   a.signs = p->d_signs;
   a.tiles_per_segment = p->tiles_per_segment;
+  a.seg_shift = pow2_shift(p->tiles_per_segment);
   a.tile_base = p->tile_base;
   a.dither_seed = p->dither_seed;
   a.keys = round_keys(p->dither_seed);
@@ -179,6 +181,7 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
   a.dec.out_kind = -1;
   a.n_kv = n_kv_heads;
   a.n_tokens = n_tokens;
+  a.tok_shift = pow2_shift(n_tokens);
   a.q = d_q;
   a.B = B;
   a.Hq = Hq;

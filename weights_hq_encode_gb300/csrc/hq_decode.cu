@@ -56,31 +56,29 @@ __device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
 // Finds where every lane's unary codes start, parses this lane's 16 symbols
 // and returns e = v - u for them (lattice domain).  The group's words are read
 // straight from global memory (each is read by the scan first, so the parse
-// hits L1).  The return value is block-uniform: false when the group is
-// corrupt (e is then all zeros).
-template <int LAT, int K>
-__device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_t *s_start,
-                            uint32_t (*s_warp)[kDecThreads / 32]) {
+// hits L1).  Bit positions within the group have type P: 32-bit for groups
+// below 2^31 bits (every group of a sane stream), 64-bit otherwise.  The
+// return value is block-uniform: false when the group is corrupt (e is then
+// all zeros).
+template <int LAT, int K, class P>
+__device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, int nt,
+                                              const uint32_t *W, P nwords, bool bad,
+                                              float e[16], P *s_start,
+                                              uint32_t (*s_warp)[kDecThreads / 32]) {
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7, lane = tid & 31, warp = tid >> 5;
   const int k = K >= 0 ? K : a.rice_k;
-  const int64_t t0 = g * kGroupTiles;
-  const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
-  const uint64_t base = a.offsets[g], end = a.offsets[g + 1];
-  bool bad = end < base || end > a.stream_words;
-  const uint64_t nwords = bad ? 0 : end - base;
-  const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
-  const uint64_t ustart = (uint64_t)nt * R;
+  const P R = (P)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
+  const P ustart = (P)nt * R;
   if (ustart > nwords * 32) bad = true;
-  const uint32_t *W = a.stream + base;
 
   // ---- unary starts: the 16m-th one of the U-area ends lane m-1's codes.
   // One word per thread per window; a warp scan plus one barrier per window.
-  const uint64_t want = 128ull * (uint64_t)nt;
-  uint64_t ones = 0;
+  const P want = (P)128 * (P)nt;
+  P ones = 0;
   if (!bad) {
     int par = 0;
-    for (uint64_t wb = ustart >> 5; wb < nwords; wb += kDecThreads) {
-      const uint64_t w = wb + tid;
+    for (P wb = ustart >> 5; wb < nwords; wb += kDecThreads) {
+      const P w = wb + (P)tid;
       uint32_t word = w < nwords ? __ldg(W + w) : 0u;
       if (w == (ustart >> 5)) word &= 0xFFFFFFFFu >> (ustart & 31);
       const uint32_t pc = __popc(word);
@@ -99,12 +97,12 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_
         before_w += i < warp ? ws : 0u;
         total += ws;
       }
-      const uint64_t before = ones + before_w + incl - pc;
-      uint64_t m = (before / 16 + 1) * 16;       // at most two boundaries per word
+      const P before = ones + (P)(before_w + incl - pc);
+      P m = (before / 16 + 1) * 16;               // at most two boundaries per word
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
         if (m <= before + pc && m <= want)
-          s_start[m / 16] = w * 32 + (uint64_t)nth_set_bit_msb(word, (int)(m - before)) + 1;
+          s_start[m / 16] = w * 32 + (P)nth_set_bit_msb(word, (int)(m - before)) + 1;
         m += 16;
       }
       ones += total;
@@ -121,12 +119,12 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_
   const bool valid = tl < nt;
   if (!bad && valid) {
     const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
-    uint64_t rpos = (uint64_t)tl * R + (uint64_t)r * 2 * rb8;
+    P rpos = (P)tl * R + (P)(r * 2 * rb8);
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       if (K >= 0) {
         constexpr int KK = K >= 0 ? K : 0;
-        const uint64_t rv = rb8 > 0 ? read_bits(W, rpos, rb8) : 0ull;
+        const uint64_t rv = rb8 > 0 ? read_bits(W, (uint64_t)rpos, rb8) : 0ull;
         int off = rb8;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -136,22 +134,22 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_
           sym[8 * jj + c] = nb > 0 ? (uint32_t)((rv >> off) & ((1ull << nb) - 1ull)) << lowb : 0u;
         }
       } else {
-        uint64_t p = rpos;
+        P q = rpos;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int lowb = stripped_low_bits<LAT>(c, k);
           const int nb = k - lowb;
-          sym[8 * jj + c] = nb > 0 ? (uint32_t)read_bits(W, p, nb) << lowb : 0u;
-          p += (uint64_t)(nb > 0 ? nb : 0);
+          sym[8 * jj + c] = nb > 0 ? (uint32_t)read_bits(W, (uint64_t)q, nb) << lowb : 0u;
+          q += (P)(nb > 0 ? nb : 0);
         }
       }
-      rpos += (uint64_t)rb8;
+      rpos += (P)rb8;
     }
     // unary codes from a 64-bit window refilled one word at a time; a run of
     // 32 or more zeros (a quotient >= 32) takes the counting loop
-    const uint64_t pos = s_start[tid], stop = s_start[tid + 1];
+    const P pos = s_start[tid], stop = s_start[tid + 1];
     const uint32_t qmax = (kSymbolLimit - 1u) >> k;
-    uint64_t nextw = (pos >> 5) + 2;
+    P nextw = (pos >> 5) + 2;
     const uint32_t a0 = (pos >> 5) < nwords ? __ldg(W + (pos >> 5)) : 0u;
     const uint32_t a1 = (pos >> 5) + 1 < nwords ? __ldg(W + (pos >> 5) + 1) : 0u;
     const int sh = (int)(pos & 31);
@@ -184,13 +182,12 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_
       win <<= z + 1;
       avail -= (int)z + 1;
     }
-    const uint64_t consumed_end = nextw * 32 - (uint64_t)avail;   // bit after the last code
-    if (!lbad && consumed_end != stop) lbad = true;
+    if (!lbad && nextw * 32 - (P)avail != stop) lbad = true;   // bit after the last code
   }
 
   // ---- restore stripped bits, subtract the dither
   if (!bad && valid && !lbad) {
-    const uint64_t gt = a.tile_base + (uint64_t)(t0 + tl);
+    const uint64_t gt = a.tile_base + (uint64_t)(g * kGroupTiles + tl);
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       int32_t v[8];
@@ -218,6 +215,24 @@ __device__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16], uint64_
   return !any_bad;
 }
 
+// Dispatch on the group's size: 32-bit bit positions unless the group holds
+// 2^31 bits or more.
+template <int LAT, int K>
+__device__ __forceinline__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16],
+                                            uint64_t *s_start64,
+                                            uint32_t (*s_warp)[kDecThreads / 32]) {
+  const int64_t t0 = g * kGroupTiles;
+  const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
+  const uint64_t base = a.offsets[g], end = a.offsets[g + 1];
+  const bool bad = end < base || end > a.stream_words;
+  const uint64_t nwords = bad ? 0 : end - base;
+  const uint32_t *W = a.stream + (bad ? 0 : base);
+  if (nwords < (1ull << 26))
+    return decode_lane_p<LAT, K, uint32_t>(a, g, nt, W, (uint32_t)nwords, bad, e,
+                                           reinterpret_cast<uint32_t *>(s_start64), s_warp);
+  return decode_lane_p<LAT, K, uint64_t>(a, g, nt, W, nwords, bad, e, s_start64, s_warp);
+}
+
 template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads, 8)
 decode_kernel(DecodeArgs a) {
@@ -226,7 +241,7 @@ decode_kernel(DecodeArgs a) {
   __shared__ float4 s_scale[kTile / 4];          // D_i * s_dec of the block's first segment
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
-  const int64_t seg0 = (g * kGroupTiles) / a.tiles_per_segment;
+  const int64_t seg0 = div_by(g * kGroupTiles, a.tiles_per_segment, a.seg_shift);
   if (tid < kTile) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 5));
     reinterpret_cast<float *>(s_scale)[tid] =
@@ -241,7 +256,7 @@ decode_kernel(DecodeArgs a) {
   if (t >= a.n_tiles) return;
   if (ok) {
     // x = D fl(z s_dec) = fl(z (D s_dec)): the sign commutes with rounding
-    if (t / a.tiles_per_segment == seg0) {
+    if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float4 sc = s_scale[4 * r + c];
@@ -251,7 +266,7 @@ decode_kernel(DecodeArgs a) {
         e[4 * c + 3] = __fmul_rn(e[4 * c + 3], sc.w);
       }
     } else {
-      const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
+      const uint32_t *mask = a.signs + 4 * (div_by(t, a.tiles_per_segment, a.seg_shift));
       const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
 #pragma unroll
       for (int i = 0; i < 16; ++i)
@@ -281,7 +296,7 @@ __global__ void rotate_queries_kernel(QkArgs a) {
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= a.B * a.Hq) return;
   const int hq = row % a.Hq, h = hq / (a.Hq / a.n_kv);
-  const int64_t seg = ((int64_t)h * a.n_tokens) / a.dec.tiles_per_segment;
+  const int64_t seg = div_by((int64_t)h * a.n_tokens, a.dec.tiles_per_segment, a.dec.seg_shift);
   const uint32_t *mask = a.dec.signs + 4 * seg;
   float x[128];
   const uint16_t *q = a.q + (int64_t)row * kTile;
@@ -310,7 +325,7 @@ scores_kernel(QkArgs a) {
   if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
   const int64_t tile = g * kGroupTiles + tl;
   const bool valid = tile < a.dec.n_tiles;
-  const int h = valid ? (int)(tile / a.n_tokens) : 0;
+  const int h = valid ? (int)div_by(tile, a.n_tokens, a.tok_shift) : 0;
   const int64_t tok = valid ? tile - (int64_t)h * a.n_tokens : 0;
   const int G = a.Hq / a.n_kv;
   const int rows = a.B * G;                     // query rows that read this head

@@ -233,7 +233,7 @@ encode_kernel(EncodeArgs a) {
   const int64_t t = t0 + tl;
   const bool valid = tl < nt;
   // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
-  const int64_t seg0 = t0 / a.tiles_per_segment;
+  const int64_t seg0 = div_by(t0, a.tiles_per_segment, a.seg_shift);
   if (tid < kTile / 2) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
     reinterpret_cast<uint32_t *>(s_signx)[tid] =
@@ -247,12 +247,12 @@ encode_kernel(EncodeArgs a) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
     const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
     uint32_t sw[8];
-    if (t / a.tiles_per_segment == seg0) {
+    if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
       const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
       sw[0] = s0.x; sw[1] = s0.y; sw[2] = s0.z; sw[3] = s0.w;
       sw[4] = s1.x; sw[5] = s1.y; sw[6] = s1.z; sw[7] = s1.w;
     } else {
-      const uint32_t *mask = a.signs + 4 * (t / a.tiles_per_segment);
+      const uint32_t *mask = a.signs + 4 * (div_by(t, a.tiles_per_segment, a.seg_shift));
       const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
 #pragma unroll
       for (int q = 0; q < 8; ++q) sw[q] = (((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u;

@@ -29,6 +29,7 @@ struct EncodeArgs {
   uint32_t *status;
   const uint32_t *signs;
   int64_t tiles_per_segment;
+  int seg_shift;            // log2(tiles_per_segment) when a power of two, else -1
   uint64_t tile_base;
   uint64_t dither_seed;
   PhiloxKeys keys;
@@ -50,6 +51,7 @@ struct DecodeArgs {
   uint32_t *status;
   const uint32_t *signs;
   int64_t tiles_per_segment;
+  int seg_shift;            // log2(tiles_per_segment) when a power of two, else -1
   uint64_t tile_base;
   uint64_t dither_seed;
   PhiloxKeys keys;
@@ -63,11 +65,23 @@ struct QkArgs {
   DecodeArgs dec;           // K stream
   int n_kv;
   int64_t n_tokens;
+  int tok_shift;            // log2(n_tokens) when a power of two, else -1
   const uint16_t *q;        // [B][Hq][128] bf16
   int B, Hq;
   float *qrot;              // [B][Hq][128] fp32 workspace: s_dec * H * D_h * q
   float *scores;            // [B][Hq][n_tokens]
 };
+
+// Segment (or head) of tile t: a shift when the divisor is a power of two.
+__host__ __device__ __forceinline__ int64_t div_by(int64_t t, int64_t d, int shift) {
+  return shift >= 0 ? (t >> shift) : t / d;
+}
+__host__ __device__ __forceinline__ int pow2_shift(int64_t d) {
+  if (d <= 0 || (d & (d - 1)) != 0) return -1;
+  int s = 0;
+  while ((1ll << s) < d) ++s;
+  return s;
+}
 
 int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st);
 int encode_tiles_per_block();
