@@ -313,43 +313,73 @@ __global__ void rotate_queries_kernel(QkArgs a) {
 // Scores of one group of K tiles.  Lane r holds 16 lattice-domain values of
 // its tile; partial dots with 8 query rows at a time are reduced over the
 // tile's 8 lanes by a butterfly that leaves one finished row on each lane.
+// The rotated query rows of the head of the group's first tile are staged in
+// shared memory, laid out [row][lane r][16 + 4] so that the 8 lanes of a tile
+// read distinct banks; tiles of another head read their rows from global.
+constexpr int kQkRowsSmem = 64;
+constexpr int kQkLaneStride = 20;                // 16 values + 4 floats of padding
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 8)
+__global__ void __launch_bounds__(kDecThreads, 3)
 scores_kernel(QkArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ uint32_t s_warp[2][kDecThreads / 32];
+  __shared__ __align__(16) float s_q[kQkRowsSmem * 8 * kQkLaneStride];
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
+  const int G = a.Hq / a.n_kv;
+  const int rows = a.B * G;                     // query rows that read one head
+  const int h0 = (int)div_by(g * kGroupTiles, a.n_tokens, a.tok_shift);
+  const bool staged = rows <= kQkRowsSmem;
+  if (staged) {
+    for (int i = tid; i < rows * 32; i += kDecThreads) {   // float4 units
+      const int rr = i >> 5, c4 = i & 31;                   // row, 4-float chunk
+      const int b = rr / G, gq = rr - b * G;
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(
+          a.qrot + ((int64_t)b * a.Hq + (int64_t)h0 * G + gq) * kTile) + c4);
+      const int rl = c4 >> 2, cc = (c4 & 3) * 4;
+      *reinterpret_cast<float4 *>(&s_q[(rr * 8 + rl) * kQkLaneStride + cc]) = v;
+    }
+  }
   float e[16];
-  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);
+  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);   // barriers inside
   if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
   const int64_t tile = g * kGroupTiles + tl;
   const bool valid = tile < a.dec.n_tiles;
-  const int h = valid ? (int)div_by(tile, a.n_tokens, a.tok_shift) : 0;
+  const int h = valid ? (int)div_by(tile, a.n_tokens, a.tok_shift) : h0;
   const int64_t tok = valid ? tile - (int64_t)h * a.n_tokens : 0;
-  const int G = a.Hq / a.n_kv;
-  const int rows = a.B * G;                     // query rows that read this head
+  const bool from_smem = staged && h == h0;
   for (int r0 = 0; r0 < rows; r0 += 8) {
     float p[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int rr = r0 + i;
-      p[i] = 0.0f;
+      float acc = 0.0f;
       if (rr < rows) {
-        const int b = rr / G, gq = rr - b * G;
-        const float4 *qr = reinterpret_cast<const float4 *>(
-            a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile + 16 * r);
-        float acc = 0.0f;
+        if (from_smem) {
+          const float4 *qr = reinterpret_cast<const float4 *>(&s_q[(rr * 8 + r) * kQkLaneStride]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 qv = __ldg(qr + c);
-          acc = __fmaf_rn(qv.x, e[4 * c], acc);
-          acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
-          acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
-          acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
+          for (int c = 0; c < 4; ++c) {
+            const float4 qv = qr[c];
+            acc = __fmaf_rn(qv.x, e[4 * c], acc);
+            acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
+            acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
+            acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
+          }
+        } else {
+          const int b = rr / G, gq = rr - b * G;
+          const float4 *qr = reinterpret_cast<const float4 *>(
+              a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile + 16 * r);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 qv = __ldg(qr + c);
+            acc = __fmaf_rn(qv.x, e[4 * c], acc);
+            acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
+            acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
+            acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
+          }
         }
-        p[i] = acc;
       }
+      p[i] = acc;
     }
     // reduce-scatter over the 8 lanes: after the step with mask m a lane keeps
     // the half of its slots whose bit m matches its own lane bit
