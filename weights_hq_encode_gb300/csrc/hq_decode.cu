@@ -53,6 +53,58 @@ __device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
   return p;
 }
 
+
+// Quotients of the 16 unary codes from bit pos to stop in the general case: a
+// 64-bit window refilled one word at a time, and a counting loop for runs of
+// 32 zeros or more.  Out of line: lanes take it only when their codes span
+// more than 64 bits or hold a quotient of 32 or more.
+struct Quot16 {
+  uint32_t q[16];
+  bool bad;
+};
+
+template <class P>
+__device__ __noinline__ Quot16 unary_general(const uint32_t *W, P pos, P stop, P nwords, int k) {
+  Quot16 out;
+  out.bad = false;
+  const uint32_t qmax = (kSymbolLimit - 1u) >> k;
+  const P pw = pos >> 5;
+  const uint32_t a0 = pw < nwords ? __ldg(W + pw) : 0u;
+  const uint32_t a1 = pw + 1 < nwords ? __ldg(W + pw + 1) : 0u;
+  P nextw = pw + 2;
+  const int sh = (int)(pos & 31);
+  uint64_t win = ((((uint64_t)a0) << 32) | a1) << sh;
+  int avail = 64 - sh;
+  for (int j = 0; j < 16; ++j) {
+    if (avail < 32) {
+      const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
+      win |= (uint64_t)nw << (32 - avail);
+      avail += 32;
+      ++nextw;
+    }
+    uint32_t z = __clz((uint32_t)(win >> 32));
+    uint32_t q = 0;
+    while (z == 32u) {                            // a run of 32 zeros or more
+      q += 32u;
+      win <<= 32;
+      avail -= 32;
+      const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
+      win |= (uint64_t)nw << (32 - avail);
+      avail += 32;
+      ++nextw;
+      if (q > qmax || nextw > nwords + 2) { out.bad = true; z = 0u; break; }
+      z = __clz((uint32_t)(win >> 32));
+    }
+    q += z;
+    if (q > qmax) out.bad = true;
+    out.q[j] = q;
+    win <<= z + 1;
+    avail -= (int)z + 1;
+  }
+  if (!out.bad && nextw * 32 - (P)avail != stop) out.bad = true;   // bit after the last code
+  return out;
+}
+
 // Finds where every lane's unary codes start, parses this lane's 16 symbols
 // and returns e = v - u for them (lattice domain).  The group's words are read
 // straight from global memory (each is read by the scan first, so the parse
@@ -145,44 +197,42 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
       }
       rpos += (P)rb8;
     }
-    // unary codes from a 64-bit window refilled one word at a time; a run of
-    // 32 or more zeros (a quotient >= 32) takes the counting loop
     const P pos = s_start[tid], stop = s_start[tid + 1];
-    const uint32_t qmax = (kSymbolLimit - 1u) >> k;
-    P nextw = (pos >> 5) + 2;
-    const uint32_t a0 = (pos >> 5) < nwords ? __ldg(W + (pos >> 5)) : 0u;
-    const uint32_t a1 = (pos >> 5) + 1 < nwords ? __ldg(W + (pos >> 5) + 1) : 0u;
+    const P pw = pos >> 5;
+    const uint32_t a0 = pw < nwords ? __ldg(W + pw) : 0u;
+    const uint32_t a1 = pw + 1 < nwords ? __ldg(W + pw + 1) : 0u;
     const int sh = (int)(pos & 31);
-    uint64_t win = ((((uint64_t)a0) << 32) | a1) << sh;
-    int avail = 64 - sh;
+    bool slow = stop - pos > (P)64;
+    if (!slow) {
+      // The lane's 16 codes (exactly 16 ones, the last at bit stop-1) lie in
+      // the 64 bits (hi:lo) from pos: each quotient is the count of zeros
+      // before the next one.  A quotient of 32 or more (hi all zeros) leaves
+      // bit 5 set in zo and the lane takes the general parser below; shorter
+      // quotients are below qmax for every k <= 15, and the 16th one ends at
+      // stop by construction of the boundaries.
+      const uint32_t a2 = pw + 2 < nwords ? __ldg(W + pw + 2) : 0u;
+      uint32_t hi = __funnelshift_l(a1, a0, sh), lo = __funnelshift_l(a2, a1, sh);
+      uint32_t zo = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (avail < 32) {
-        const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
-        win |= (uint64_t)nw << (32 - avail);
-        avail += 32;
-        ++nextw;
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t z = __clz(hi);
+        zo |= z;
+        sym[j] += z << k;                        // the low k bits hold the remainder
+        hi = __funnelshift_lc(lo, hi, z + 1u);
+        lo = shl_clamp(lo, z + 1u);
       }
-      uint32_t z = __clz((uint32_t)(win >> 32));
-      uint32_t q = 0;
-      while (z == 32u) {                          // rare: a long run of zeros
-        q += 32u;
-        win <<= 32;
-        avail -= 32;
-        const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
-        win |= (uint64_t)nw << (32 - avail);
-        avail += 32;
-        ++nextw;
-        if (q > qmax || nextw > nwords + 2) { lbad = true; z = 0u; break; }
-        z = __clz((uint32_t)(win >> 32));
+      if (zo & 32u) {
+        slow = true;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sym[j] &= (1u << k) - 1u;
       }
-      q += z;
-      if (q > qmax) lbad = true;
-      sym[j] |= q << k;
-      win <<= z + 1;
-      avail -= (int)z + 1;
     }
-    if (!lbad && nextw * 32 - (P)avail != stop) lbad = true;   // bit after the last code
+    if (slow) {
+      const Quot16 gq = unary_general<P>(W, pos, stop, nwords, k);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sym[j] |= gq.q[j] << k;
+      lbad |= gq.bad;
+    }
   }
 
   // ---- restore stripped bits, subtract the dither

@@ -107,6 +107,13 @@ __device__ __forceinline__ uint32_t bit_at(uint32_t n) {
   return r;
 }
 
+// x << n with the PTX rule for n >= 32 (the result is 0), unlike C's shift.
+__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t n) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(n));
+  return r;
+}
+
 // ---------------------------------------------------------------- lattices
 __device__ __forceinline__ uint32_t fbits(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ uint32_t zigzag(int32_t n) {
