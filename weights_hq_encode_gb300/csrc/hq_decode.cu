@@ -54,54 +54,46 @@ __device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
 }
 
 
-// Quotients of the 16 unary codes from bit pos to stop in the general case: a
-// 64-bit window refilled one word at a time, and a counting loop for runs of
-// 32 zeros or more.  Out of line: lanes take it only when their codes span
-// more than 64 bits or hold a quotient of 32 or more.
-struct Quot16 {
-  uint32_t q[16];
+// Quotients of 8 unary codes from bit pos in the general case (a code longer
+// than the lane's 64-bit window, or a quotient of 32 or more): one 32-bit view
+// per step, runs of zeros counted 32 at a time.  Lanes rarely take it (a
+// divergent branch).  next = the bit after the 8th code; bad = a quotient
+// above qmax or codes running past the group's last word.
+template <class P>
+struct Quot8 {
+  uint32_t q[8];
+  P next;
   bool bad;
 };
 
 template <class P>
-__device__ __noinline__ Quot16 unary_general(const uint32_t *W, P pos, P stop, P nwords, int k) {
-  Quot16 out;
+__device__ __forceinline__ Quot8<P> unary8_general(const uint32_t *W, P pos, P nwords, int k) {
+  Quot8<P> out;
   out.bad = false;
   const uint32_t qmax = (kSymbolLimit - 1u) >> k;
-  const P pw = pos >> 5;
-  const uint32_t a0 = pw < nwords ? __ldg(W + pw) : 0u;
-  const uint32_t a1 = pw + 1 < nwords ? __ldg(W + pw + 1) : 0u;
-  P nextw = pw + 2;
-  const int sh = (int)(pos & 31);
-  uint64_t win = ((((uint64_t)a0) << 32) | a1) << sh;
-  int avail = 64 - sh;
-  for (int j = 0; j < 16; ++j) {
-    if (avail < 32) {
-      const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
-      win |= (uint64_t)nw << (32 - avail);
-      avail += 32;
-      ++nextw;
-    }
-    uint32_t z = __clz((uint32_t)(win >> 32));
+  const P end = nwords * 32;
+  for (int j = 0; j < 8; ++j) out.q[j] = 0u;
+  for (int j = 0; j < 8 && !out.bad; ++j) {
     uint32_t q = 0;
-    while (z == 32u) {                            // a run of 32 zeros or more
-      q += 32u;
-      win <<= 32;
-      avail -= 32;
-      const uint32_t nw = nextw < nwords ? __ldg(W + nextw) : 0u;
-      win |= (uint64_t)nw << (32 - avail);
-      avail += 32;
-      ++nextw;
-      if (q > qmax || nextw > nwords + 2) { out.bad = true; z = 0u; break; }
-      z = __clz((uint32_t)(win >> 32));
+    for (;;) {
+      if (pos >= end || q > qmax) { out.bad = true; break; }
+      const P w = pos >> 5;
+      const uint32_t b0 = __ldg(W + w), b1 = w + 1 < nwords ? __ldg(W + w + 1) : 0u;
+      const uint32_t view = __funnelshift_l(b1, b0, (uint32_t)(pos & 31));
+      if (view == 0u) {                          // 32 more zeros of this code
+        q += 32u;
+        pos += 32;
+        continue;
+      }
+      const uint32_t z = __clz(view);
+      q += z;
+      pos += (P)(z + 1u);
+      break;
     }
-    q += z;
     if (q > qmax) out.bad = true;
     out.q[j] = q;
-    win <<= z + 1;
-    avail -= (int)z + 1;
   }
-  if (!out.bad && nextw * 32 - (P)avail != stop) out.bad = true;   // bit after the last code
+  out.next = pos;
   return out;
 }
 
@@ -165,83 +157,88 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
   __syncthreads();
   if (!bad && (ones != want || ((s_start[8 * nt] + 31) >> 5) != nwords)) bad = true;
 
-  // ---- this lane's symbols
-  uint32_t sym[16];
+  // ---- this lane's symbols: remainder bits first, then the quotients
   bool lbad = false;
   const bool valid = tl < nt;
+  const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
+  const P rpos = (P)tl * R + (P)(r * 2 * rb8);
+  uint64_t rv[2] = {0ull, 0ull};                 // remainder bits of each 8-group
+  uint32_t qp[4] = {0u, 0u, 0u, 0u};             // quotient j in byte j % 4 of qp[j / 4]
+  bool slow = false;
+  P pos = 0, stop = 0;
   if (!bad && valid) {
-    const int rb8 = K >= 0 ? rbits8<LAT>(K) : (int)(R / 16);
-    P rpos = (P)tl * R + (P)(r * 2 * rb8);
+    if (K >= 0 && rb8 > 0) {
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      if (K >= 0) {
-        constexpr int KK = K >= 0 ? K : 0;
-        const uint64_t rv = rb8 > 0 ? read_bits(W, (uint64_t)rpos, rb8) : 0ull;
-        int off = rb8;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int lowb = stripped_low_bits<LAT>(c, KK);
-          const int nb = KK - lowb;
-          off -= nb;
-          sym[8 * jj + c] = nb > 0 ? (uint32_t)((rv >> off) & ((1ull << nb) - 1ull)) << lowb : 0u;
-        }
-      } else {
-        P q = rpos;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int lowb = stripped_low_bits<LAT>(c, k);
-          const int nb = k - lowb;
-          sym[8 * jj + c] = nb > 0 ? (uint32_t)read_bits(W, (uint64_t)q, nb) << lowb : 0u;
-          q += (P)(nb > 0 ? nb : 0);
-        }
-      }
-      rpos += (P)rb8;
+      for (int jj = 0; jj < 2; ++jj) rv[jj] = read_bits(W, (uint64_t)(rpos + (P)(jj * rb8)), rb8);
     }
-    const P pos = s_start[tid], stop = s_start[tid + 1];
-    const P pw = pos >> 5;
-    const uint32_t a0 = pw < nwords ? __ldg(W + pw) : 0u;
-    const uint32_t a1 = pw + 1 < nwords ? __ldg(W + pw + 1) : 0u;
-    const int sh = (int)(pos & 31);
-    bool slow = stop - pos > (P)64;
+    pos = s_start[tid];
+    stop = s_start[tid + 1];
+    slow = stop - pos > (P)64;
     if (!slow) {
       // The lane's 16 codes (exactly 16 ones, the last at bit stop-1) lie in
       // the 64 bits (hi:lo) from pos: each quotient is the count of zeros
       // before the next one.  A quotient of 32 or more (hi all zeros) leaves
-      // bit 5 set in zo and the lane takes the general parser below; shorter
+      // bit 5 set in zo and the lane takes the general parser; shorter
       // quotients are below qmax for every k <= 15, and the 16th one ends at
       // stop by construction of the boundaries.
+      const P pw = pos >> 5;
+      const uint32_t a0 = pw < nwords ? __ldg(W + pw) : 0u;
+      const uint32_t a1 = pw + 1 < nwords ? __ldg(W + pw + 1) : 0u;
       const uint32_t a2 = pw + 2 < nwords ? __ldg(W + pw + 2) : 0u;
+      const uint32_t sh = (uint32_t)(pos & 31);
       uint32_t hi = __funnelshift_l(a1, a0, sh), lo = __funnelshift_l(a2, a1, sh);
       uint32_t zo = 0u;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const uint32_t z = __clz(hi);
         zo |= z;
-        sym[j] += z << k;                        // the low k bits hold the remainder
+        qp[j >> 2] += z << (8 * (j & 3));
         hi = __funnelshift_lc(lo, hi, z + 1u);
         lo = shl_clamp(lo, z + 1u);
       }
-      if (zo & 32u) {
-        slow = true;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sym[j] &= (1u << k) - 1u;
-      }
-    }
-    if (slow) {
-      const Quot16 gq = unary_general<P>(W, pos, stop, nwords, k);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sym[j] |= gq.q[j] << k;
-      lbad |= gq.bad;
+      slow = (zo & 32u) != 0u;
     }
   }
 
-  // ---- restore stripped bits, subtract the dither
-  if (!bad && valid && !lbad) {
+  // ---- symbols, restore stripped bits, subtract the dither
+  if (!bad && valid) {
     const uint64_t gt = a.tile_base + (uint64_t)(g * kGroupTiles + tl);
+    P posj = pos;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
+      uint32_t s8[8];
+      if (K >= 0) {
+        constexpr int KK = K >= 0 ? K : 0;
+        int off = rb8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int lowb = stripped_low_bits<LAT>(c, KK);
+          const int nb = KK - lowb;
+          off -= nb;
+          s8[c] = nb > 0 ? (uint32_t)((rv[jj] >> off) & ((1ull << nb) - 1ull)) << lowb : 0u;
+        }
+      } else {
+        P q = rpos + (P)(jj * rb8);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int lowb = stripped_low_bits<LAT>(c, k);
+          const int nb = k - lowb;
+          s8[c] = nb > 0 ? (uint32_t)read_bits(W, (uint64_t)q, nb) << lowb : 0u;
+          q += (P)(nb > 0 ? nb : 0);
+        }
+      }
+      if (!slow) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) s8[c] += ((qp[2 * jj + (c >> 2)] >> (8 * (c & 3))) & 0xFFu) << k;
+      } else {
+        const Quot8<P> g8 = unary8_general<P>(W, posj, nwords, k);
+        posj = g8.next;
+        lbad |= g8.bad;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) s8[c] += g8.q[c] << k;
+      }
       int32_t v[8];
-      unfold8<LAT>(sym + 8 * jj, k, v, &lbad);
+      unfold8<LAT>(s8, k, v, &lbad);
       float u[8];
       if (a.dither) {
         dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + jj), u);
@@ -256,6 +253,7 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
         e[8 * jj + i] = __fsub_rn(fv, u[i]);
       }
     }
+    if (slow && posj != stop) lbad = true;       // bit after the last code
   }
   const int any_bad = __syncthreads_or((bad || lbad) ? 1 : 0);
   if (any_bad || !valid) {

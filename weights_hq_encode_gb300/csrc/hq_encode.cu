@@ -144,6 +144,16 @@ struct BitOut {
   }
 };
 
+// OR nb (1..32) bits, right-aligned in v, into the shared-memory window at
+// bit position bp (MSB-first, window-relative); they touch at most two words.
+__device__ __forceinline__ void or_bits32(uint32_t *stage, uint32_t bp, uint32_t v, uint32_t nb) {
+  const uint32_t t = v << (32u - nb);            // left-aligned
+  const uint32_t o = bp & 31u;
+  const uint32_t hi = t >> o, lo = shl_clamp(t, 32u - o);
+  if (hi != 0u) atomicOr(stage + (bp >> 5), hi);
+  if (lo != 0u) atomicOr(stage + (bp >> 5) + 1, lo);
+}
+
 // Kept remainder bits of one 8-group of symbols, MSB-first, right-aligned
 // (rbits8<LAT>(K) bits, at most 64).
 template <int LAT, int K>
@@ -373,7 +383,30 @@ encode_kernel(EncodeArgs a) {
       for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
       __syncthreads();
     }
-    if (valid && a.stream != nullptr) {
+    // unary bits of each 8-group of the lane (q zeros then a one per code)
+    uint32_t la = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) la += (sym[i] >> k) + 1u;
+    if (K >= 0 && 2 * rb8 <= 32 && one_window && valid && a.stream != nullptr && la <= 32u &&
+        ubits - la <= 32u) {
+      // common case: window-relative positions (below 2^17), the remainder
+      // bits of the lane and each 8-group's unary codes in one 32-bit value
+      if (rb8 > 0) {
+        constexpr int KK = K >= 0 ? K : 0;
+        constexpr int RB = 2 * rbits8<LAT>(KK) <= 32 ? rbits8<LAT>(KK) : 0;
+        const uint32_t rv = ((uint32_t)r_bits_of<LAT, KK>(sym) << RB) |
+                            (uint32_t)r_bits_of<LAT, KK>(sym + 8);
+        or_bits32(s_stage, (uint32_t)r_pos, rv, (uint32_t)(2 * rb8));
+      }
+      uint32_t ua = 0u, ub = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ua = ((ua << (sym[i] >> k)) << 1) | 1u;
+        ub = ((ub << (sym[8 + i] >> k)) << 1) | 1u;
+      }
+      or_bits32(s_stage, (uint32_t)u_pos, ua, la);
+      or_bits32(s_stage, (uint32_t)u_pos + la, ub, ubits - la);
+    } else if (valid && a.stream != nullptr) {
       BitOut o;
       if (rb8 > 0) {
         o.begin(s_stage, cb, r_pos);
