@@ -123,31 +123,40 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
     int par = 0;
     for (P wb = ustart >> 5; wb < nwords; wb += kDecThreads) {
       const P w = wb + (P)tid;
-      uint32_t word = w < nwords ? __ldg(W + w) : 0u;
-      if (w == (ustart >> 5)) word &= 0xFFFFFFFFu >> (ustart & 31);
-      const uint32_t pc = __popc(word);
-      uint32_t incl = pc;
+      const bool wact = wb + (P)(warp * 32) < nwords;   // warp-uniform: any word to scan
+      uint32_t word = 0u, pc = 0u, incl = 0u;
+      if (wact) {
+        word = w < nwords ? __ldg(W + w) : 0u;
+        if (w == (ustart >> 5)) word &= 0xFFFFFFFFu >> (ustart & 31);
+        pc = __popc(word);
+        incl = pc;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += o;
+        }
       }
       if (lane == 31) s_warp[par][warp] = incl;
       __syncthreads();
+      static_assert(kDecThreads / 32 == 8, "two 16-byte reads of the warp totals");
+      const uint4 q0 = reinterpret_cast<const uint4 *>(s_warp[par])[0];
+      const uint4 q1 = reinterpret_cast<const uint4 *>(s_warp[par])[1];
+      const uint32_t ws[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
       uint32_t before_w = 0, total = 0;
 #pragma unroll
-      for (int i = 0; i < kDecThreads / 32; ++i) {
-        const uint32_t ws = s_warp[par][i];
-        before_w += i < warp ? ws : 0u;
-        total += ws;
+      for (int i = 0; i < 8; ++i) {
+        before_w += i < warp ? ws[i] : 0u;
+        total += ws[i];
       }
-      const P before = ones + (P)(before_w + incl - pc);
-      P m = (before / 16 + 1) * 16;               // at most two boundaries per word
+      if (wact) {
+        const P before = ones + (P)(before_w + incl - pc);
+        P m = (before / 16 + 1) * 16;             // at most two boundaries per word
 #pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        if (m <= before + pc && m <= want)
-          s_start[m / 16] = w * 32 + (P)nth_set_bit_msb(word, (int)(m - before)) + 1;
-        m += 16;
+        for (int rep = 0; rep < 2; ++rep) {
+          if (m <= before + pc && m <= want)
+            s_start[m / 16] = w * 32 + (P)nth_set_bit_msb(word, (int)(m - before)) + 1;
+          m += 16;
+        }
       }
       ones += total;
       par ^= 1;
@@ -285,7 +294,7 @@ template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads, 8)
 decode_kernel(DecodeArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ uint32_t s_warp[2][kDecThreads / 32];
+  __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
   __shared__ float4 s_scale[kTile / 4];          // D_i * s_dec of the block's first segment
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
@@ -370,7 +379,7 @@ template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads, 3)
 scores_kernel(QkArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ uint32_t s_warp[2][kDecThreads / 32];
+  __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
   __shared__ __align__(16) float s_q[kQkRowsSmem * 8 * kQkLaneStride];
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
