@@ -16,8 +16,9 @@
  * Conventions for every entry point:
  *   - All pointers named d_* are device pointers (CUDA global memory); the
  *     caller allocates, owns and frees every buffer.  The library allocates
- *     nothing, never synchronises the stream, and keeps no state between
- *     calls, so calls on different streams are independent.
+ *     nothing and keeps no state between calls, so calls on different
+ *     streams are independent.  Every entry point is asynchronous except
+ *     hq_calibrate, a host loop that reads each rate back.
  *   - The return value reports synchronous errors only: HQ_ERR_INVALID for a
  *     bad argument (nothing is launched), HQ_ERR_CUDA for a failed launch.
  *   - Data-dependent errors are OR-ed into *d_status (a device uint32 the
@@ -123,6 +124,48 @@ size_t hq_encode_workspace_bytes(int64_t n_tiles);
 int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
               uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
               uint32_t *d_status, hq_stream_t stream);
+
+/* Payload size of an encode without writing it (Method 3: the realized rate
+ * counts Rice bits, the kept remainder bits and the unary codes of every
+ * symbol; group padding and the index are not payload).  Runs the encoder in
+ * size mode over the same tiles and adds their payload bits to *d_bits.
+ *   d_bits     device uint64, 8-byte aligned; the caller zeroes it (calls
+ *              accumulate).
+ *   d_ws       as for hq_encode; d_status OR-ed with HQ_ERR_{TIMEOUT,RANGE}.
+ * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
+int hq_payload_bits(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint64_t *d_bits,
+                    void *d_ws, size_t ws_bytes, uint32_t *d_status, hq_stream_t stream);
+
+/* Result of hq_calibrate. */
+typedef struct hq_calibration {
+  float alpha;        /* chosen alpha (fp32, as hq_params carries it) */
+  int32_t rice_k;     /* chosen Rice parameter */
+  double bps;         /* realized payload rate at (alpha, rice_k), bits per element */
+  int32_t feasible;   /* 1 if some k in [k_min, k_max] reached the target within tol */
+  int32_t evaluations;/* rate evaluations made (one size-mode encode each) */
+} hq_calibration;
+
+/* Rate calibration of alpha and the Rice parameter (Method 2: alpha is set so
+ * that the codes fit the budget; Method 3: the realized rate lands within
+ * about 0.01 bps of the target, k chosen per rate).  For each k in
+ * [k_min, k_max]: if the rate at alpha = 2^-14 already exceeds
+ * target_bps - tol/2 the k is skipped; otherwise log2(alpha) is bisected on
+ * [-14, 18] (at most 60 steps, stopping once |rate - target| <= tol) and the
+ * midpoint with the rate nearest the target is rounded to fp32 and evaluated
+ * again; it is feasible if that rate is within tol.  The feasible k with the
+ * largest alpha (least distortion) wins, ties to the smaller k.  Rates are
+ * hq_payload_bits / (128 n_tiles) of the tiles given; p supplies lattice,
+ * dither, seeds, signs and segments (its alpha and rice_k are ignored).
+ *   d_bits     device uint64 scratch; d_status device uint32 scratch, zeroed
+ *              before every evaluation (it holds the last evaluation's bits).
+ * Synchronous: every evaluation is read back with cudaStreamSynchronize on
+ * `stream` (the only entry point that waits on the GPU).  Returns HQ_OK (see
+ * out->feasible), HQ_ERR_INVALID, or HQ_ERR_CUDA (also when a cross-block
+ * wait ran out). */
+int hq_calibrate(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, double target_bps,
+                 double tol, int k_min, int k_max, void *d_ws, size_t ws_bytes,
+                 uint64_t *d_bits, uint32_t *d_status, hq_stream_t stream,
+                 hq_calibration *out);
 
 /* Decode n_tiles tiles from a stream written by hq_encode with the same
  * params (Method 1-4 inverted: unpack, Rice decode, restore stripped bits,

@@ -57,3 +57,11 @@ def test_params_layout(hqlib):
     # the ctypes mirror must match the C struct: 4+4+4+4+8+8+8+8+4+4 = 56 bytes
     assert ctypes.sizeof(hqlib.hq_params) == 56
     assert hqlib.hq_params.d_signs.offset == 32
+
+
+def test_calibration_layout(hqlib):
+    import ctypes
+    # float, int32, double, int32, int32 -> 4+4+8+4+4 = 24 bytes, bps at offset 8
+    assert ctypes.sizeof(hqlib.hq_calibration) == 24
+    assert hqlib.hq_calibration.bps.offset == 8
+    assert hqlib.hq_calibration.evaluations.offset == 20

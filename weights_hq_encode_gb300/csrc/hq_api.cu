@@ -97,17 +97,19 @@ size_t hq_encode_workspace_bytes(int64_t n_tiles) {
   return 8 + 8 * (size_t)blocks;
 }
 
-int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
-              uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
-              uint32_t *d_status, hq_stream_t stream) {
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (!params_ok(p) || n_tiles < 0 || !d_offsets || !d_status) return HQ_ERR_INVALID;
+namespace {
+
+// hq_encode, plus the optional payload counter of hq_payload_bits.
+int encode_impl(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
+                uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
+                uint32_t *d_status, cudaStream_t st, unsigned long long *d_bits) {
   if (n_tiles == 0) {
+    if (d_offsets == nullptr) return HQ_OK;
     return cudaMemsetAsync(d_offsets, 0, sizeof(uint64_t), st) == cudaSuccess ? HQ_OK
                                                                              : HQ_ERR_CUDA;
   }
   if (!d_x || !aligned(d_x, 16) || !d_ws || !aligned(d_ws, 8) ||
-      ws_bytes < hq_encode_workspace_bytes(n_tiles) || !aligned(d_offsets, 8))
+      ws_bytes < hq_encode_workspace_bytes(n_tiles) || (d_offsets && !aligned(d_offsets, 8)))
     return HQ_ERR_INVALID;
   EncodeArgs a;
   std::memset(&a, 0, sizeof a);
@@ -119,7 +121,8 @@ int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t
   if (blocks > 0x7FFFFFFF) return HQ_ERR_INVALID;
   a.n_blocks = (uint32_t)blocks;
   a.stream = d_stream;
-  a.cap_words = d_stream ? cap_words : 0;
+  // a size query reports the capacity it would need; a payload count does not
+  a.cap_words = d_stream ? cap_words : (d_bits ? UINT64_MAX : 0);
   a.offsets = d_offsets;
   a.ws = d_ws;
   a.status = d_status;
@@ -134,11 +137,120 @@ int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t
   a.rbits = rbits_of(p->lattice, p->rice_k);
   a.dither = p->dither;
   a.spins = p->lookback_spins ? p->lookback_spins : kDefaultSpins;
+  a.payload_bits = d_bits;
   if (!(p->flags & HQ_FLAG_WORKSPACE_READY)) {
     if (cudaMemsetAsync(d_ws, 0, hq_encode_workspace_bytes(n_tiles), st) != cudaSuccess)
       return HQ_ERR_CUDA;
   }
   return hq::launch_encode(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
+}  // namespace
+
+int hq_encode(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32_t *d_stream,
+              uint64_t cap_words, uint64_t *d_offsets, void *d_ws, size_t ws_bytes,
+              uint32_t *d_status, hq_stream_t stream) {
+  if (!params_ok(p) || n_tiles < 0 || !d_offsets || !d_status) return HQ_ERR_INVALID;
+  return encode_impl(p, d_x, n_tiles, d_stream, cap_words, d_offsets, d_ws, ws_bytes, d_status,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int hq_payload_bits(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint64_t *d_bits,
+                    void *d_ws, size_t ws_bytes, uint32_t *d_status, hq_stream_t stream) {
+  if (!params_ok(p) || n_tiles < 0 || !d_bits || !aligned(d_bits, 8) || !d_status)
+    return HQ_ERR_INVALID;
+  return encode_impl(p, d_x, n_tiles, nullptr, 0, nullptr, d_ws, ws_bytes, d_status,
+                     reinterpret_cast<cudaStream_t>(stream),
+                     reinterpret_cast<unsigned long long *>(d_bits));
+}
+
+namespace {
+
+// One rate evaluation of hq_calibrate: payload bits per element of the call's
+// tiles at (alpha, k), read back synchronously.
+int calib_rate(const hq_params &base, float alpha, int k, const uint16_t *d_x, int64_t n_tiles,
+               void *d_ws, size_t ws_bytes, uint64_t *d_bits, uint32_t *d_status,
+               cudaStream_t st, double *rate) {
+  hq_params q = base;
+  q.alpha = alpha;
+  q.rice_k = k;
+  q.flags &= ~HQ_FLAG_WORKSPACE_READY;
+  if (cudaMemsetAsync(d_bits, 0, sizeof(uint64_t), st) != cudaSuccess ||
+      cudaMemsetAsync(d_status, 0, sizeof(uint32_t), st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  int rc = hq_payload_bits(&q, d_x, n_tiles, d_bits, d_ws, ws_bytes, d_status,
+                           reinterpret_cast<hq_stream_t>(st));
+  if (rc != HQ_OK) return rc;
+  uint64_t bits = 0;
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&bits, d_bits, sizeof bits, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(&status, d_status, sizeof status, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  if (status & HQ_ERR_TIMEOUT) return HQ_ERR_CUDA;
+  *rate = (double)bits / ((double)n_tiles * HQ_TILE);
+  return HQ_OK;
+}
+
+}  // namespace
+
+int hq_calibrate(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, double target_bps,
+                 double tol, int k_min, int k_max, void *d_ws, size_t ws_bytes,
+                 uint64_t *d_bits, uint32_t *d_status, hq_stream_t stream,
+                 hq_calibration *out) {
+  if (!p || !out || n_tiles <= 0 || !(target_bps > 0.0) || !(tol > 0.0) || k_min < 0 ||
+      k_max > 15 || k_min > k_max || !d_bits || !d_status)
+    return HQ_ERR_INVALID;
+  hq_params base = *p;
+  base.alpha = 1.0f;
+  base.rice_k = k_min;
+  if (!params_ok(&base)) return HQ_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  std::memset(out, 0, sizeof *out);
+  bool have = false;
+  for (int k = k_min; k <= k_max; ++k) {
+    // bisection on log2(alpha) over [-14, 18]; a k whose rate at the smallest
+    // alpha is already above the target cannot reach it
+    double lo = -14.0, hi = 18.0, r = 0.0;
+    int rc = calib_rate(base, (float)std::pow(2.0, lo), k, d_x, n_tiles, d_ws, ws_bytes, d_bits,
+                        d_status, st, &r);
+    if (rc != HQ_OK) return rc;
+    ++out->evaluations;
+    if (r > target_bps - tol / 2) continue;
+    bool have_best = false;
+    double best_mid = 0.0, best_r = 0.0;
+    for (int it = 0; it < 60; ++it) {
+      const double mid = 0.5 * (lo + hi);
+      rc = calib_rate(base, (float)std::pow(2.0, mid), k, d_x, n_tiles, d_ws, ws_bytes, d_bits,
+                      d_status, st, &r);
+      if (rc != HQ_OK) return rc;
+      ++out->evaluations;
+      if (!have_best || std::fabs(r - target_bps) < std::fabs(best_r - target_bps)) {
+        have_best = true;
+        best_mid = mid;
+        best_r = r;
+      }
+      if (std::fabs(r - target_bps) <= tol) break;
+      if (r < target_bps) lo = mid;
+      else hi = mid;
+    }
+    const float alpha = (float)std::pow(2.0, best_mid);
+    double bps = 0.0;
+    rc = calib_rate(base, alpha, k, d_x, n_tiles, d_ws, ws_bytes, d_bits, d_status, st, &bps);
+    if (rc != HQ_OK) return rc;
+    ++out->evaluations;
+    if (!(std::fabs(bps - target_bps) <= tol)) continue;
+    // keep the largest alpha (least distortion); among equal alphas the smaller k
+    if (!have || alpha > out->alpha) {
+      have = true;
+      out->alpha = alpha;
+      out->rice_k = k;
+      out->bps = bps;
+    }
+  }
+  out->feasible = have ? 1 : 0;
+  return HQ_OK;
 }
 
 int hq_decode(const hq_params *p, const uint32_t *d_stream, uint64_t stream_words,

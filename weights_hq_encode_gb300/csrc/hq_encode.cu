@@ -347,10 +347,12 @@ encode_kernel(EncodeArgs a) {
       if (lane >= d) ui += o;
     }
     s_tile_uoff[tid] = ui - tu;
-    const uint64_t words = ((uint64_t)nt * R + __shfl_sync(0xffffffffu, ui, 31) + 31) >> 5;
+    const uint64_t gbits = (uint64_t)nt * R + __shfl_sync(0xffffffffu, ui, 31);
+    const uint64_t words = (gbits + 31) >> 5;
     if (tid == 0) {
       s_words = words;
       publish_total(state, g, words);
+      if (a.payload_bits != nullptr) atomicAdd(a.payload_bits, (unsigned long long)gbits);
     }
   }
   __syncthreads();
@@ -370,8 +372,10 @@ encode_kernel(EncodeArgs a) {
       if (!ok) {
         atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
       } else {
-        a.offsets[g] = excl;
-        if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + gwords;
+        if (a.offsets != nullptr) {
+          a.offsets[g] = excl;
+          if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + gwords;
+        }
         if (excl + gwords > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
         if (s_flags) atomicOr(a.status, s_flags);
       }

@@ -38,6 +38,7 @@ struct EncodeArgs {
   int rbits;
   int dither;
   uint32_t spins;
+  unsigned long long *payload_bits;   // non-null: add each group's Rice bits here
 };
 
 struct DecodeArgs {

@@ -24,7 +24,7 @@ HQ_FLAG_WORKSPACE_READY = 1
 
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
             "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
-            "hq_encode_noalloc")
+            "hq_encode_noalloc", "hq_payload_bits", "hq_calibrate")
 HQ_NOALLOC_MAX_TILES = 1 << 22
 
 
@@ -34,6 +34,11 @@ class hq_params(ctypes.Structure):
                 ("dither_seed", ctypes.c_uint64), ("tile_base", ctypes.c_uint64),
                 ("d_signs", ctypes.c_void_p), ("tiles_per_segment", ctypes.c_int64),
                 ("lookback_spins", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+
+
+class hq_calibration(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("rice_k", ctypes.c_int32), ("bps", ctypes.c_double),
+                ("feasible", ctypes.c_int32), ("evaluations", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -54,6 +59,11 @@ def _load():
     L.hq_encode.argtypes = [vp, vp, i64, vp, u64, vp, vp, sz, vp, vp]
     L.hq_encode_noalloc.restype = ctypes.c_int
     L.hq_encode_noalloc.argtypes = [vp, vp, i64, vp, u64, vp, vp, vp]
+    L.hq_payload_bits.restype = ctypes.c_int
+    L.hq_payload_bits.argtypes = [vp, vp, i64, vp, vp, sz, vp, vp]
+    L.hq_calibrate.restype = ctypes.c_int
+    L.hq_calibrate.argtypes = [vp, vp, i64, ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_int, vp, sz, vp, vp, vp, vp]
     L.hq_decode.restype = ctypes.c_int
     L.hq_decode.argtypes = [vp, vp, u64, vp, i64, vp, ctypes.c_int, vp, vp]
     L.hq_decode_qk_workspace_bytes.restype = sz
@@ -132,6 +142,25 @@ def hq_encode_noalloc(p: hq_params, x: torch.Tensor, n_tiles: int, stream_buf, c
     """hq_encode with the library's built-in scratch (no workspace argument)."""
     return int(_lib.hq_encode_noalloc(ctypes.byref(p), _ptr(x), n_tiles, _ptr(stream_buf),
                                       cap_words, _ptr(offsets), _ptr(status), _stream(stream)))
+
+
+def hq_payload_bits(p: hq_params, x: torch.Tensor, n_tiles: int, bits: torch.Tensor,
+                    ws: torch.Tensor, status: torch.Tensor, stream=None) -> int:
+    """Adds the Rice payload bits of encoding x to the device int64 `bits`."""
+    return int(_lib.hq_payload_bits(ctypes.byref(p), _ptr(x), n_tiles, _ptr(bits), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _ptr(status),
+                                    _stream(stream)))
+
+
+def hq_calibrate(p: hq_params, x: torch.Tensor, n_tiles: int, target_bps: float, tol: float,
+                 k_min: int, k_max: int, ws: torch.Tensor, bits: torch.Tensor,
+                 status: torch.Tensor, stream=None):
+    """(return code, hq_calibration) of the GPU rate calibration."""
+    out = hq_calibration()
+    rc = int(_lib.hq_calibrate(ctypes.byref(p), _ptr(x), n_tiles, float(target_bps), float(tol),
+                               k_min, k_max, _ptr(ws), ws.numel() * ws.element_size(), _ptr(bits),
+                               _ptr(status), _stream(stream), ctypes.byref(out)))
+    return rc, out
 
 
 def hq_decode(p: hq_params, stream_buf: torch.Tensor, stream_words: int, offsets: torch.Tensor,
