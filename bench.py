@@ -273,6 +273,7 @@ def run_ours(args, rank, world):
 
     # ---- fused scores on compressed K (reported beside the step, not in `value`)
     fused = run_fused(hq, I, cal, dev, args) if rank == 0 and not args.skip_fused else None
+    attn = run_attention(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -291,6 +292,7 @@ def run_ours(args, rank, world):
                           "parallelism": f"{world} independent replicas (tile shards)"},
                "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
                "gpu_launches": len(order) * args.steps, "fused_scores": fused,
+               "fused_attention": attn,
                "cpu_baseline": cpu, "source_hash": source_hash()}
         print(json.dumps(res), flush=True)
 
@@ -379,6 +381,57 @@ def run_fused(hq, I, cal, dev, args):
     peak, _ = hbm_peak()
     flops = 2.0 * B * Hq * T * 128
     return {"workload": "K 8 heads x 32768 tokens E8 3 bps; q 16 x 32 heads; fp32 scores",
+            "ms": round(ms, 4), "alg_bytes": int(alg),
+            "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
+            "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+            "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2), "status": int(st.item())}
+
+
+def run_attention(hq, I, cal, dev):
+    """One decode step of attention over the compressed K (E8, 3 bps) and V
+    (E8, 2 bps) of the scores workload: scores, softmax, P.V, all in the
+    library's kernels."""
+    import numpy as np
+    import torch
+    C = I.SCORES
+    B, Hq, T, n_kv = C["batch"], C["q_heads"], C["tokens"], C["kv_heads"]
+    n = n_kv * T
+    sides = []
+    for X, rate, seed, lseed in ((I.scores_keys(dev), "3.0", C["dither_seeds"][0], C["layer_sign_seed"]),
+                                 (I.scores_values(dev), "2.0", C["dither_seeds"][1], C["layer_sign_seed"] + 1)):
+        c = cal["kv_cache_8b"]["E8"][rate]
+        m = [a ^ b for a, b in zip(hq.hq_make_signs(C["sign_seed"], 0), hq.hq_make_signs(lseed, 0))]
+        signs = torch.from_numpy(np.asarray(m, np.uint32).view(np.int32).reshape(1, 4)).to(dev)
+        p = hq.make_params(8, c["k"], c["alpha"], 1, seed, signs, n)
+        sides.append((p, hq.encode(X, p), signs))
+    (pk, ek, _), (pv, ev, _) = sides
+    q = I.scores_queries(dev).view(torch.int16)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(hq.hq_decode_attention_workspace_bytes(n_kv, T, B, Hq), dtype=torch.uint8,
+                     device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        return hq.hq_decode_attention(pk, ek.stream, ek.total_words, ek.offsets, pv, ev.stream,
+                                      ev.total_words, ev.offsets, n_kv, T, q, B, Hq, 128 ** -0.5,
+                                      out, None, ws, st)
+    for _ in range(3):
+        assert call() == hq.HQ_OK
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    alg = (ek.total_words + ev.total_words) * 4 + (ek.offsets.numel() + ev.offsets.numel()) * 8 \
+        + q.numel() * 2 + out.numel() * 4
+    peak, _ = hbm_peak()
+    flops = 4.0 * B * Hq * T * 128
+    return {"workload": "K and V 8 heads x 32768 tokens (E8, 3 and 2 bps); q 16 x 32 heads; "
+                        "softmax(q K^T / sqrt(128)) V in fp32",
             "ms": round(ms, 4), "alg_bytes": int(alg),
             "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
             "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),

@@ -198,6 +198,37 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
                  float *d_scores, void *d_ws, size_t ws_bytes, uint32_t *d_status,
                  hq_stream_t stream);
 
+/* Bytes of device workspace hq_decode_attention needs: the rotated queries
+ * (B * Hq * 128 fp32), the scores / probabilities (B * Hq * n_tokens fp32)
+ * and the partial sums of the value contraction.  0 for invalid sizes. */
+size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int B, int Hq);
+
+/* One decode step of attention read straight from compressed K and V
+ * (closing section, fused decode + MMA; Method 4 for the KV cache):
+ *   s[b][hq][t] = scale * sum_d q[b][hq][d] * Khat[h][t][d],  h = hq / (Hq / n_kv_heads)
+ *   p[b][hq][.] = softmax over t of s[b][hq][.]
+ *   out[b][hq][d] = sum_t p[b][hq][t] * Vhat[h][t][d]
+ * with Khat / Vhat the decodes of tile h * n_tokens + t of the K / V stream
+ * (each with its own params pk / pv).  Neither K nor V is written out: the
+ * value side is accumulated in the lattice domain and transformed once per
+ * query row.
+ *   d_q        [B][Hq][128] bf16, device.
+ *   d_out      [B][Hq][128] fp32, device, 16-byte aligned.
+ *   d_probs    optional [B][Hq][n_tokens] fp32 output of p (NULL: kept in
+ *              the workspace only).
+ *   d_ws       >= hq_decode_attention_workspace_bytes() bytes, 16-byte aligned.
+ *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group of either stream.
+ * Requires Hq % n_kv_heads == 0 and every head's tiles in one sign segment of
+ * each stream (tiles_per_segment of pk and pv multiples of n_tokens).
+ * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
+int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_t k_words,
+                        const uint64_t *d_k_offsets, const hq_params *pv,
+                        const uint32_t *d_v_stream, uint64_t v_words,
+                        const uint64_t *d_v_offsets, int n_kv_heads, int64_t n_tokens,
+                        const uint16_t *d_q, int B, int Hq, float scale, float *d_out,
+                        float *d_probs, void *d_ws, size_t ws_bytes, uint32_t *d_status,
+                        hq_stream_t stream);
+
 /* Largest n_tiles accepted by hq_encode_noalloc: 2^22 tiles (2^29 elements,
  * 1 GiB of bf16 per call). */
 #define HQ_NOALLOC_MAX_TILES (1LL << 22)

@@ -1,0 +1,165 @@
+"""GPU parity of decode attention over compressed K and V (closing section of
+the HyperQuant summary: fused decode + MMA) against the fp64 oracle
+(oracle/attention.py) on the oracle's own decodes.
+
+The K and V streams are written by the CPU oracle and copied to the GPU, so
+every expected value comes from the oracle alone.
+
+Tolerance, derived to first order in u = 2^-24 from the fp32 steps of the
+CUDA path.  A score is a 128-term fp32 dot of the rotated query (7 rounded
+transform stages and one scaling) with e, so |dz_t| <= (128 + 8) u zeta,
+zeta = scale |q| max_t |Khat_t| (the transform is orthogonal, so
+|q'| |e_t| = |q| |Khat_t|).  Softmax turns that into a relative error of
+p_t of at most 2 max|dz| plus a few u for exp and the division.  The value
+side sums p_t e_t in fp32 over at most 512 tokens per chunk and 65 chunks
+per head, adding (512 + 64) u relative to sum_t p_t |Vhat_t,d|.  So an
+element of out is held to (2 * 136 u zeta + 600 u) of sum_t p_t |Vhat_t,d|,
+i.e. (1.7e-5 zeta + 3.6e-5), and p_t to (1.7e-5 zeta + 1e-6) of p_t plus
+1e-38 for values below the fp32 normal range."""
+import numpy as np
+import pytest
+import torch
+
+from _cases import calibration
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weights_hq_encode_gb300 import build
+    build.build()
+    from weights_hq_encode_gb300 import hq as H
+    return H
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.reshape(-1, 128).cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+class Side:
+    """One compressed stream (K or V), written and decoded by the oracle."""
+
+    def __init__(self, oracle, hq, x_bits, lattice, k, alpha, seed, mask, tps):
+        self.P = oracle.make_params(lattice, k, alpha, 1, seed, mask, tps)
+        enc = oracle.encode(self.P, x_bits)
+        assert enc["status"] == 0
+        self.words = int(enc["total_words"])
+        self.hat = oracle.decode(self.P, enc["stream"], enc["offsets"], x_bits.shape[0])["out"]
+        s = np.ascontiguousarray(enc["stream"][:max(self.words, 1)]).view(np.int32)
+        self.stream = torch.from_numpy(s.copy()).cuda()
+        self.offsets = torch.from_numpy(np.ascontiguousarray(enc["offsets"]).view(np.int64).copy()).cuda()
+        signs = torch.from_numpy(np.ascontiguousarray(mask, dtype=np.uint32).view(np.int32).copy()).cuda()
+        self.p = hq.make_params(lattice, k, alpha, 1, seed, signs, tps)
+
+
+def _masks(oracle, layer_seed):
+    from weights_hq_encode_gb300 import inputs as I
+    C = I.SCORES
+    return (oracle.make_signs(C["sign_seed"], 0) ^ oracle.make_signs(layer_seed, 0)).reshape(1, 4)
+
+
+def _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, probs=True):
+    q = torch.from_numpy(q_bits.view(np.int16).copy()).cuda()
+    out = torch.full((B, Hq, 128), 7.0, dtype=torch.float32, device="cuda")
+    pr = torch.full((B, Hq, T), 7.0, dtype=torch.float32, device="cuda") if probs else None
+    ws = torch.empty(hq.hq_decode_attention_workspace_bytes(n_kv, T, B, Hq), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = hq.hq_decode_attention(Ks.p, Ks.stream, Ks.words, Ks.offsets, Vs.p, Vs.stream, Vs.words,
+                                Vs.offsets, n_kv, T, q, B, Hq, scale, out, pr, ws, st)
+    assert rc == hq.HQ_OK
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), (pr.cpu().numpy() if probs else None), int(st.item())
+
+
+def _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs):
+    ref, P = A.attention(Ks.hat, Vs.hat, q_bits, n_kv, T, B, Hq, scale)
+    G = Hq // n_kv
+    V = np.abs(Vs.hat.astype(np.float64)).reshape(n_kv, T, 128)
+    size = np.stack([np.einsum("bgt,td->bgd", P[:, h * G:(h + 1) * G], V[h]) for h in range(n_kv)],
+                    axis=1).reshape(B, Hq, 128)
+    qn = np.linalg.norm(A.bf16_bits_to_f64(q_bits), axis=-1)                      # [B, Hq]
+    kmax = np.linalg.norm(Ks.hat.astype(np.float64).reshape(n_kv, T, 128), axis=-1).max(-1)
+    zeta = scale * qn * np.repeat(kmax, G)[None, :]                                # [B, Hq]
+    tol = (1.7e-5 * zeta + 3.6e-5)[:, :, None]
+    err = np.abs(out - ref) / (size + 1e-30)
+    worst = np.unravel_index(np.argmax(err / tol), err.shape)
+    assert np.all(err <= tol), (err[worst], zeta[worst[:2]], tol[worst[0], worst[1], 0])
+    if probs is not None:
+        tolp = (1.7e-5 * zeta + 1e-6)[:, :, None]
+        assert np.all(np.abs(probs - P) <= tolp * P + 1e-38)
+    return (err / tol).max()
+
+
+def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8):
+    from weights_hq_encode_gb300 import inputs as I
+    C = I.SCORES
+    cal = calibration()
+    ck = cal["kv_cache_8b"]["E8"]["3.0"] if lat_k == 8 else cal["long_context"]["D4"]["2.5"]
+    cv = cal["kv_cache_8b"]["E8"]["2.0"] if lat_v == 8 else cal["long_context"]["Z"]["2.0"]
+    kb = _bits(I.scores_keys("cpu", tokens=T)[:n_kv])
+    vb = _bits(I.scores_values("cpu", tokens=T)[:n_kv])
+    n = n_kv * T
+    Ks = Side(oracle, hq, kb, lat_k, ck["k"], ck["alpha"], C["dither_seeds"][0],
+              _masks(oracle, C["layer_sign_seed"]), n)
+    Vs = Side(oracle, hq, vb, lat_v, cv["k"], cv["alpha"], C["dither_seeds"][1],
+              _masks(oracle, C["layer_sign_seed"] + 1), n)
+    q_bits = _bits(I.scores_queries("cpu", batch=B, q_heads=Hq)).reshape(B, Hq, 128)
+    return Ks, Vs, q_bits
+
+
+@pytest.mark.parametrize("n_kv,T,B,Hq,lat_k,lat_v", [
+    (2, 100, 3, 6, 8, 8),        # groups straddle the two heads (T not a multiple of 32)
+    (2, 64, 20, 8, 8, 8),        # 80 query rows per head: two row tiles
+    (1, 1, 1, 1, 8, 8),          # one token
+    (3, 700, 2, 6, 4, 1),        # D4 keys, Z values
+])
+def test_attention_against_oracle(hq, oracle, n_kv, T, B, Hq, lat_k, lat_v):
+    from oracle import attention as A
+    Ks, Vs, q_bits = _workload(oracle, hq, n_kv, T, B, Hq, lat_k, lat_v)
+    scale = 128 ** -0.5
+    out, probs, st = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, scale)
+    assert st == 0
+    _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs)
+    out2, _, st2 = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, probs=False)
+    assert st2 == 0 and np.array_equal(out, out2)             # deterministic
+
+
+def test_attention_full_size(hq, oracle):
+    """The decode-attention workload: 8 KV heads x 32768 tokens, batch 16 x 32
+    query heads, K at 3 bps and V at 2 bps (E8)."""
+    from oracle import attention as A
+    from weights_hq_encode_gb300 import inputs as I
+    C = I.SCORES
+    n_kv, T, B, Hq = C["kv_heads"], C["tokens"], C["batch"], C["q_heads"]
+    Ks, Vs, q_bits = _workload(oracle, hq, n_kv, T, B, Hq)
+    out, probs, st = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, 128 ** -0.5)
+    assert st == 0
+    _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, 128 ** -0.5, out, probs)
+
+
+def test_attention_corrupt_value_stream_is_flagged(hq, oracle):
+    n_kv, T, B, Hq = 2, 96, 2, 4
+    Ks, Vs, q_bits = _workload(oracle, hq, n_kv, T, B, Hq)
+    Vs.offsets[1] = Vs.offsets[2] + 1                        # group 0 now ends past group 1
+    out, _, st = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, 0.1, probs=False)
+    assert st & hq.HQ_ERR_CORRUPT
+    assert np.isfinite(out).all()
+
+
+def test_attention_invalid_arguments(hq, oracle):
+    n_kv, T, B, Hq = 2, 64, 2, 4
+    Ks, Vs, q_bits = _workload(oracle, hq, n_kv, T, B, Hq)
+    q = torch.from_numpy(q_bits.view(np.int16).copy()).cuda()
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(hq.hq_decode_attention_workspace_bytes(n_kv, T, B, Hq), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hq.hq_decode_attention_workspace_bytes(3, T, B, Hq) == 0     # Hq % n_kv != 0
+    args = [Ks.p, Ks.stream, Ks.words, Ks.offsets, Vs.p, Vs.stream, Vs.words, Vs.offsets]
+    assert hq.hq_decode_attention(*args, 3, T, q, B, Hq, 0.1, out, None, ws, st) == hq.HQ_ERR_INVALID
+    assert hq.hq_decode_attention(*args, n_kv, T, q, B, Hq, 0.1, out, None, ws[:16], st) == hq.HQ_ERR_INVALID
+    assert hq.hq_decode_attention(*args, n_kv, T, None, B, Hq, 0.1, out, None, ws, st) == hq.HQ_ERR_INVALID

@@ -268,6 +268,79 @@ int hq_decode(const hq_params *p, const uint32_t *d_stream, uint64_t stream_word
   return hq::launch_decode(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
 }
 
+namespace {
+
+// Attention workspace geometry: rotated queries, scores (probabilities),
+// then the partial P . E rows of every (head, chunk, row tile).
+struct AttnGeometry {
+  int64_t chunks = 0, rowtiles = 0;
+  size_t qrot = 0, scores = 0, partials = 0;
+};
+
+bool attn_geometry(int n_kv, int64_t n_tokens, int B, int Hq, AttnGeometry *g) {
+  if (n_kv <= 0 || n_tokens <= 0 || B <= 0 || Hq <= 0 || Hq % n_kv != 0) return false;
+  const int64_t rows = (int64_t)B * (Hq / n_kv);
+  const int64_t groups = (n_tokens + HQ_GROUP_TILES - 1) / HQ_GROUP_TILES + 1;   // a head's groups
+  g->chunks = (groups + hq::kPvGroupsPerChunk - 1) / hq::kPvGroupsPerChunk;
+  g->rowtiles = (rows + hq::kPvRows - 1) / hq::kPvRows;
+  if (g->chunks > 0x7FFFFFFF || g->rowtiles > 65535 || n_kv > 65535) return false;
+  // every region starts on a 256-byte boundary (the kernels use 16-byte vectors)
+  auto round256 = [](size_t v) { return (v + 255) / 256 * 256; };
+  g->qrot = round256((size_t)B * Hq * HQ_TILE * sizeof(float));
+  g->scores = round256((size_t)B * Hq * (size_t)n_tokens * sizeof(float));
+  g->partials = (size_t)n_kv * g->chunks * g->rowtiles * hq::kPvRows * HQ_TILE * sizeof(float);
+  return true;
+}
+
+}  // namespace
+
+size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int B, int Hq) {
+  AttnGeometry g;
+  if (!attn_geometry(n_kv_heads, n_tokens, B, Hq, &g)) return 0;
+  return g.qrot + g.scores + g.partials;
+}
+
+int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_t k_words,
+                        const uint64_t *d_k_offsets, const hq_params *pv,
+                        const uint32_t *d_v_stream, uint64_t v_words,
+                        const uint64_t *d_v_offsets, int n_kv_heads, int64_t n_tokens,
+                        const uint16_t *d_q, int B, int Hq, float scale, float *d_out,
+                        float *d_probs, void *d_ws, size_t ws_bytes, uint32_t *d_status,
+                        hq_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!params_ok(pk) || !params_ok(pv) || !d_status || !(scale == scale)) return HQ_ERR_INVALID;
+  if (B == 0) return HQ_OK;
+  AttnGeometry g;
+  if (!attn_geometry(n_kv_heads, n_tokens, B, Hq, &g)) return HQ_ERR_INVALID;
+  if (pk->tiles_per_segment % n_tokens != 0 || pv->tiles_per_segment % n_tokens != 0)
+    return HQ_ERR_INVALID;
+  if (!d_k_stream || !d_k_offsets || !d_v_stream || !d_v_offsets || !d_q || !d_out || !d_ws ||
+      ws_bytes < g.qrot + g.scores + g.partials || !aligned(d_ws, 16) || !aligned(d_out, 16) ||
+      !aligned(d_k_offsets, 8) || !aligned(d_v_offsets, 8) || (d_probs && !aligned(d_probs, 4)))
+    return HQ_ERR_INVALID;
+  char *ws = reinterpret_cast<char *>(d_ws);
+  hq::AttnArgs a;
+  const int64_t n_tiles = (int64_t)n_kv_heads * n_tokens;
+  a.qk.dec = make_decode_args(pk, d_k_stream, k_words, d_k_offsets, n_tiles, d_status);
+  a.qk.dec.out_kind = -1;
+  a.qk.n_kv = n_kv_heads;
+  a.qk.n_tokens = n_tokens;
+  a.qk.tok_shift = pow2_shift(n_tokens);
+  a.qk.q = d_q;
+  a.qk.B = B;
+  a.qk.Hq = Hq;
+  a.qk.qrot = reinterpret_cast<float *>(ws);
+  a.qk.scores = d_probs ? d_probs : reinterpret_cast<float *>(ws + g.qrot);
+  a.v = make_decode_args(pv, d_v_stream, v_words, d_v_offsets, n_tiles, d_status);
+  a.v.out_kind = -1;
+  a.scale = scale;
+  a.partials = reinterpret_cast<float *>(ws + g.qrot + g.scores);
+  a.chunks = (int)g.chunks;
+  a.rowtiles = (int)g.rowtiles;
+  a.out = d_out;
+  return hq::launch_decode_attention(a, pk->lattice, pv->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
 size_t hq_decode_qk_workspace_bytes(int B, int Hq) {
   if (B <= 0 || Hq <= 0) return 0;
   return (size_t)B * (size_t)Hq * HQ_TILE * sizeof(float);

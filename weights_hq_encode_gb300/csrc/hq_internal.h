@@ -73,6 +73,19 @@ struct QkArgs {
   float *scores;            // [B][Hq][n_tokens]
 };
 
+// Decode attention: the K side is the scores pass (qk), the V side another
+// stream; probabilities overwrite qk.scores, partial P.E sums go to partials.
+constexpr int kPvRows = 64;           // query rows per contraction tile
+constexpr int kPvGroupsPerChunk = 16; // groups of 32 tokens per block
+struct AttnArgs {
+  QkArgs qk;                // K stream, queries, rotated queries, scores -> probabilities
+  DecodeArgs v;             // V stream
+  float scale;              // softmax scale applied to the scores
+  float *partials;          // [n_kv][chunks][rowtiles][kPvRows][128]
+  int chunks, rowtiles;
+  float *out;               // [B][Hq][128] fp32
+};
+
 // Segment (or head) of tile t: a shift when the divisor is a power of two.
 __host__ __device__ __forceinline__ int64_t div_by(int64_t t, int64_t d, int shift) {
   return shift >= 0 ? (t >> shift) : t / d;
@@ -88,5 +101,6 @@ int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st);
 int encode_tiles_per_block();
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st);
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);
+int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cudaStream_t st);
 
 }  // namespace hq

@@ -24,7 +24,8 @@ HQ_FLAG_WORKSPACE_READY = 1
 
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
             "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
-            "hq_encode_noalloc", "hq_payload_bits", "hq_calibrate")
+            "hq_encode_noalloc", "hq_payload_bits", "hq_calibrate",
+            "hq_decode_attention_workspace_bytes", "hq_decode_attention")
 HQ_NOALLOC_MAX_TILES = 1 << 22
 
 
@@ -71,6 +72,12 @@ def _load():
     L.hq_decode_qk.restype = ctypes.c_int
     L.hq_decode_qk.argtypes = [vp, vp, u64, vp, ctypes.c_int, i64, vp, ctypes.c_int,
                                ctypes.c_int, vp, vp, sz, vp, vp]
+    L.hq_decode_attention_workspace_bytes.restype = sz
+    L.hq_decode_attention_workspace_bytes.argtypes = [ctypes.c_int, i64, ctypes.c_int, ctypes.c_int]
+    L.hq_decode_attention.restype = ctypes.c_int
+    L.hq_decode_attention.argtypes = [vp, vp, u64, vp, vp, vp, u64, vp, ctypes.c_int, i64, vp,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp, vp, sz,
+                                      vp, vp]
     L.hq_make_signs.restype = None
     L.hq_make_signs.argtypes = [u64, u64, vp]
     L.hq_status_string.restype = ctypes.c_char_p
@@ -176,6 +183,22 @@ def hq_decode_qk(p: hq_params, k_stream: torch.Tensor, stream_words: int, k_offs
     return int(_lib.hq_decode_qk(ctypes.byref(p), _ptr(k_stream), stream_words, _ptr(k_offsets),
                                  n_kv_heads, n_tokens, _ptr(q), B, Hq, _ptr(scores), _ptr(ws),
                                  ws.numel() * ws.element_size(), _ptr(status), _stream(stream)))
+
+
+def hq_decode_attention_workspace_bytes(n_kv_heads: int, n_tokens: int, B: int, Hq: int) -> int:
+    return int(_lib.hq_decode_attention_workspace_bytes(n_kv_heads, n_tokens, B, Hq))
+
+
+def hq_decode_attention(pk: hq_params, k_stream: torch.Tensor, k_words: int,
+                        k_offsets: torch.Tensor, pv: hq_params, v_stream: torch.Tensor,
+                        v_words: int, v_offsets: torch.Tensor, n_kv_heads: int, n_tokens: int,
+                        q: torch.Tensor, B: int, Hq: int, scale: float, out: torch.Tensor,
+                        probs, ws: torch.Tensor, status: torch.Tensor, stream=None) -> int:
+    return int(_lib.hq_decode_attention(
+        ctypes.byref(pk), _ptr(k_stream), k_words, _ptr(k_offsets), ctypes.byref(pv),
+        _ptr(v_stream), v_words, _ptr(v_offsets), n_kv_heads, n_tokens, _ptr(q), B, Hq,
+        float(scale), _ptr(out), _ptr(probs), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(status), _stream(stream)))
 
 
 def hq_make_signs(seed: int, segment: int):

@@ -110,6 +110,13 @@ def scores_keys(device="cuda", tokens: int | None = None) -> torch.Tensor:
     return kv_slab(slab_seed(SCORES["data_seed"], 0, 0), SCORES["kv_heads"], T, device)
 
 
+def scores_values(device="cuda", tokens: int | None = None) -> torch.Tensor:
+    """V [8, tokens, 128] bf16 for the decode-attention workload (the V slab of
+    the same layer as scores_keys)."""
+    T = SCORES["tokens"] if tokens is None else tokens
+    return kv_slab(slab_seed(SCORES["data_seed"], 0, 1), SCORES["kv_heads"], T, device)
+
+
 def scores_queries(device="cuda", batch: int | None = None, q_heads: int | None = None) -> torch.Tensor:
     """q [batch, q_heads, 128] bf16, N(0, 1)."""
     B = SCORES["batch"] if batch is None else batch
