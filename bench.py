@@ -274,6 +274,7 @@ def run_ours(args, rank, world):
     # ---- fused scores on compressed K (reported beside the step, not in `value`)
     fused = run_fused(hq, I, cal, dev, args) if rank == 0 and not args.skip_fused else None
     attn = run_attention(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
+    gemm = run_gemm(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -292,7 +293,7 @@ def run_ours(args, rank, world):
                           "parallelism": f"{world} independent replicas (tile shards)"},
                "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
                "gpu_launches": len(order) * args.steps, "fused_scores": fused,
-               "fused_attention": attn,
+               "fused_attention": attn, "fused_gemm": gemm,
                "cpu_baseline": cpu, "source_hash": source_hash()}
         print(json.dumps(res), flush=True)
 
@@ -436,6 +437,53 @@ def run_attention(hq, I, cal, dev):
             "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
             "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
             "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2), "status": int(st.item())}
+
+
+def run_gemm(hq, I, cal, dev):
+    """Products with compressed Llama-3.1-8B-shaped weights (4 bps, E8): the
+    gate/up-shaped matrix 14336 x 4096 with 1 and 16 activation rows."""
+    import numpy as np
+    import torch
+    C = I.WEIGHTS8B
+    index = 3
+    rows, cols = C["shapes"][index]
+    c = cal["weights_8b"]["E8"]["4.0"][index]
+    m = hq.hq_make_signs(C["sign_seed"], 0)
+    signs = torch.from_numpy(np.asarray(m, np.uint32).view(np.int32).reshape(1, 4)).to(dev)
+    p = hq.make_params(8, c["k"], c["alpha"], 0, 0, signs, 1 << 40)
+    enc = hq.encode(I.weight_matrix(index, dev), p)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    peak, _ = hbm_peak()
+    res = {"workload": f"W {rows} x {cols} bf16 coded E8 at 4 bps ({enc.total_words * 32 / (rows * cols):.3f} "
+                       "realized); y = x What^T in fp32"}
+    for B in (1, 16):
+        x = I.activations(B, cols, device=dev).view(torch.int16)
+        y = torch.empty((B, rows), dtype=torch.float32, device=dev)
+        ws = torch.empty(hq.hq_decode_gemm_workspace_bytes(rows, cols, B), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            return hq.hq_decode_gemm(p, enc.stream, enc.total_words, enc.offsets, rows, cols, x, B,
+                                     y, ws, st)
+        for _ in range(3):
+            assert call() == hq.HQ_OK
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record()
+        for _ in range(reps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        alg = enc.total_words * 4 + enc.offsets.numel() * 8 + x.numel() * 2 + y.numel() * 4
+        res[f"B{B}"] = {"ms": round(ms, 4), "alg_bytes": int(alg),
+                        "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
+                        "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+                        "bf16_weight_GBps": round(2.0 * rows * cols / (ms * 1e-3) / 1e9, 1),
+                        "TFLOPs": round(2.0 * B * rows * cols / (ms * 1e-3) / 1e12, 2)}
+    res["status"] = int(st.item())
+    return res
 
 
 def main():

@@ -229,6 +229,31 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
                         float *d_probs, void *d_ws, size_t ws_bytes, uint32_t *d_status,
                         hq_stream_t stream);
 
+/* Bytes of device workspace hq_decode_gemm needs: the rotated activations
+ * (B * cols fp32) and one partial sum per (activation row, tile)
+ * (B * rows * cols / 128 fp32).  0 for invalid sizes. */
+size_t hq_decode_gemm_workspace_bytes(int64_t rows, int64_t cols, int B);
+
+/* Product with a compressed weight matrix (Method 2: weights coded with the
+ * same tile codec; closing section: decode fused with the matrix product):
+ *   y[b][o] = sum_i What[o][i] * x[b][i]
+ * where W [rows][cols] (cols a multiple of 128) was coded row-major, tile t
+ * holding W[t / (cols/128)][128 (t % (cols/128)) ...], and What is its decode.
+ * What is never written: each tile is decoded to the lattice domain and dotted
+ * with the activation tile rotated once (s_dec H D x).
+ *   d_x        [B][cols] bf16, device.
+ *   d_y        [B][rows] fp32, device.
+ *   d_ws       >= hq_decode_gemm_workspace_bytes() bytes, 16-byte aligned.
+ *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group.
+ * Requires the whole matrix in one sign segment (p->tiles_per_segment >=
+ * rows * cols / 128).  The sum over a row's tiles has a fixed order, so the
+ * result is deterministic.  Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.
+ * Asynchronous. */
+int hq_decode_gemm(const hq_params *p, const uint32_t *d_w_stream, uint64_t w_words,
+                   const uint64_t *d_w_offsets, int64_t rows, int64_t cols, const uint16_t *d_x,
+                   int B, float *d_y, void *d_ws, size_t ws_bytes, uint32_t *d_status,
+                   hq_stream_t stream);
+
 /* Largest n_tiles accepted by hq_encode_noalloc: 2^22 tiles (2^29 elements,
  * 1 GiB of bf16 per call). */
 #define HQ_NOALLOC_MAX_TILES (1LL << 22)

@@ -341,6 +341,52 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
   return hq::launch_decode_attention(a, pk->lattice, pv->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
 }
 
+namespace {
+
+bool gemm_sizes(int64_t rows, int64_t cols, int B, size_t *xrot, size_t *partial) {
+  if (rows <= 0 || cols <= 0 || cols % HQ_TILE != 0 || B <= 0) return false;
+  const int64_t n_tiles = rows * (cols / HQ_TILE);
+  if (n_tiles / rows != cols / HQ_TILE || (int64_t)B * rows > ((int64_t)1 << 40)) return false;
+  *xrot = ((size_t)B * cols * sizeof(float) + 255) / 256 * 256;
+  *partial = (size_t)B * n_tiles * sizeof(float);
+  return true;
+}
+
+}  // namespace
+
+size_t hq_decode_gemm_workspace_bytes(int64_t rows, int64_t cols, int B) {
+  size_t xr = 0, pa = 0;
+  return gemm_sizes(rows, cols, B, &xr, &pa) ? xr + pa : 0;
+}
+
+int hq_decode_gemm(const hq_params *p, const uint32_t *d_w_stream, uint64_t w_words,
+                   const uint64_t *d_w_offsets, int64_t rows, int64_t cols, const uint16_t *d_x,
+                   int B, float *d_y, void *d_ws, size_t ws_bytes, uint32_t *d_status,
+                   hq_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!params_ok(p) || !d_status) return HQ_ERR_INVALID;
+  size_t xr = 0, pa = 0;
+  if (!gemm_sizes(rows, cols, B, &xr, &pa)) return HQ_ERR_INVALID;
+  const int64_t n_tiles = rows * (cols / HQ_TILE);
+  if (n_tiles > p->tiles_per_segment) return HQ_ERR_INVALID;   // one sign segment
+  if (!d_w_stream || !d_w_offsets || !d_x || !d_y || !d_ws || ws_bytes < xr + pa ||
+      !aligned(d_ws, 16) || !aligned(d_w_offsets, 8))
+    return HQ_ERR_INVALID;
+  hq::GemmArgs a;
+  a.dec = make_decode_args(p, d_w_stream, w_words, d_w_offsets, n_tiles, d_status);
+  a.dec.out_kind = -1;
+  a.rows = rows;
+  a.cols = cols;
+  a.tpr = cols / HQ_TILE;
+  a.tpr_shift = pow2_shift(a.tpr);
+  a.x = d_x;
+  a.B = B;
+  a.xrot = reinterpret_cast<float *>(d_ws);
+  a.partial = reinterpret_cast<float *>(reinterpret_cast<char *>(d_ws) + xr);
+  a.y = d_y;
+  return hq::launch_decode_gemm(a, p->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+}
+
 size_t hq_decode_qk_workspace_bytes(int B, int Hq) {
   if (B <= 0 || Hq <= 0) return 0;
   return (size_t)B * (size_t)Hq * HQ_TILE * sizeof(float);

@@ -607,6 +607,91 @@ __global__ void __launch_bounds__(kTile) pv_finish_kernel(AttnArgs a) {
   a.out[(int64_t)row * kTile + d] = ((mw >> (d & 31)) & 1u) ? -y : y;
 }
 
+// ---------------------------------------------------------------- weights
+// x'[b][j] = s_dec * H * (D x[b][j]) for each 128-column tile j of activation
+// row b (the whole matrix is one sign segment).
+__global__ void rotate_x_kernel(GemmArgs a) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (b, j)
+  if (i >= (int64_t)a.B * a.tpr) return;
+  const uint32_t *mask = a.dec.signs;
+  float x[128];
+  const uint16_t *src = a.x + i * kTile;
+#pragma unroll
+  for (int k = 0; k < 128; ++k) {
+    const float f = __uint_as_float((uint32_t)src[k] << 16);
+    x[k] = ((mask[k >> 5] >> (k & 31)) & 1u) ? -f : f;
+  }
+  fwht128(x);
+#pragma unroll
+  for (int k = 0; k < 128; ++k) a.xrot[i * kTile + k] = __fmul_rn(x[k], a.dec.s_dec);
+}
+
+// Each tile's share of y: lane r of tile t holds 16 lattice-domain values;
+// partial dots with 8 activation rows at a time are reduced over the tile's
+// 8 lanes by a butterfly that leaves one finished row on each lane.
+template <int LAT, int K>
+__global__ void __launch_bounds__(kDecThreads, 3) gemm_kernel(GemmArgs a) {
+  __shared__ uint64_t s_start[kDecThreads + 1];
+  __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+  const int64_t g = blockIdx.x;
+  float e[16];
+  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);   // barriers inside
+  if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
+  const int64_t tile = g * kGroupTiles + tl;
+  const bool valid = tile < a.dec.n_tiles;
+  const int64_t row = valid ? div_by(tile, a.tpr, a.tpr_shift) : 0;
+  const int64_t j = valid ? tile - row * a.tpr : 0;
+  for (int b0 = 0; b0 < a.B; b0 += 8) {
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float acc = 0.0f;
+      if (b0 + i < a.B) {
+        const float4 *xr = reinterpret_cast<const float4 *>(
+            a.xrot + (int64_t)(b0 + i) * a.cols + j * kTile + 16 * r);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 xv = __ldg(xr + c);
+          acc = __fmaf_rn(xv.x, e[4 * c], acc);
+          acc = __fmaf_rn(xv.y, e[4 * c + 1], acc);
+          acc = __fmaf_rn(xv.z, e[4 * c + 2], acc);
+          acc = __fmaf_rn(xv.w, e[4 * c + 3], acc);
+        }
+      }
+      p[i] = acc;
+    }
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+#pragma unroll
+      for (int i = 0; i < m; ++i) {
+        const bool upper = (r & m) != 0;
+        const float send = upper ? p[i] : p[i + m];
+        const float keep = upper ? p[i + m] : p[i];
+        const float got = __shfl_xor_sync(0xffffffffu, send, m);
+        p[i] = __fadd_rn(keep, got);
+      }
+    }
+    const int b = b0 + r;                        // slot kept by lane r is row b0 + r
+    if (valid && b < a.B) a.partial[(int64_t)b * a.dec.n_tiles + tile] = p[0];
+  }
+}
+
+// y[b][o] = sum over the row's tiles of their shares: one warp per (b, o),
+// lanes strided over the tiles, then a fixed butterfly (deterministic).
+__global__ void gemm_reduce_kernel(GemmArgs a) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // (b, o)
+  const int lane = threadIdx.x & 31;
+  if (w >= (int64_t)a.B * a.rows) return;        // warp-uniform
+  const int64_t b = w / a.rows, o = w - b * a.rows;
+  const float *src = a.partial + b * a.dec.n_tiles + o * a.tpr;
+  float s = 0.0f;
+  for (int64_t jj = lane; jj < a.tpr; jj += 32) s = __fadd_rn(s, src[jj]);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
+  if (lane == 0) a.y[b * a.rows + o] = s;
+}
+
 template <int LAT>
 static void launch_dec_lat(const DecodeArgs &a, cudaStream_t st) {
   dim3 grid((unsigned)a.n_groups), block(kDecThreads);
@@ -646,6 +731,17 @@ static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
   }
 }
 
+template <int LAT>
+static void launch_gemm_lat(const GemmArgs &a, cudaStream_t st) {
+  dim3 grid((unsigned)a.dec.n_groups), block(kDecThreads);
+  switch (a.dec.rice_k) {
+    case 2: gemm_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
+    case 3: gemm_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
+    case 4: gemm_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
+    default: gemm_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+  }
+}
+
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st) {
   switch (lattice) {
     case 8: launch_dec_lat<8>(a, st); break;
@@ -679,6 +775,21 @@ int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cud
   }
   if (cudaGetLastError() != cudaSuccess) return 1;
   pv_finish_kernel<<<rows, kTile, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {
+  const int64_t xt = (int64_t)a.B * a.tpr;
+  rotate_x_kernel<<<(unsigned)((xt + 127) / 128), 128, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return 1;
+  switch (lattice) {
+    case 8: launch_gemm_lat<8>(a, st); break;
+    case 4: launch_gemm_lat<4>(a, st); break;
+    default: launch_gemm_lat<1>(a, st); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return 1;
+  const int64_t warps = (int64_t)a.B * a.rows;
+  gemm_reduce_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 

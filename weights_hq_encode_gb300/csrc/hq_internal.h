@@ -86,6 +86,20 @@ struct AttnArgs {
   float *out;               // [B][Hq][128] fp32
 };
 
+// Product with a compressed weight matrix W [rows][cols] (row-major tiles):
+// y[b][o] = sum_i What[o][i] x[b][i].
+struct GemmArgs {
+  DecodeArgs dec;           // W stream
+  int64_t rows, cols;
+  int64_t tpr;              // tiles per row = cols / 128
+  int tpr_shift;            // log2(tpr) when a power of two, else -1
+  const uint16_t *x;        // [B][cols] bf16
+  int B;
+  float *xrot;              // [B][cols] fp32: s_dec * H * D * x, per 128-column tile
+  float *partial;           // [B][n_tiles] fp32: one tile's share of y
+  float *y;                 // [B][rows] fp32
+};
+
 // Segment (or head) of tile t: a shift when the divisor is a power of two.
 __host__ __device__ __forceinline__ int64_t div_by(int64_t t, int64_t d, int shift) {
   return shift >= 0 ? (t >> shift) : t / d;
@@ -102,5 +116,6 @@ int encode_tiles_per_block();
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st);
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);
 int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cudaStream_t st);
+int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st);
 
 }  // namespace hq

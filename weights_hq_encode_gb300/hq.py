@@ -25,7 +25,8 @@ HQ_FLAG_WORKSPACE_READY = 1
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
             "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
             "hq_encode_noalloc", "hq_payload_bits", "hq_calibrate",
-            "hq_decode_attention_workspace_bytes", "hq_decode_attention")
+            "hq_decode_attention_workspace_bytes", "hq_decode_attention",
+            "hq_decode_gemm_workspace_bytes", "hq_decode_gemm")
 HQ_NOALLOC_MAX_TILES = 1 << 22
 
 
@@ -78,6 +79,10 @@ def _load():
     L.hq_decode_attention.argtypes = [vp, vp, u64, vp, vp, vp, u64, vp, ctypes.c_int, i64, vp,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp, vp, sz,
                                       vp, vp]
+    L.hq_decode_gemm_workspace_bytes.restype = sz
+    L.hq_decode_gemm_workspace_bytes.argtypes = [i64, i64, ctypes.c_int]
+    L.hq_decode_gemm.restype = ctypes.c_int
+    L.hq_decode_gemm.argtypes = [vp, vp, u64, vp, i64, i64, vp, ctypes.c_int, vp, vp, sz, vp, vp]
     L.hq_make_signs.restype = None
     L.hq_make_signs.argtypes = [u64, u64, vp]
     L.hq_status_string.restype = ctypes.c_char_p
@@ -199,6 +204,19 @@ def hq_decode_attention(pk: hq_params, k_stream: torch.Tensor, k_words: int,
         _ptr(v_stream), v_words, _ptr(v_offsets), n_kv_heads, n_tokens, _ptr(q), B, Hq,
         float(scale), _ptr(out), _ptr(probs), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(status), _stream(stream)))
+
+
+def hq_decode_gemm_workspace_bytes(rows: int, cols: int, B: int) -> int:
+    return int(_lib.hq_decode_gemm_workspace_bytes(rows, cols, B))
+
+
+def hq_decode_gemm(p: hq_params, w_stream: torch.Tensor, w_words: int, w_offsets: torch.Tensor,
+                   rows: int, cols: int, x: torch.Tensor, B: int, y: torch.Tensor,
+                   ws: torch.Tensor, status: torch.Tensor, stream=None) -> int:
+    return int(_lib.hq_decode_gemm(ctypes.byref(p), _ptr(w_stream), w_words, _ptr(w_offsets),
+                                   rows, cols, _ptr(x), B, _ptr(y), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _ptr(status),
+                                   _stream(stream)))
 
 
 def hq_make_signs(seed: int, segment: int):

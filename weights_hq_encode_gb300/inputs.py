@@ -125,6 +125,12 @@ def scores_queries(device="cuda", batch: int | None = None, q_heads: int | None 
     return torch.randn((B, H, TILE), generator=g, device=device).to(torch.bfloat16)
 
 
+def activations(batch: int, cols: int, seed: int = 77, device="cuda") -> torch.Tensor:
+    """x [batch, cols] bf16, N(0, 1): the activations multiplied by a weight matrix."""
+    g = _gen(seed, device)
+    return torch.randn((batch, cols), generator=g, device=device).to(torch.bfloat16)
+
+
 def weight_matrix(index: int, device="cuda", rows: int | None = None) -> torch.Tensor:
     """Llama-3.1-8B-shaped linear weight [out, in] bf16 (optionally the first `rows` rows)."""
     out_f, in_f = WEIGHTS8B["shapes"][index]
