@@ -12,7 +12,7 @@ of the cache, which are drawn identically on every device); the first 512
 rows of each weight matrix; the first 16384 tokens of the long-context layer.
 
 Writes ``weights_hq_encode_gb300/calibration.json``.  Run:
-``python -m oracle.calibrate [--only NAME]``.
+``python -m oracle.calibrate [--only NAME] [--lattices E8,A2]``.
 """
 from __future__ import annotations
 
@@ -34,7 +34,7 @@ from weights_hq_encode_gb300 import inputs as I  # noqa: E402
 
 OUT = os.path.join(ROOT, "weights_hq_encode_gb300", "calibration.json")
 TOL = 0.002
-LATTICES = {"E8": O.E8, "D4": O.D4, "Z": O.Z}
+LATTICES = {"E8": O.E8, "D4": O.D4, "A2": O.A2, "Z": O.Z}
 
 
 def rate(x, lattice, k, alpha, dither, seed, signs, tps) -> float:
@@ -76,7 +76,7 @@ def kv_masks(seed_d, seed_s, layer):
     return (O.make_signs(seed_d, 0) ^ O.make_signs(seed_s, layer)).reshape(1, 4)
 
 
-def run(only=None):
+def run(only=None, lattices=None):
     res = json.load(open(OUT)) if os.path.exists(OUT) else {}
     t0 = time.time()
 
@@ -121,8 +121,10 @@ def run(only=None):
         x = np.concatenate([I.bf16_bits(I.kv_slab(I.slab_seed(C["data_seed"], 0, kv), C["kv_heads"],
                                                   16384)).reshape(-1, 128) for kv in (0, 1)])
         m = kv_masks(C["sign_seed"], C["layer_sign_seed"], 0)
-        res["long_context"] = {}
+        res.setdefault("long_context", {})
         for name, lat in LATTICES.items():
+            if lattices and name not in lattices:
+                continue
             res["long_context"][name] = {}
             for target in (1.7, 2.0, 2.5, 3.0):
                 c = calibrate(x, lat, target, 1, C["dither_seed"], m, 1 << 40)
@@ -140,4 +142,6 @@ def run(only=None):
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--only", default=None)
-    run(ap.parse_args().only)
+    ap.add_argument("--lattices", default=None, help="comma-separated subset for long_context")
+    a = ap.parse_args()
+    run(a.only, a.lattices.split(",") if a.lattices else None)

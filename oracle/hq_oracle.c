@@ -48,7 +48,7 @@
 #define RANGE_LIMIT 1048576.0f      /* |y| above 2^20 is a range error */
 #define SYMBOL_LIMIT (1u << 22)     /* no valid symbol reaches 2^22 */
 
-enum { ORA_Z = 1, ORA_D4 = 4, ORA_E8 = 8 };
+enum { ORA_Z = 1, ORA_A2 = 2, ORA_D4 = 4, ORA_E8 = 8 };
 enum {
   ORA_OK = 0, ORA_ERR_INVALID = 1, ORA_ERR_CAPACITY = 4, ORA_ERR_CORRUPT = 8,
   ORA_ERR_RANGE = 32
@@ -205,6 +205,46 @@ void oracle_nearest_e8(const float *y, int32_t *v) {
   }
 }
 
+/* [LAT] A2, the hexagonal lattice of minimal distance 1, with the integer
+ * embedding (m, n) in Z^2, m = n (mod 2), for the point (m / 2, (sqrt 3 / 2) n)
+ * (reading of "integer embedding" for A2: twice the first coordinate and the
+ * second in units of sqrt(3)/2).  A2 is the union of two cosets of the
+ * rectangular lattice Z x sqrt(3) Z, whose nearest points are found by
+ * rounding each coordinate on its own:
+ *   m, n even:  m = 2 rint(x),        n = 2 rint(y c)
+ *   m, n odd:   m = 2 rint(x - 1/2) + 1,  n = 2 rint(y c - 1/2) + 1
+ * with c = fl32(1/sqrt 3).  The nearer one wins; the squared distance of a
+ * candidate is fmaf(dx, dx, fl(dy dy)) with dx = x - fl(m / 2) and
+ * dy = y - fl(h n), h = fl32(sqrt(3) / 2), and exact ties go to the even coset.
+ * Reading: these fp32 constants and this order are part of the definition
+ * (the summary gives none). */
+static const float A2_C = 0.57735026918962576f;   /* fl32(1/sqrt 3) */
+static const float A2_H = 0.86602540378443865f;   /* fl32(sqrt(3)/2) */
+
+float oracle_a2_point_y(int32_t n) { return A2_H * (float)n; }
+
+void oracle_nearest_a2(const float *y, int32_t *v) {
+  int32_t me = 2 * (int32_t)rintf(y[0]);
+  int32_t ne = 2 * (int32_t)rintf(y[1] * A2_C);
+  int32_t mo = 2 * (int32_t)rintf(y[0] - 0.5f) + 1;
+  int32_t no = 2 * (int32_t)rintf(y[1] * A2_C - 0.5f) + 1;
+  float dxe = y[0] - 0.5f * (float)me, dye = y[1] - oracle_a2_point_y(ne);
+  float dxo = y[0] - 0.5f * (float)mo, dyo = y[1] - oracle_a2_point_y(no);
+  float de = fmaf(dxe, dxe, dye * dye);
+  float d_o = fmaf(dxo, dxo, dyo * dyo);
+  if (d_o < de) { v[0] = mo; v[1] = no; }
+  else { v[0] = me; v[1] = ne; }
+}
+
+/* Lattice point of a code vector: the identity for Z, D4 and 2E8; for A2 each
+ * pair (m, n) is the point (m / 2, fl(h n)). */
+void oracle_point(int lattice, const int32_t *v, float *pt, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (lattice == ORA_A2) pt[i] = (i & 1) ? oracle_a2_point_y(v[i]) : 0.5f * (float)v[i];
+    else pt[i] = (float)v[i];
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Subtractive dither [BIAS].                                               */
 /* ------------------------------------------------------------------------ */
@@ -222,7 +262,11 @@ void oracle_nearest_e8(const float *y, int32_t *v) {
  *   D4: u0_i = -1/2 + (b + 1/2) 2^-16 for i < 3, u0_3 = -1 + (b + 1/2) 2^-15
  *       (a fundamental region of D4).
  *   Z : u_i = -1/2 + (b + 1/2) 2^-16, already inside V(Z).
- * All of these values, and u0 - Q(u0), are exact in fp32. */
+ *   A2: per pair, u0_x = -1/2 + (b + 1/2) 2^-16 and
+ *       u0_y = fl(h (-1 + (b' + 1/2) 2^-15)), a point of the box
+ *       [-1/2, 1/2) x [-h, h) (a fundamental region of Z x sqrt(3) Z, i.e. two
+ *       cells of A2, up to the rounding of h); u = fl(u0 - point(Q(u0))).
+ * All of these values except the A2 ones, and u0 - Q(u0), are exact in fp32. */
 void oracle_dither(int lattice, uint64_t seed, uint64_t tile, float *u) {
   uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
   for (uint32_t j = 0; j < 16; ++j) {
@@ -251,6 +295,17 @@ void oracle_dither(int lattice, uint64_t seed, uint64_t tile, float *u) {
         oracle_nearest_d4(u0, lam);
         for (int i = 0; i < 4; ++i) uj[4 * h + i] = u0[i] - (float)lam[i];
       }
+    } else if (lattice == ORA_A2) {
+      for (int h = 0; h < 4; ++h) {
+        float u0[2], pt[2];
+        int32_t lam[2];
+        u0[0] = -0.5f + b[2 * h] * 0x1p-16f;
+        u0[1] = A2_H * (-1.0f + b[2 * h + 1] * 0x1p-15f);
+        oracle_nearest_a2(u0, lam);
+        oracle_point(ORA_A2, lam, pt, 2);
+        uj[2 * h] = u0[0] - pt[0];
+        uj[2 * h + 1] = u0[1] - pt[1];
+      }
     } else {
       for (int i = 0; i < 8; ++i) uj[i] = -0.5f + b[i] * 0x1p-16f;
     }
@@ -278,6 +333,8 @@ static int32_t unzigzag(uint32_t m) {
  *       bit 1 of s_7 (= r): 8 bits per vector = log2 [Z^8 : 2E8].
  *   D4: r = (v_0 + v_1 + v_2) mod 2, t = (v_3 - r)/2; s_i = Z(v_i) (i < 3),
  *       s_3 = 2 Z(t) + r.  Fixed bit: bit 0 of s_3.
+ *   A2: per pair (m, n): p = n mod 2 (= m mod 2), w = (m - p)/2;
+ *       s_0 = Z(n), s_1 = 2 Z(w) + p.  Fixed bit: bit 0 of s_1.
  *   Z : s = Z(v).  Nothing fixed. */
 void oracle_fold(int lattice, const int32_t *v, uint32_t *s, int n) {
   if (lattice == ORA_E8) {
@@ -298,6 +355,13 @@ void oracle_fold(int lattice, const int32_t *v, uint32_t *s, int n) {
       for (int i = 0; i < 3; ++i) s[b + i] = zigzag(v[b + i]);
       s[b + 3] = 2u * zigzag(t) + (uint32_t)r;
     }
+  } else if (lattice == ORA_A2) {
+    for (int b = 0; b < n; b += 2) {
+      int32_t p = v[b + 1] & 1;
+      int32_t w = (v[b] - p) / 2;
+      s[b] = zigzag(v[b + 1]);
+      s[b + 1] = 2u * zigzag(w) + (uint32_t)p;
+    }
   } else {
     for (int i = 0; i < n; ++i) s[i] = zigzag(v[i]);
   }
@@ -312,12 +376,14 @@ int oracle_bit_stripped(int lattice, int coord, int bit, int k) {
     if (bit == 1 && coord == 7) return 1;
   } else if (lattice == ORA_D4) {
     if (bit == 0 && coord == 3) return 1;
+  } else if (lattice == ORA_A2) {
+    if (bit == 0 && coord == 1) return 1;
   }
   return 0;
 }
 
 static int lattice_dim(int lattice) {
-  return lattice == ORA_E8 ? 8 : (lattice == ORA_D4 ? 4 : 1);
+  return lattice == ORA_E8 ? 8 : (lattice == ORA_D4 ? 4 : (lattice == ORA_A2 ? 2 : 1));
 }
 
 /* Inverse of oracle_fold.  Stripped bits arrive as 0 and are restored from
@@ -351,6 +417,16 @@ int oracle_unfold(int lattice, int k, const uint32_t *s_in, int32_t *v, int n) {
       if (oracle_bit_stripped(ORA_D4, 3, 0, k)) s3 |= (uint32_t)r;
       else if ((s3 & 1u) != (uint32_t)r) bad = 1;
       v[b + 3] = 2 * unzigzag(s3 >> 1) + r;
+    }
+  } else if (lattice == ORA_A2) {
+    for (int b = 0; b < n; b += 2) {
+      uint32_t s1 = s_in[b + 1];
+      int32_t nn = unzigzag(s_in[b]);
+      uint32_t p = (uint32_t)nn & 1u;
+      if (oracle_bit_stripped(ORA_A2, 1, 0, k)) s1 |= p;
+      else if ((s1 & 1u) != p) bad = 1;
+      v[b] = 2 * unzigzag(s1 >> 1) + (int32_t)p;
+      v[b + 1] = nn;
     }
   } else {
     for (int i = 0; i < n; ++i) v[i] = unzigzag(s_in[i]);
@@ -425,6 +501,8 @@ int oracle_tile_codes(const ora_params *P, const uint16_t *x, int64_t t,
     for (int b = 0; b < TILE; b += 8) oracle_nearest_e8(y + b, v + b);
   } else if (P->lattice == ORA_D4) {
     for (int b = 0; b < TILE; b += 4) oracle_nearest_d4(y + b, v + b);
+  } else if (P->lattice == ORA_A2) {
+    for (int b = 0; b < TILE; b += 2) oracle_nearest_a2(y + b, v + b);
   } else {
     for (int i = 0; i < TILE; ++i) v[i] = oracle_nearest_z(y[i]);
   }
@@ -440,7 +518,9 @@ void oracle_tile_reconstruct(const ora_params *P, const int32_t *v, int64_t t,
   float u[TILE], z[TILE];
   if (P->dither) oracle_dither(P->lattice, P->dither_seed, P->tile_base + (uint64_t)t, u);
   else for (int i = 0; i < TILE; ++i) u[i] = 0.0f;
-  for (int i = 0; i < TILE; ++i) z[i] = (float)v[i] - u[i];
+  float pt[TILE];
+  oracle_point(P->lattice, v, pt, TILE);
+  for (int i = 0; i < TILE; ++i) z[i] = pt[i] - u[i];
   oracle_fwht128(z);
   float s = oracle_decode_scale(P->alpha);
   for (int i = 0; i < TILE; ++i) {
@@ -549,7 +629,9 @@ static void enc_write(void *c, int64_t gb, int64_t ge) {
 
 static int params_ok(const ora_params *P) {
   if (!P || !P->signs) return 0;
-  if (P->lattice != ORA_Z && P->lattice != ORA_D4 && P->lattice != ORA_E8) return 0;
+  if (P->lattice != ORA_Z && P->lattice != ORA_A2 && P->lattice != ORA_D4 &&
+      P->lattice != ORA_E8)
+    return 0;
   if (P->rice_k < 0 || P->rice_k > 15) return 0;
   if (!(P->alpha > 0.0f) || !isfinite(P->alpha)) return 0;
   if (P->dither != 0 && P->dither != 1) return 0;

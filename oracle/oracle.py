@@ -24,7 +24,7 @@ _LIB = os.path.join(_BUILD, "libhq_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-Z, D4, E8 = 1, 4, 8
+Z, A2, D4, E8 = 1, 2, 4, 8
 OK, ERR_INVALID, ERR_CAPACITY, ERR_CORRUPT, ERR_RANGE = 0, 1, 4, 8, 32
 TILE = 128
 
@@ -72,6 +72,8 @@ def lib():
             L.oracle_fwht128.argtypes = [vp]
             L.oracle_nearest_e8.argtypes = [vp, vp]
             L.oracle_nearest_d4.argtypes = [vp, vp]
+            L.oracle_nearest_a2.argtypes = [vp, vp]
+            L.oracle_point.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int]
             L.oracle_nearest_z.restype = ctypes.c_int32
             L.oracle_nearest_z.argtypes = [ctypes.c_float]
             L.oracle_dither.argtypes = [ctypes.c_int, u64, u64, vp]
@@ -132,6 +134,22 @@ def nearest_d4(y) -> np.ndarray:
     v = np.zeros(4, np.int32)
     lib().oracle_nearest_d4(_p(a), _p(v))
     return v
+
+
+def nearest_a2(y) -> np.ndarray:
+    """Codes (m, n) of the nearest A2 point to y (2 floats)."""
+    a = np.ascontiguousarray(y, dtype=np.float32).reshape(2)
+    v = np.zeros(2, np.int32)
+    lib().oracle_nearest_a2(_p(a), _p(v))
+    return v
+
+
+def point(lattice: int, v) -> np.ndarray:
+    """Lattice point (fp32 coordinates) of a code vector."""
+    a = np.ascontiguousarray(v, dtype=np.int32)
+    pt = np.zeros(a.size, np.float32)
+    lib().oracle_point(lattice, _p(a), _p(pt), a.size)
+    return pt
 
 
 def nearest_z(y: float) -> int:

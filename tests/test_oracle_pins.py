@@ -203,6 +203,45 @@ def test_d4_and_z_nearest_point_brute_force(oracle):
         assert oracle.nearest_z(t) == int(np.round(t))       # numpy rounds half to even
 
 
+def test_a2_nearest_point_brute_force(oracle):
+    """Hexagonal lattice {(m/2, (sqrt 3/2) n) : m = n mod 2}: the oracle's
+    point is the nearest one of a window of candidates (exact sqrt 3 in fp64),
+    except where two candidates are within 1e-5 of equally near."""
+    rng = np.random.default_rng(11)
+    y = (rng.standard_normal((4000, 2)) * 4).astype(np.float32).astype(np.float64)
+    h = np.sqrt(3.0) / 2
+    v = np.stack([oracle.nearest_a2(r) for r in y])
+    assert ((v[:, 0] - v[:, 1]) % 2 == 0).all()
+    m0, n0 = np.floor(2 * y[:, 0]), np.floor(y[:, 1] / h)
+    dm, dn = np.meshgrid(np.arange(-3, 4), np.arange(-3, 4), indexing="ij")
+    M = m0[:, None] + dm.reshape(-1)[None]
+    N = n0[:, None] + dn.reshape(-1)[None]
+    d = (M / 2 - y[:, :1]) ** 2 + (N * h - y[:, 1:]) ** 2
+    d[((M - N) % 2) != 0] = np.inf
+    order = np.sort(d, axis=1)
+    clear = order[:, 1] - order[:, 0] > 1e-5
+    best = np.argmin(d, axis=1)
+    bm, bn = M[np.arange(len(y)), best], N[np.arange(len(y)), best]
+    assert clear.mean() > 0.99
+    assert (v[clear, 0] == bm[clear]).all() and (v[clear, 1] == bn[clear]).all()
+
+
+def test_a2_fold_round_trip_and_parity_copy(oracle):
+    vals = np.arange(-21, 22)
+    g = np.stack(np.meshgrid(vals, vals, indexing="ij"), -1).reshape(-1, 2)
+    v = g[((g[:, 0] - g[:, 1]) % 2) == 0].astype(np.int32)
+    s = oracle.fold(2, v.reshape(-1))
+    assert (s.reshape(-1, 2)[:, 1] & 1 == v[:, 1] & 1).all()       # bit 0 of s_1 = parity
+    for k in range(0, 4):
+        back, rc = oracle.unfold(2, k, _strip(2, s, k, oracle))
+        assert rc == 0 and (back.reshape(-1, 2) == v).all()
+    bad = oracle.fold(2, np.array([1, 3], np.int32))
+    bad[1] ^= 1                                                # break the copy of p
+    assert oracle.unfold(2, 0, bad)[1] == oracle.ERR_CORRUPT
+    pt = oracle.point(2, np.array([3, -1], np.int32))
+    assert pt[0] == 1.5 and abs(pt[1] + np.sqrt(3) / 2) < 1e-7
+
+
 # ------------------------------------------------------------------ dither
 def _voronoi_check_e8(u):
     """u must be at least as close to 0 as to any lattice point."""
@@ -210,15 +249,17 @@ def _voronoi_check_e8(u):
     return d0 <= _brute_e8_min(u.astype(np.float64)) + 1e-9
 
 
-@pytest.mark.parametrize("lat", [8, 4, 1])
+@pytest.mark.parametrize("lat", [8, 4, 2, 1])
 def test_dither_in_voronoi_cell_with_right_second_moment(oracle, lat):
     gold = {r[0]: float(r[3]) for r in _read_table("lattice_nsm.txt")}
-    target = {8: gold["E8"], 4: gold["D4"], 1: gold["Z"]}[lat]
+    target = {8: gold["E8"], 4: gold["D4"], 2: gold["A2"], 1: gold["Z"]}[lat]
     u = np.stack([oracle.dither(lat, 99, t) for t in range(600)]).reshape(-1, lat if lat > 1 else 1)
     if lat == 8:
         assert _voronoi_check_e8(u).all()
     elif lat == 4:
         assert (np.stack([oracle.nearest_d4(r) for r in u[:4000]]) == 0).all()
+    elif lat == 2:
+        assert (np.stack([oracle.nearest_a2(r) for r in u[:4000]]) == 0).all()
     else:
         assert (np.abs(u) < 0.5).all()
     m = (u.astype(np.float64) ** 2).mean()
@@ -229,7 +270,7 @@ def test_dither_in_voronoi_cell_with_right_second_moment(oracle, lat):
     assert not (oracle.dither(lat, 99, 5) == oracle.dither(lat, 99, 6)).all()
 
 
-@pytest.mark.parametrize("lat,name", [(8, "E8"), (4, "D4"), (1, "Z")])
+@pytest.mark.parametrize("lat,name", [(8, "E8"), (4, "D4"), (2, "A2"), (1, "Z")])
 def test_dithered_error_second_moment(oracle, lat, name):
     """With subtractive dither the error v - u - y is uniform on the Voronoi
     cell, so its per-dimension mean square is G(Lambda) det^(2/n)."""
@@ -247,7 +288,8 @@ def test_dithered_error_second_moment(oracle, lat, name):
     H = scipy_linalg.hadamard(128).astype(np.float64)
     y = (xb @ H.T) * (alpha / np.sqrt(128.0))
     u = np.stack([oracle.dither(lat, 1234, t) for t in range(n_tiles)]).astype(np.float64)
-    e = enc["codes"] - u - y
+    pts = oracle.point(lat, enc["codes"].reshape(-1)).reshape(enc["codes"].shape)
+    e = pts.astype(np.float64) - u - y
     dim = lat if lat > 1 else 1
     per_vec = (e.reshape(-1, dim) ** 2).mean(-1)
     m, se = per_vec.mean(), per_vec.std() / np.sqrt(per_vec.size)
@@ -256,7 +298,9 @@ def test_dithered_error_second_moment(oracle, lat, name):
 
 def test_nsm_ordering(oracle):
     gold = {r[0]: float(r[1]) for r in _read_table("lattice_nsm.txt")}
-    assert gold["E8"] < gold["D4"] < gold["Z"]
+    assert gold["E8"] < gold["D4"] < gold["A2"] < gold["Z"]
+    assert abs(gold["A2"] - 5 / (36 * np.sqrt(3))) < 1e-9
+    assert abs(gold["A2"] * np.sqrt(3) / 2 - 5 / 72) < 1e-9
 
 
 # ------------------------------------------------------------ fold / strip
@@ -271,7 +315,7 @@ def _all_2e8(limit):
 
 
 def _strip(lattice, s, k, oracle):
-    dim = {8: 8, 4: 4, 1: 1}[lattice]
+    dim = {8: 8, 4: 4, 2: 2, 1: 1}[lattice]
     s = s.copy().reshape(-1, dim)
     for c in range(dim):
         for b in range(k):
@@ -344,7 +388,7 @@ def test_unstripped_parity_copies_are_checked(oracle):
 # ------------------------------------------------------------ stream layout
 def _parse_stream_py(stream, offsets, n_tiles, lattice, k, oracle):
     """Independent reader of the documented layout (pure Python)."""
-    dim = {8: 8, 4: 4, 1: 1}[lattice]
+    dim = {8: 8, 4: 4, 2: 2, 1: 1}[lattice]
     syms = np.zeros((n_tiles, 128), np.int64)
     words = [int(w) for w in stream]
 
@@ -375,7 +419,7 @@ def _parse_stream_py(stream, offsets, n_tiles, lattice, k, oracle):
     return syms
 
 
-@pytest.mark.parametrize("lat,k", [(8, 2), (8, 0), (4, 1), (1, 3)])
+@pytest.mark.parametrize("lat,k", [(8, 2), (8, 0), (4, 1), (2, 1), (1, 3)])
 def test_stream_layout_and_tile_length_closed_form(oracle, lat, k):
     from weights_hq_encode_gb300 import inputs as I
     x = I.bf16_bits(I.tiny_kv())[:70]                          # 3 groups, ragged tail
@@ -383,7 +427,7 @@ def test_stream_layout_and_tile_length_closed_form(oracle, lat, k):
     enc = oracle.encode(P, x, want_codes=True)
     assert enc["status"] == 0
     s = oracle.fold(lat, enc["codes"].reshape(-1)).reshape(-1, 128).astype(np.int64)
-    dim = {8: 8, 4: 4, 1: 1}[lat]
+    dim = {8: 8, 4: 4, 2: 2, 1: 1}[lat]
     stripped = sum(oracle.bit_stripped(lat, c, b, k) for c in range(dim) for b in range(k))
     closed = ((s >> k) + 1 + k).sum(-1) - (128 // dim) * stripped
     assert (enc["tile_bits"] == closed).all()
