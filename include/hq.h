@@ -62,14 +62,16 @@ enum {
                            was coded as an all-zero tile */
 };
 
-enum { HQ_Z = 1, HQ_D4 = 4, HQ_E8 = 8 };      /* lattice = its dimension */
+enum { HQ_Z = 1, HQ_A2 = 2, HQ_D4 = 4, HQ_E8 = 8 };   /* lattice = its dimension */
 enum { HQ_OUT_BF16 = 0, HQ_OUT_F32 = 1 };
 
 #define HQ_TILE 128
 #define HQ_GROUP_TILES 32
 
 /* Codec parameters, identical for the encode and decode of one stream.
- *   lattice            HQ_E8 (2E8 in Z^8), HQ_D4 or HQ_Z.
+ *   lattice            HQ_E8 (2E8 in Z^8), HQ_D4, HQ_A2 (hexagonal lattice,
+ *                      codes (m, n) with m = n mod 2 for the point
+ *                      (m/2, (sqrt 3/2) n)) or HQ_Z.
  *   rice_k             Rice parameter, 0..15.
  *   alpha              > 0: lattice units per unit of the orthonormal RHT
  *                      (H / sqrt(128)) output.

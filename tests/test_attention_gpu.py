@@ -98,8 +98,10 @@ def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8):
     from weights_hq_encode_gb300 import inputs as I
     C = I.SCORES
     cal = calibration()
-    ck = cal["kv_cache_8b"]["E8"]["3.0"] if lat_k == 8 else cal["long_context"]["D4"]["2.5"]
-    cv = cal["kv_cache_8b"]["E8"]["2.0"] if lat_v == 8 else cal["long_context"]["Z"]["2.0"]
+    other = {4: cal["long_context"]["D4"]["2.5"], 1: cal["long_context"]["Z"]["2.0"],
+             2: dict(k=1, alpha=cal["long_context"]["D4"]["2.5"]["alpha"])}
+    ck = cal["kv_cache_8b"]["E8"]["3.0"] if lat_k == 8 else other[lat_k]
+    cv = cal["kv_cache_8b"]["E8"]["2.0"] if lat_v == 8 else other[lat_v]
     kb = _bits(I.scores_keys("cpu", tokens=T)[:n_kv])
     vb = _bits(I.scores_values("cpu", tokens=T)[:n_kv])
     n = n_kv * T
@@ -116,6 +118,7 @@ def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8):
     (2, 64, 20, 8, 8, 8),        # 80 query rows per head: two row tiles
     (1, 1, 1, 1, 8, 8),          # one token
     (3, 700, 2, 6, 4, 1),        # D4 keys, Z values
+    (2, 160, 2, 4, 2, 2),        # A2 keys and values
 ])
 def test_attention_against_oracle(hq, oracle, n_kv, T, B, Hq, lat_k, lat_v):
     from oracle import attention as A

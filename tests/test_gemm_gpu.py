@@ -75,13 +75,14 @@ def _check(G, what, xb, rows, cols, y):
     (3, 100, 17, "5.0", 8, 1),    # 4096 columns, three batch chunks, dither on
     (1, 50, 3, "4.0", 4, 0),      # D4
     (0, 20, 2, "4.0", 1, 0),      # Z
+    (1, 24, 4, "4.0", 2, 1),      # A2, dither on
 ])
 def test_gemm_against_oracle(hq, oracle, index, rows, B, rate, lattice, dither):
     from oracle import gemm as G
     from weights_hq_encode_gb300 import inputs as I
     cols = I.WEIGHTS8B["shapes"][index][1]
     c = calibration()["weights_8b"]["E8"][rate][index]
-    alpha = c["alpha"] if lattice == 8 else c["alpha"] * (0.5 if lattice == 4 else 0.35)
+    alpha = c["alpha"] if lattice == 8 else c["alpha"] * {4: 0.5, 2: 0.45, 1: 0.35}[lattice]
     wb = _bits(I.weight_matrix(index, "cpu", rows=rows))
     p, stream, words, offsets, what, _s = _weights(oracle, hq, wb, rows, cols, lattice, c["k"],
                                                    alpha, dither, 901)

@@ -78,6 +78,10 @@ CASES = [
     (4, 0, 0.8, 1, 65, 2, 0),
     (4, 1, 1.3, 1, 200, 1, 7),
     (4, 3, 6.0, 0, 31, 1, 0),
+    (2, 0, 0.9, 1, 90, 1, 0),         # A2 (hexagonal), parity copies written at k = 0
+    (2, 1, 1.5, 1, 260, 2, 11),
+    (2, 3, 5.0, 0, 47, 1, 0),
+    (2, 6, 120.0, 1, 33, 1, 0),       # generic-width remainders
     (1, 0, 0.3, 1, 100, 1, 0),
     (1, 2, 2.0, 1, 257, 3, 99),
     (1, 4, 16.0, 0, 64, 1, 0),
@@ -305,7 +309,7 @@ def test_long_context_sweep_sampled(hq, oracle):
     mask = (oracle.make_signs(C["sign_seed"], 0) ^ oracle.make_signs(C["layer_sign_seed"], 0))
     mask = mask.reshape(1, 4)
     signs = torch.from_numpy(mask.view(np.int32).copy()).cuda()
-    for name, lat in (("Z", 1), ("D4", 4), ("E8", 8)):
+    for name, lat in (("Z", 1), ("A2", 2), ("D4", 4), ("E8", 8)):
         for rate in ("1.7", "2.0", "2.5", "3.0"):
             c = cal[name][rate]
             p = hq.make_params(lat, c["k"], c["alpha"], 1, C["dither_seed"], signs, 1 << 40)

@@ -14,7 +14,7 @@ using namespace hq;
 
 constexpr uint32_t kDefaultSpins = 1u << 20;   // ~0.3 s of polling per predecessor
 
-bool lattice_ok(int l) { return l == HQ_Z || l == HQ_D4 || l == HQ_E8; }
+bool lattice_ok(int l) { return l == HQ_Z || l == HQ_A2 || l == HQ_D4 || l == HQ_E8; }
 
 int rbits_of(int lattice, int k) {
   // kept remainder bits per tile: 128 k minus the membership-fixed low bits
@@ -23,6 +23,7 @@ int rbits_of(int lattice, int k) {
     int strip = 0;
     if (lattice == HQ_E8) strip = (c == 0) ? 0 : (c == 7 ? (k < 2 ? k : 2) : (k < 1 ? k : 1));
     else if (lattice == HQ_D4) strip = ((c & 3) == 3) ? (k < 1 ? k : 1) : 0;
+    else if (lattice == HQ_A2) strip = (c & 1) ? (k < 1 ? k : 1) : 0;
     per8 += k - strip;
   }
   return per8 * 16;

@@ -255,12 +255,10 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[i] = 0.0f;
       }
+      float fv[8];
+      point8<LAT>(v, fv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        // exact int -> float for |v| < 2^22 (magic-number conversion)
-        const float fv = __fsub_rn(__int_as_float(0x4B400000 + v[i]), kMagic1);
-        e[8 * jj + i] = __fsub_rn(fv, u[i]);
-      }
+      for (int i = 0; i < 8; ++i) e[8 * jj + i] = __fsub_rn(fv[i], u[i]);
     }
     if (slow && posj != stop) lbad = true;       // bit after the last code
   }
@@ -746,6 +744,7 @@ int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st) {
   switch (lattice) {
     case 8: launch_dec_lat<8>(a, st); break;
     case 4: launch_dec_lat<4>(a, st); break;
+    case 2: launch_dec_lat<2>(a, st); break;
     default: launch_dec_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
@@ -758,6 +757,7 @@ int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
   switch (lattice) {
     case 8: launch_qk_lat<8>(a, st); break;
     case 4: launch_qk_lat<4>(a, st); break;
+    case 2: launch_qk_lat<2>(a, st); break;
     default: launch_qk_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
@@ -771,6 +771,7 @@ int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cud
   switch (v_lattice) {
     case 8: launch_pv_lat<8>(a, st); break;
     case 4: launch_pv_lat<4>(a, st); break;
+    case 2: launch_pv_lat<2>(a, st); break;
     default: launch_pv_lat<1>(a, st); break;
   }
   if (cudaGetLastError() != cudaSuccess) return 1;
@@ -785,6 +786,7 @@ int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {
   switch (lattice) {
     case 8: launch_gemm_lat<8>(a, st); break;
     case 4: launch_gemm_lat<4>(a, st); break;
+    case 2: launch_gemm_lat<2>(a, st); break;
     default: launch_gemm_lat<1>(a, st); break;
   }
   if (cudaGetLastError() != cudaSuccess) return 1;

@@ -153,6 +153,28 @@ __device__ __forceinline__ int32_t nearest_z(float y) {
   return (int32_t)(fbits(__fadd_rn(y, kMagic1)) - fbits(kMagic1));
 }
 
+// A2 (hexagonal, minimal distance 1) as codes (m, n), m = n mod 2, for the
+// point (m / 2, h n): the nearer of the two cosets of Z x sqrt(3) Z, each
+// rounded coordinate by coordinate (c = fl32(1/sqrt 3), h = fl32(sqrt(3)/2));
+// exact ties go to the coset with m, n even.
+constexpr float kA2C = 0x1.279a74p-1f;           // fl32(1/sqrt 3)
+constexpr float kA2H = 0x1.bb67aep-1f;           // fl32(sqrt(3)/2)
+__device__ __forceinline__ float a2_px(int32_t m) { return __fmul_rn(0.5f, __int2float_rn(m)); }
+__device__ __forceinline__ float a2_py(int32_t n) { return __fmul_rn(kA2H, __int2float_rn(n)); }
+__device__ __forceinline__ void nearest_a2(float x, float y, int32_t &m, int32_t &n) {
+  const float yc = __fmul_rn(y, kA2C);
+  const int32_t me = 2 * __float2int_rn(x), ne = 2 * __float2int_rn(yc);
+  const int32_t mo = 2 * __float2int_rn(__fsub_rn(x, 0.5f)) + 1;
+  const int32_t no = 2 * __float2int_rn(__fsub_rn(yc, 0.5f)) + 1;
+  const float dxe = __fsub_rn(x, a2_px(me)), dye = __fsub_rn(y, a2_py(ne));
+  const float dxo = __fsub_rn(x, a2_px(mo)), dyo = __fsub_rn(y, a2_py(no));
+  const float de = __fmaf_rn(dxe, dxe, __fmul_rn(dye, dye));
+  const float dd = __fmaf_rn(dxo, dxo, __fmul_rn(dyo, dyo));
+  const bool odd = dd < de;
+  m = odd ? mo : me;
+  n = odd ? no : ne;
+}
+
 // ---------------------------------------------------------------- dither
 // a * sign(e): the sign bit of e flips a (e is never zero here).
 __device__ __forceinline__ float mulsign(float a, float e) {
@@ -226,6 +248,18 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
         open = open && !hit;
         u[4 * h + i] = hit ? __fsub_rn(e[i], mulsign(1.0f, e[i])) : e[i];
       }
+    }
+  } else if (LAT == 2) {
+    // pair m: u0 = (-1/2 + (b + 1/2) 2^-16, fl(h (-1 + (b' + 1/2) 2^-15))) on
+    // the box [-1/2, 1/2) x [-h, h), two cells of A2; u = u0 - point(Q(u0))
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float x0 = __fadd_rn(grid_lo(w[m]), kGrid16);
+      const float y0 = __fmul_rn(kA2H, __fmaf_rn(grid_hi(w[m]), 2.0f, kGrid15));
+      int32_t qm, qn;
+      nearest_a2(x0, y0, qm, qn);
+      u[2 * m] = __fsub_rn(x0, a2_px(qm));
+      u[2 * m + 1] = __fsub_rn(y0, a2_py(qn));
     }
   } else {
 #pragma unroll
@@ -310,6 +344,16 @@ __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) 
       s[4 * h + 2] = zigzag(v[2]);
       s[4 * h + 3] = 2u * zigzag(t) + (uint32_t)r;
     }
+  } else if (LAT == 2) {
+    // pair (m, n): p = n mod 2, w = (m - p)/2; s_0 = Z(n), s_1 = 2 Z(w) + p
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      int32_t m, n;
+      nearest_a2(y[2 * h], y[2 * h + 1], m, n);
+      const int32_t p = n & 1;
+      s[2 * h] = zigzag(n);
+      s[2 * h + 1] = 2u * zigzag((m - p) >> 1) + (uint32_t)p;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i] = zigzag(nearest_z(y[i]));
@@ -326,6 +370,8 @@ __device__ __host__ __forceinline__ constexpr int stripped_low_bits(int c, int k
     return k < 1 ? k : 1;
   } else if (LAT == 4) {
     return ((c & 3) == 3) ? (k < 1 ? k : 1) : 0;
+  } else if (LAT == 2) {
+    return (c & 1) ? (k < 1 ? k : 1) : 0;
   }
   return 0;
 }
@@ -364,9 +410,32 @@ __device__ __forceinline__ void unfold8(uint32_t s[8], int k, int32_t v[8], bool
       else if ((q[3] & 1u) != (uint32_t)r) *bad = true;
       o[3] = 2 * unzigzag(q[3] >> 1) + r;
     }
+  } else if (LAT == 2) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int32_t n = unzigzag(s[2 * h]);
+      const uint32_t p = (uint32_t)n & 1u;
+      uint32_t s1 = s[2 * h + 1];
+      if (k >= 1) s1 |= p;
+      else if ((s1 & 1u) != p) *bad = true;
+      v[2 * h] = 2 * unzigzag(s1 >> 1) + (int32_t)p;
+      v[2 * h + 1] = n;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = unzigzag(s[i]);
+  }
+}
+
+// Lattice point of 8 codes: the identity for Z, D4 and 2E8 (exact int ->
+// float for |v| < 2^22 by the magic-number conversion); for A2 each pair
+// (m, n) is (m / 2, fl(h n)).
+template <int LAT>
+__device__ __forceinline__ void point8(const int32_t v[8], float fv[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (LAT == 2) fv[i] = (i & 1) ? a2_py(v[i]) : a2_px(v[i]);
+    else fv[i] = __fsub_rn(__int_as_float(0x4B400000 + v[i]), kMagic1);
   }
 }
 

@@ -471,6 +471,7 @@ int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st) {
   switch (lattice) {
     case 8: launch_lat<8>(a, st); break;
     case 4: launch_lat<4>(a, st); break;
+    case 2: launch_lat<2>(a, st); break;
     default: launch_lat<1>(a, st); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 1;

@@ -17,7 +17,7 @@ from . import build as _build
 
 HQ_OK, HQ_ERR_INVALID, HQ_ERR_CUDA, HQ_ERR_CAPACITY = 0, 1, 2, 4
 HQ_ERR_CORRUPT, HQ_ERR_TIMEOUT, HQ_ERR_RANGE = 8, 16, 32
-HQ_Z, HQ_D4, HQ_E8 = 1, 4, 8
+HQ_Z, HQ_A2, HQ_D4, HQ_E8 = 1, 2, 4, 8
 HQ_OUT_BF16, HQ_OUT_F32 = 0, 1
 HQ_TILE, HQ_GROUP_TILES = 128, 32
 HQ_FLAG_WORKSPACE_READY = 1
