@@ -10,7 +10,9 @@
 // Bit lengths are scanned across the 8 lanes of a tile and the 32 tiles of
 // the group; groups are chained by a decoupled look-back (Merrill & Garland
 // 2016) with bounded waits.  The group's words are assembled in shared memory
-// and stored with coalesced 32-bit writes.
+// by all warps; then warps 1-7 exit, so that their slots go to the next
+// block, while warp 0 alone waits for the predecessors' prefix and stores
+// the words with coalesced 32-bit writes.
 #include <cuda_runtime.h>
 
 #include "hq_device.cuh"
@@ -362,8 +364,9 @@ encode_kernel(EncodeArgs a) {
   const int64_t u_pos = (int64_t)nt * (int64_t)R + (int64_t)s_tile_uoff[tl] + u_in_tile;
   const bool one_window = gwords <= (uint64_t)kStageWords;
 
-  // ---- warp 0 waits for the predecessors while the other warps assemble
-  if (tid < 32) {
+  // ---- groups larger than the staging window: warp 0 waits for the
+  // predecessors first, then every window is assembled and copied out
+  if (!one_window && tid < 32) {
     uint64_t excl = 0;
     const bool ok = lookback_warp(state, g, gwords, a.spins, &excl);
     if (tid == 0) {
@@ -438,6 +441,32 @@ encode_kernel(EncodeArgs a) {
       o.finish();
     }
     __syncthreads();
+    if (one_window) {
+      // warps 1..7 are done and leave (their slots go to the next block);
+      // warp 0 alone waits for the predecessors and copies the group out
+      if (tid >= 32) return;
+      uint64_t excl = 0;
+      const bool ok = lookback_warp(state, g, gwords, a.spins, &excl);
+      excl = __shfl_sync(0xffffffffu, excl, 0);
+      if (tid == 0) {
+        if (!ok) {
+          atomicOr(a.status, (uint32_t)HQ_ERR_TIMEOUT);
+        } else {
+          if (a.offsets != nullptr) {
+            a.offsets[g] = excl;
+            if ((int64_t)g == a.n_groups - 1) a.offsets[a.n_groups] = excl + gwords;
+          }
+          if (excl + gwords > a.cap_words) atomicOr(a.status, (uint32_t)HQ_ERR_CAPACITY);
+          if (s_flags) atomicOr(a.status, s_flags);
+        }
+      }
+      if (!ok || a.stream == nullptr) return;
+      for (int64_t i = tid; i < (int64_t)gwords; i += 32) {
+        const uint64_t gw = excl + (uint64_t)i;
+        if (gw < a.cap_words) a.stream[gw] = s_stage[i];
+      }
+      return;
+    }
     if (!s_ok || a.stream == nullptr) return;
     const uint64_t base = s_base;
     const int64_t nw = min((int64_t)kStageWords, (int64_t)gwords - cb);
