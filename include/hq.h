@@ -88,7 +88,11 @@ enum { HQ_OUT_BF16 = 0, HQ_OUT_F32 = 1 };
  *                      predecessor in the encoder's cross-block scan, after
  *                      which HQ_ERR_TIMEOUT is raised.
  *   flags              bit 0 (HQ_FLAG_WORKSPACE_READY): the caller has zeroed
- *                      the encode workspace itself; hq_encode skips its memset. */
+ *                      the encode workspace itself; hq_encode skips its memset
+ *                      and the encoder blocks take their groups from the
+ *                      workspace's ticket counter (one atomic per block)
+ *                      rather than from their launch index; the output is
+ *                      the same. */
 typedef struct hq_params {
   int32_t lattice;
   int32_t rice_k;

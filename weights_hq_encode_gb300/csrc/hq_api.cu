@@ -139,6 +139,7 @@ int encode_impl(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32
   a.dither = p->dither;
   a.spins = p->lookback_spins ? p->lookback_spins : kDefaultSpins;
   a.payload_bits = d_bits;
+  a.use_ticket = (p->flags & HQ_FLAG_WORKSPACE_READY) ? 1 : 0;
   if (!(p->flags & HQ_FLAG_WORKSPACE_READY)) {
     if (cudaMemsetAsync(d_ws, 0, hq_encode_workspace_bytes(n_tiles), st) != cudaSuccess)
       return HQ_ERR_CUDA;

@@ -230,20 +230,34 @@ encode_kernel(EncodeArgs a) {
 
   const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
   uint64_t *state = reinterpret_cast<uint64_t *>(a.ws) + 1;
-  if (tid == 0) {
-    s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
-    s_flags = 0u;
+  // This block's group.  Blocks start in index order, so every predecessor
+  // of a waiting block has started and the look-back always progresses; with
+  // a caller-prepared workspace the group comes from its ticket counter
+  // instead (a counter set ahead leaves groups unprocessed, which the
+  // bounded waits turn into HQ_ERR_TIMEOUT).
+  uint32_t g = blockIdx.x;
+  if (a.use_ticket) {                            // uniform over the grid
+    if (tid == 0) s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
+    __syncthreads();
+    g = s_ticket;
   }
+  if (tid == 0) s_flags = 0u;
 #pragma unroll
   for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
-  __syncthreads();
-  const uint32_t g = s_ticket;                   // this block's group
-  if (g >= a.n_blocks) return;                   // only with a pre-filled ticket
+  if (g >= a.n_blocks) return;                   // only with a counter set ahead
   const int k = K >= 0 ? K : a.rice_k;
   const int64_t t0 = (int64_t)g * kGroupTiles;
   const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
   const int64_t t = t0 + tl;
   const bool valid = tl < nt;
+  // the lane's 16 bf16 coordinates, loaded before the sign table is built so
+  // that the two loads overlap
+  uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+  if (valid) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
+    v0 = __ldg(src);
+    v1 = __ldg(src + 1);
+  }
   // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
   const int64_t seg0 = div_by(t0, a.tiles_per_segment, a.seg_shift);
   if (tid < kTile / 2) {
@@ -253,11 +267,9 @@ encode_kernel(EncodeArgs a) {
   }
   __syncthreads();
 
-  // ---- load 16 bf16 coordinates, sign mask, FWHT
+  // ---- sign mask, FWHT
   float x[16];
   if (valid) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
-    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
     uint32_t sw[8];
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
       const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];

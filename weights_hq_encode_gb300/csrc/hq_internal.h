@@ -39,6 +39,7 @@ struct EncodeArgs {
   int dither;
   uint32_t spins;
   unsigned long long *payload_bits;   // non-null: add each group's Rice bits here
+  int use_ticket;           // groups from the workspace's ticket counter, not blockIdx
 };
 
 struct DecodeArgs {
