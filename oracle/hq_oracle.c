@@ -65,6 +65,7 @@ typedef struct {
   uint64_t tile_base;         /* global index of the first tile of the call */
   const uint32_t *signs;      /* [n_segments][4] sign masks, bit set = -1 */
   int64_t tiles_per_segment;  /* tile t uses mask t / tiles_per_segment */
+  const float *rot;           /* NULL, or [n_segments][128][128] row-major R */
 } ora_params;
 
 /* ------------------------------------------------------------------------ */
@@ -453,6 +454,37 @@ static const uint32_t *tile_mask(const ora_params *P, int64_t t) {
 }
 static int mask_bit(const uint32_t *m, int i) { return (int)((m[i >> 5] >> (i & 31)) & 1u); }
 
+/* [BIAS] The per-layer rotation may be a full Haar-uniform (QJL) orthogonal
+ * matrix instead of the cheap +-1 diagonal.  Reading: R (one per segment,
+ * row-major fp32) is applied to the tile before the sign diagonal and the
+ * Hadamard transform, RHT(R x); every output is one fused multiply-add chain
+ * over the inputs in index order, starting from +0:
+ *   z_i = fmaf(R[i][127], x[127], ... fmaf(R[i][1], x[1], fmaf(R[i][0], x[0], 0)))
+ * and the decoder applies the transpose the same way (over i for each j),
+ * after the inverse Hadamard transform and the sign diagonal. */
+static const float *tile_rot(const ora_params *P, int64_t t) {
+  int64_t seg = P->tiles_per_segment > 0 ? t / P->tiles_per_segment : 0;
+  return P->rot + seg * TILE * TILE;
+}
+void oracle_rotate(const float *R, const float *x, float *out) {
+  float z[TILE];
+  for (int i = 0; i < TILE; ++i) {
+    float acc = 0.0f;
+    for (int j = 0; j < TILE; ++j) acc = fmaf(R[i * TILE + j], x[j], acc);
+    z[i] = acc;
+  }
+  memcpy(out, z, sizeof z);
+}
+void oracle_rotate_t(const float *R, const float *y, float *out) {
+  float z[TILE];
+  for (int j = 0; j < TILE; ++j) {
+    float acc = 0.0f;
+    for (int i = 0; i < TILE; ++i) acc = fmaf(R[i * TILE + j], y[i], acc);
+    z[j] = acc;
+  }
+  memcpy(out, z, sizeof z);
+}
+
 static float bf16_to_float(uint16_t h) {
   uint32_t bits = (uint32_t)h << 16;
   float f;
@@ -481,11 +513,10 @@ float oracle_decode_scale(float alpha) { return (float)(1.0 / ((double)alpha * s
 int oracle_tile_codes(const ora_params *P, const uint16_t *x, int64_t t,
                       int32_t *v) {
   const uint32_t *m = tile_mask(P, t);
-  float z[TILE], u[TILE], y[TILE];
-  for (int i = 0; i < TILE; ++i) {
-    float f = bf16_to_float(x[i]);
-    z[i] = mask_bit(m, i) ? -f : f;
-  }
+  float z[TILE], u[TILE], y[TILE], xf[TILE];
+  for (int i = 0; i < TILE; ++i) xf[i] = bf16_to_float(x[i]);
+  if (P->rot) oracle_rotate(tile_rot(P, t), xf, xf);
+  for (int i = 0; i < TILE; ++i) z[i] = mask_bit(m, i) ? -xf[i] : xf[i];
   oracle_fwht128(z);
   if (P->dither) oracle_dither(P->lattice, P->dither_seed, P->tile_base + (uint64_t)t, u);
   else for (int i = 0; i < TILE; ++i) u[i] = 0.0f;
@@ -527,6 +558,7 @@ void oracle_tile_reconstruct(const ora_params *P, const int32_t *v, int64_t t,
     float r = z[i] * s;
     out[i] = mask_bit(m, i) ? -r : r;
   }
+  if (P->rot) oracle_rotate_t(tile_rot(P, t), out, out);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -45,7 +45,8 @@ class Params(ctypes.Structure):
     _fields_ = [("lattice", ctypes.c_int32), ("rice_k", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("dither", ctypes.c_int32),
                 ("dither_seed", ctypes.c_uint64), ("tile_base", ctypes.c_uint64),
-                ("signs", ctypes.c_void_p), ("tiles_per_segment", ctypes.c_int64)]
+                ("signs", ctypes.c_void_p), ("tiles_per_segment", ctypes.c_int64),
+                ("rot", ctypes.c_void_p)]
 
 
 def _p(a):
@@ -78,6 +79,8 @@ def lib():
             L.oracle_nearest_z.argtypes = [ctypes.c_float]
             L.oracle_dither.argtypes = [ctypes.c_int, u64, u64, vp]
             L.oracle_fold.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int]
+            L.oracle_rotate.argtypes = [vp, vp, vp]
+            L.oracle_rotate_t.argtypes = [vp, vp, vp]
             L.oracle_unfold.restype = ctypes.c_int
             L.oracle_unfold.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int]
             L.oracle_bit_stripped.restype = ctypes.c_int
@@ -152,6 +155,15 @@ def point(lattice: int, v) -> np.ndarray:
     return pt
 
 
+def rotate(R, x, transpose=False) -> np.ndarray:
+    """R x (or R^T x) as the codec's fixed-order fp32 FMA chains."""
+    Rm = np.ascontiguousarray(R, dtype=np.float32).reshape(128, 128)
+    xv = np.ascontiguousarray(x, dtype=np.float32).reshape(128)
+    out = np.zeros(128, np.float32)
+    (lib().oracle_rotate_t if transpose else lib().oracle_rotate)(_p(Rm), _p(xv), _p(out))
+    return out
+
+
 def nearest_z(y: float) -> int:
     return int(lib().oracle_nearest_z(float(y)))
 
@@ -201,11 +213,15 @@ GROUP_TILES = 32
 
 # ----------------------------------------------------------------- codec
 def make_params(lattice, rice_k, alpha, dither, dither_seed, signs, tiles_per_segment,
-                tile_base=0):
+                tile_base=0, rot=None):
+    """rot: None, or [n_segments][128][128] fp32 row-major rotations R (the
+    tile is coded as RHT(R x))."""
     signs = np.ascontiguousarray(signs, dtype=np.uint32).reshape(-1, 4)
+    R = None if rot is None else np.ascontiguousarray(rot, dtype=np.float32).reshape(-1, 128, 128)
     P = Params(lattice, rice_k, alpha, dither, dither_seed, tile_base,
-               ctypes.c_void_p(signs.ctypes.data), tiles_per_segment)
-    P._keep = signs          # keep the mask array alive with the struct
+               ctypes.c_void_p(signs.ctypes.data), tiles_per_segment,
+               ctypes.c_void_p(R.ctypes.data) if R is not None else ctypes.c_void_p(0))
+    P._keep = (signs, R)     # keep the arrays alive with the struct
     return P
 
 

@@ -125,6 +125,18 @@ def scores_queries(device="cuda", batch: int | None = None, q_heads: int | None 
     return torch.randn((B, H, TILE), generator=g, device=device).to(torch.bfloat16)
 
 
+def haar_rotations(n: int, seed: int = 88):
+    """[n][128][128] fp32 numpy: n independent Haar-uniform orthogonal
+    matrices (QR of a Gaussian matrix with the signs of R's diagonal moved
+    into Q), drawn on the CPU so that every device gets the same values."""
+    import numpy as np
+    g = _gen(seed, "cpu")
+    a = torch.randn((n, TILE, TILE), generator=g, dtype=torch.float64)
+    q, r = torch.linalg.qr(a)
+    q = q * torch.sign(torch.diagonal(r, dim1=-2, dim2=-1)).unsqueeze(-2)
+    return np.ascontiguousarray(q.to(torch.float32).numpy())
+
+
 def activations(batch: int, cols: int, seed: int = 77, device="cuda") -> torch.Tensor:
     """x [batch, cols] bf16, N(0, 1): the activations multiplied by a weight matrix."""
     g = _gen(seed, device)
