@@ -92,7 +92,15 @@ enum { HQ_OUT_BF16 = 0, HQ_OUT_F32 = 1 };
  *                      and the encoder blocks take their groups from the
  *                      workspace's ticket counter (one atomic per block)
  *                      rather than from their launch index; the output is
- *                      the same. */
+ *                      the same.
+ *   d_rot              NULL, or device [n_segments][128][128] fp32 row-major
+ *                      per-layer dense rotations R (Method 3-4: a full
+ *                      Haar-uniform QJL matrix instead of the +-1 diagonal):
+ *                      tile t of segment s is coded as RHT(R_s x), each
+ *                      (R x)_i one fused multiply-add chain over j = 0..127
+ *                      from +0, and decoded with R_s^T applied after the
+ *                      inverse transform (chain over i).  16-byte aligned;
+ *                      tiles_per_segment must then be a multiple of 32. */
 typedef struct hq_params {
   int32_t lattice;
   int32_t rice_k;
@@ -104,6 +112,7 @@ typedef struct hq_params {
   int64_t tiles_per_segment;
   uint32_t lookback_spins;
   uint32_t flags;
+  const float *d_rot;
 } hq_params;
 
 #define HQ_FLAG_WORKSPACE_READY 1u

@@ -26,21 +26,23 @@ class Case:
     """One codec configuration with its inputs on both sides."""
 
     def __init__(self, x_bits: np.ndarray, lattice: int, k: int, alpha: float, dither: int,
-                 seed: int, masks: np.ndarray, tps: int, tile_base: int = 0):
+                 seed: int, masks: np.ndarray, tps: int, tile_base: int = 0, rot=None):
         self.x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1, 128)
         self.n = self.x_bits.shape[0]
         self.lattice, self.k, self.alpha, self.dither, self.seed = lattice, k, alpha, dither, seed
         self.masks = np.ascontiguousarray(masks, dtype=np.uint32).reshape(-1, 4)
         self.tps, self.tile_base = tps, tile_base
+        self.rot = None if rot is None else np.ascontiguousarray(rot, dtype=np.float32)
 
     def oracle_params(self, O):
         return O.make_params(self.lattice, self.k, self.alpha, self.dither, self.seed, self.masks,
-                             self.tps, self.tile_base)
+                             self.tps, self.tile_base, rot=self.rot)
 
     def gpu_params(self, hq, **kw):
         signs = torch.from_numpy(self.masks.view(np.int32).copy()).cuda()
+        rot = None if self.rot is None else torch.from_numpy(self.rot.copy()).cuda()
         return hq.make_params(self.lattice, self.k, self.alpha, self.dither, self.seed, signs,
-                              self.tps, self.tile_base, **kw)
+                              self.tps, self.tile_base, rot=rot, **kw)
 
 
 def gpu_encode(hq, p, x: torch.Tensor, n: int, cap=None):

@@ -54,8 +54,9 @@ def test_host_entry_points(hqlib, oracle):
 
 def test_params_layout(hqlib):
     import ctypes
-    # the ctypes mirror must match the C struct: 4+4+4+4+8+8+8+8+4+4 = 56 bytes
-    assert ctypes.sizeof(hqlib.hq_params) == 56
+    # the ctypes mirror must match the C struct: 4+4+4+4+8+8+8+8+4+4+8 = 64 bytes
+    assert ctypes.sizeof(hqlib.hq_params) == 64
+    assert hqlib.hq_params.d_rot.offset == 56
     assert hqlib.hq_params.d_signs.offset == 32
 
 

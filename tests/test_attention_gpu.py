@@ -42,8 +42,8 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 class Side:
     """One compressed stream (K or V), written and decoded by the oracle."""
 
-    def __init__(self, oracle, hq, x_bits, lattice, k, alpha, seed, mask, tps):
-        self.P = oracle.make_params(lattice, k, alpha, 1, seed, mask, tps)
+    def __init__(self, oracle, hq, x_bits, lattice, k, alpha, seed, mask, tps, rot=None):
+        self.P = oracle.make_params(lattice, k, alpha, 1, seed, mask, tps, rot=rot)
         enc = oracle.encode(self.P, x_bits)
         assert enc["status"] == 0
         self.words = int(enc["total_words"])
@@ -52,7 +52,8 @@ class Side:
         self.stream = torch.from_numpy(s.copy()).cuda()
         self.offsets = torch.from_numpy(np.ascontiguousarray(enc["offsets"]).view(np.int64).copy()).cuda()
         signs = torch.from_numpy(np.ascontiguousarray(mask, dtype=np.uint32).view(np.int32).copy()).cuda()
-        self.p = hq.make_params(lattice, k, alpha, 1, seed, signs, tps)
+        self.rot = None if rot is None else torch.from_numpy(np.ascontiguousarray(rot)).cuda()
+        self.p = hq.make_params(lattice, k, alpha, 1, seed, signs, tps, rot=self.rot)
 
 
 def _masks(oracle, layer_seed):
@@ -75,7 +76,7 @@ def _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, probs=True):
     return out.cpu().numpy(), (pr.cpu().numpy() if probs else None), int(st.item())
 
 
-def _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs):
+def _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs, rot=False):
     ref, P = A.attention(Ks.hat, Vs.hat, q_bits, n_kv, T, B, Hq, scale)
     G = Hq // n_kv
     V = np.abs(Vs.hat.astype(np.float64)).reshape(n_kv, T, 128)
@@ -84,17 +85,21 @@ def _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs):
     qn = np.linalg.norm(A.bf16_bits_to_f64(q_bits), axis=-1)                      # [B, Hq]
     kmax = np.linalg.norm(Ks.hat.astype(np.float64).reshape(n_kv, T, 128), axis=-1).max(-1)
     zeta = scale * qn * np.repeat(kmax, G)[None, :]                                # [B, Hq]
-    tol = (1.7e-5 * zeta + 3.6e-5)[:, :, None]
+    # a dense rotation adds one more 128-term chain on each side: R_K q doubles
+    # the score term, and R_V^T on the output row adds 128 u |out row|
+    tol = ((3.4e-5 if rot else 1.7e-5) * zeta + 3.6e-5)[:, :, None]
+    if rot:
+        tol = tol + 128 * 2.0 ** -24 * np.linalg.norm(ref, axis=-1, keepdims=True) / (size + 1e-30)
     err = np.abs(out - ref) / (size + 1e-30)
     worst = np.unravel_index(np.argmax(err / tol), err.shape)
     assert np.all(err <= tol), (err[worst], zeta[worst[:2]], tol[worst[0], worst[1], 0])
     if probs is not None:
-        tolp = (1.7e-5 * zeta + 1e-6)[:, :, None]
+        tolp = ((3.4e-5 if rot else 1.7e-5) * zeta + 1e-6)[:, :, None]
         assert np.all(np.abs(probs - P) <= tolp * P + 1e-38)
     return (err / tol).max()
 
 
-def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8):
+def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8, rot=False):
     from weights_hq_encode_gb300 import inputs as I
     C = I.SCORES
     cal = calibration()
@@ -105,10 +110,12 @@ def _workload(oracle, hq, n_kv, T, B, Hq, lat_k=8, lat_v=8):
     kb = _bits(I.scores_keys("cpu", tokens=T)[:n_kv])
     vb = _bits(I.scores_values("cpu", tokens=T)[:n_kv])
     n = n_kv * T
+    Rk = I.haar_rotations(1, seed=31) if rot else None
+    Rv = I.haar_rotations(1, seed=32) if rot else None
     Ks = Side(oracle, hq, kb, lat_k, ck["k"], ck["alpha"], C["dither_seeds"][0],
-              _masks(oracle, C["layer_sign_seed"]), n)
+              _masks(oracle, C["layer_sign_seed"]), n, rot=Rk)
     Vs = Side(oracle, hq, vb, lat_v, cv["k"], cv["alpha"], C["dither_seeds"][1],
-              _masks(oracle, C["layer_sign_seed"] + 1), n)
+              _masks(oracle, C["layer_sign_seed"] + 1), n, rot=Rv)
     q_bits = _bits(I.scores_queries("cpu", batch=B, q_heads=Hq)).reshape(B, Hq, 128)
     return Ks, Vs, q_bits
 
@@ -129,6 +136,17 @@ def test_attention_against_oracle(hq, oracle, n_kv, T, B, Hq, lat_k, lat_v):
     _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, out, probs)
     out2, _, st2 = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, scale, probs=False)
     assert st2 == 0 and np.array_equal(out, out2)             # deterministic
+
+
+@pytest.mark.parametrize("n_kv,T,B,Hq", [(2, 96, 3, 6), (1, 320, 2, 4)])
+def test_attention_with_dense_rotation(hq, oracle, n_kv, T, B, Hq):
+    """K and V coded with per-layer Haar (QJL) rotations: the queries are
+    rotated by R_K and the output rows by R_V^T."""
+    from oracle import attention as A
+    Ks, Vs, q_bits = _workload(oracle, hq, n_kv, T, B, Hq, rot=True)
+    out, probs, st = _run(hq, Ks, Vs, n_kv, T, q_bits, B, Hq, 128 ** -0.5)
+    assert st == 0
+    _check(A, Ks, Vs, n_kv, T, q_bits, B, Hq, 128 ** -0.5, out, probs, rot=True)
 
 
 def test_attention_full_size(hq, oracle):

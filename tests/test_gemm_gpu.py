@@ -32,11 +32,11 @@ def _bits(t: torch.Tensor) -> np.ndarray:
     return t.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def _weights(oracle, hq, wb, rows, cols, lattice, k, alpha, dither, seed):
+def _weights(oracle, hq, wb, rows, cols, lattice, k, alpha, dither, seed, rot=None):
     from weights_hq_encode_gb300 import inputs as I
     mask = oracle.make_signs(I.WEIGHTS8B["sign_seed"], 0).reshape(1, 4)
     n = rows * cols // 128
-    P = oracle.make_params(lattice, k, alpha, dither, seed, mask, 1 << 40)
+    P = oracle.make_params(lattice, k, alpha, dither, seed, mask, 1 << 40, rot=rot)
     enc = oracle.encode(P, wb.reshape(-1, 128))
     assert enc["status"] == 0
     words = int(enc["total_words"])
@@ -44,8 +44,9 @@ def _weights(oracle, hq, wb, rows, cols, lattice, k, alpha, dither, seed):
     stream = torch.from_numpy(np.ascontiguousarray(enc["stream"][:max(words, 1)]).view(np.int32).copy()).cuda()
     offsets = torch.from_numpy(np.ascontiguousarray(enc["offsets"]).view(np.int64).copy()).cuda()
     signs = torch.from_numpy(mask.astype(np.uint32).view(np.int32).copy()).cuda()
-    p = hq.make_params(lattice, k, alpha, dither, seed, signs, 1 << 40)
-    return p, stream, words, offsets, what, signs
+    rt = None if rot is None else torch.from_numpy(np.ascontiguousarray(rot)).cuda()
+    p = hq.make_params(lattice, k, alpha, dither, seed, signs, 1 << 40, rot=rt)
+    return p, stream, words, offsets, what, (signs, rt)
 
 
 def _run(hq, p, stream, words, offsets, rows, cols, xb):
@@ -59,13 +60,13 @@ def _run(hq, p, stream, words, offsets, rows, cols, xb):
     return y.cpu().numpy(), int(st.item())
 
 
-def _check(G, what, xb, rows, cols, y):
+def _check(G, what, xb, rows, cols, y, rot=False):
     ref = G.gemm(what, xb, rows, cols)
     tpr = cols // 128
     xn = np.linalg.norm(G.bf16_bits_to_f64(xb).reshape(-1, tpr, 128), axis=-1)        # [B, tpr]
     wn = np.linalg.norm(what.astype(np.float64).reshape(rows, tpr, 128), axis=-1)     # [rows, tpr]
     S = xn @ wn.T
-    tol = (142 + tpr / 32) * U * S
+    tol = (142 + (128 if rot else 0) + tpr / 32) * U * S   # R x_j: one more 128-term chain
     assert np.all(np.abs(y - ref) <= tol), np.max(np.abs(y - ref) / (tol + 1e-300))
 
 
@@ -92,6 +93,22 @@ def test_gemm_against_oracle(hq, oracle, index, rows, B, rate, lattice, dither):
     _check(G, what, xb, rows, cols, y)
     y2, _ = _run(hq, p, stream, words, offsets, rows, cols, xb)
     assert np.array_equal(y, y2)                                 # deterministic
+
+
+def test_gemm_with_dense_rotation(hq, oracle):
+    """Weights coded with a Haar (QJL) rotation: each activation tile is
+    rotated by R before the transform."""
+    from oracle import gemm as G
+    from weights_hq_encode_gb300 import inputs as I
+    rows, cols, B = 40, 4096, 3
+    c = calibration()["weights_8b"]["E8"]["4.0"][0]
+    wb = _bits(I.weight_matrix(0, "cpu", rows=rows))
+    p, stream, words, offsets, what, _s = _weights(oracle, hq, wb, rows, cols, 8, c["k"],
+                                                   c["alpha"], 0, 0, rot=I.haar_rotations(1, 7))
+    xb = _bits(I.activations(B, cols, device="cpu"))
+    y, st = _run(hq, p, stream, words, offsets, rows, cols, xb)
+    assert st == 0
+    _check(G, what, xb, rows, cols, y, rot=True)
 
 
 @pytest.mark.parametrize("index,B", [(0, 16), (2, 8)])

@@ -97,6 +97,37 @@ def test_small_cases_bit_exact(hq, oracle, lat, k, alpha, dither, n, nseg, base)
     _check_case(hq, oracle, Case(x, lat, k, alpha, dither, 4242 + n, masks, tps, base))
 
 
+@pytest.mark.parametrize("lat,k,alpha,dither,n,nseg", [
+    (8, 2, 1.7, 1, 160, 2),        # Haar rotation per segment (32-tile aligned segments)
+    (8, 0, 0.6, 1, 70, 1),
+    (4, 1, 1.3, 0, 96, 3),
+    (2, 2, 2.0, 1, 64, 2),
+    (1, 3, 6.0, 1, 33, 1),
+])
+def test_dense_rotation_bit_exact(hq, oracle, lat, k, alpha, dither, n, nseg):
+    """The per-layer Haar (QJL) rotation: codes, streams and decodes equal the
+    oracle's fixed-order fp32 chains bit for bit."""
+    from weights_hq_encode_gb300 import inputs as I
+    rng = np.random.default_rng(2000 + n + k)
+    x = _rand_bits(rng, n)
+    masks = np.stack([oracle.make_signs(78, s) for s in range(nseg)])
+    tps = 32 * max(1, -(-n // (32 * nseg)))
+    rot = I.haar_rotations(nseg, seed=500 + n)
+    _check_case(hq, oracle, Case(x, lat, k, alpha, dither, 77 + n, masks, tps, 0, rot=rot))
+
+
+def test_dense_rotation_needs_aligned_segments(hq, oracle):
+    from weights_hq_encode_gb300 import inputs as I
+    x = torch.zeros((40, 128), dtype=torch.int16, device="cuda")
+    c = Case(np.zeros((40, 128), np.uint16), 8, 2, 1.0, 1, 1, oracle.make_signs(1, 0), 20,
+             rot=I.haar_rotations(2))
+    p = c.gpu_params(hq)
+    offsets = torch.zeros(hq.hq_num_groups(40) + 1, dtype=torch.int64, device="cuda")
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(40), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hq.hq_encode(p, x, 40, None, 0, offsets, ws, st) == hq.HQ_ERR_INVALID
+
+
 def test_tiny_kv_config(hq, oracle):
     from weights_hq_encode_gb300 import inputs as I
     cal = calibration()["tiny_kv"]["E8"]["3.0"]

@@ -29,8 +29,13 @@ int rbits_of(int lattice, int k) {
   return per8 * 16;
 }
 
+bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
 bool params_ok(const hq_params *p) {
   if (!p || !lattice_ok(p->lattice)) return false;
+  if (p->d_rot && (!aligned(p->d_rot, 16) || p->tiles_per_segment <= 0 ||
+                   p->tiles_per_segment % HQ_GROUP_TILES != 0))
+    return false;
   if (p->rice_k < 0 || p->rice_k > 15) return false;
   if (!(p->alpha > 0.0f) || !std::isfinite(p->alpha)) return false;
   if (p->dither != 0 && p->dither != 1) return false;
@@ -38,7 +43,6 @@ bool params_ok(const hq_params *p) {
   return true;
 }
 
-bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // Scales of the orthonormal RHT in lattice units, formed in double and
 // rounded once (alpha / sqrt(128) forward, 1 / (alpha sqrt(128)) back).
@@ -81,6 +85,7 @@ DecodeArgs make_decode_args(const hq_params *p, const uint32_t *stream, uint64_t
   a.rice_k = p->rice_k;
   a.rbits = rbits_of(p->lattice, p->rice_k);
   a.dither = p->dither;
+  a.rot = p->d_rot;
   return a;
 }
 
@@ -139,6 +144,7 @@ int encode_impl(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32
   a.dither = p->dither;
   a.spins = p->lookback_spins ? p->lookback_spins : kDefaultSpins;
   a.payload_bits = d_bits;
+  a.rot = p->d_rot;
   a.use_ticket = (p->flags & HQ_FLAG_WORKSPACE_READY) ? 1 : 0;
   if (!(p->flags & HQ_FLAG_WORKSPACE_READY)) {
     if (cudaMemsetAsync(d_ws, 0, hq_encode_workspace_bytes(n_tiles), st) != cudaSuccess)

@@ -308,8 +308,9 @@ decode_kernel(DecodeArgs a) {
   if (!ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
   // the transform runs on every lane of the block (shuffles need full warps)
   fwht128_x8(e, r);
-  if (t >= a.n_tiles) return;
-  if (ok) {
+  const bool tvalid = t < a.n_tiles;
+  if (a.rot == nullptr && !tvalid) return;
+  if (ok && tvalid) {
     // x = D fl(z s_dec) = fl(z (D s_dec)): the sign commutes with rounding
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
 #pragma unroll
@@ -327,6 +328,33 @@ decode_kernel(DecodeArgs a) {
       for (int i = 0; i < 16; ++i)
         e[i] = __fmul_rn(e[i], __uint_as_float(__float_as_uint(a.s_dec) ^ (((mw >> i) & 1u) << 31)));
     }
+  }
+  if (a.rot != nullptr) {                        // uniform: x_hat = R^T y, chains over i
+    extern __shared__ __align__(16) float s_dyn[];
+    float *s_y = s_dyn;                          // [32][128]
+    float *s_r = s_dyn + kGroupTiles * kTile;    // [128][128] R of the group's segment
+    float4 *dy = reinterpret_cast<float4 *>(s_y + tl * kTile + 16 * r);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dy[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    const float4 *R4 = reinterpret_cast<const float4 *>(a.rot + seg0 * (int64_t)(kTile * kTile));
+    for (int idx = tid; idx < kTile * kTile / 4; idx += kDecThreads)
+      reinterpret_cast<float4 *>(s_r)[idx] = __ldg(R4 + idx);
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) e[c] = 0.0f;
+    for (int i = 0; i < kTile; ++i) {
+      const float yi = s_y[tl * kTile + i];
+      const float4 *rr = reinterpret_cast<const float4 *>(s_r + i * kTile + 16 * r);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 q = rr[c];
+        e[4 * c] = __fmaf_rn(q.x, yi, e[4 * c]);
+        e[4 * c + 1] = __fmaf_rn(q.y, yi, e[4 * c + 1]);
+        e[4 * c + 2] = __fmaf_rn(q.z, yi, e[4 * c + 2]);
+        e[4 * c + 3] = __fmaf_rn(q.w, yi, e[4 * c + 3]);
+      }
+    }
+    if (!tvalid) return;
   }
   if (a.out_kind == HQ_OUT_F32) {
     float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + t * kTile + 16 * r);
@@ -356,10 +384,11 @@ __global__ void rotate_queries_kernel(QkArgs a) {
   float x[128];
   const uint16_t *q = a.q + (int64_t)row * kTile;
 #pragma unroll
-  for (int i = 0; i < 128; ++i) {
-    const float f = __uint_as_float((uint32_t)q[i] << 16);
-    x[i] = ((mask[i >> 5] >> (i & 31)) & 1u) ? -f : f;
-  }
+  for (int i = 0; i < 128; ++i) x[i] = __uint_as_float((uint32_t)q[i] << 16);
+  if (a.dec.rot != nullptr) rotate128(a.dec.rot + seg * (int64_t)(kTile * kTile), x);
+#pragma unroll
+  for (int i = 0; i < 128; ++i)
+    if ((mask[i >> 5] >> (i & 31)) & 1u) x[i] = -x[i];
   fwht128(x);
 #pragma unroll
   for (int i = 0; i < 128; ++i) a.qrot[(int64_t)row * kTile + i] = __fmul_rn(x[i], a.dec.s_dec);
@@ -602,7 +631,19 @@ __global__ void __launch_bounds__(kTile) pv_finish_kernel(AttnArgs a) {
   const int64_t seg = div_by((int64_t)h * a.qk.n_tokens, a.v.tiles_per_segment, a.v.seg_shift);
   const uint32_t mw = __ldg(a.v.signs + 4 * seg + (d >> 5));
   const float y = __fmul_rn(x[d], a.v.s_dec);
-  a.out[(int64_t)row * kTile + d] = ((mw >> (d & 31)) & 1u) ? -y : y;
+  const float yd = ((mw >> (d & 31)) & 1u) ? -y : y;
+  if (a.v.rot == nullptr) {
+    a.out[(int64_t)row * kTile + d] = yd;
+    return;
+  }
+  // dense rotation of the values: out = R^T y, one chain over i per output
+  const float *R = a.v.rot + seg * (int64_t)(kTile * kTile);
+  __syncthreads();
+  x[d] = yd;
+  __syncthreads();
+  float acc = 0.0f;
+  for (int i = 0; i < kTile; ++i) acc = __fmaf_rn(__ldg(R + i * kTile + d), x[i], acc);
+  a.out[(int64_t)row * kTile + d] = acc;
 }
 
 // ---------------------------------------------------------------- weights
@@ -615,10 +656,11 @@ __global__ void rotate_x_kernel(GemmArgs a) {
   float x[128];
   const uint16_t *src = a.x + i * kTile;
 #pragma unroll
-  for (int k = 0; k < 128; ++k) {
-    const float f = __uint_as_float((uint32_t)src[k] << 16);
-    x[k] = ((mask[k >> 5] >> (k & 31)) & 1u) ? -f : f;
-  }
+  for (int k = 0; k < 128; ++k) x[k] = __uint_as_float((uint32_t)src[k] << 16);
+  if (a.dec.rot != nullptr) rotate128(a.dec.rot, x);      // the matrix is one segment
+#pragma unroll
+  for (int k = 0; k < 128; ++k)
+    if ((mask[k >> 5] >> (k & 31)) & 1u) x[k] = -x[k];
   fwht128(x);
 #pragma unroll
   for (int k = 0; k < 128; ++k) a.xrot[i * kTile + k] = __fmul_rn(x[k], a.dec.s_dec);
@@ -690,20 +732,30 @@ __global__ void gemm_reduce_kernel(GemmArgs a) {
   if (lane == 0) a.y[b * a.rows + o] = s;
 }
 
+constexpr size_t kDecRotSmemBytes = (size_t)(kGroupTiles * kTile + kTile * kTile) * 4;
+
+template <int LAT, int K>
+static void launch_dec_one(const DecodeArgs &a, cudaStream_t st) {
+  const size_t dyn = a.rot != nullptr ? kDecRotSmemBytes : 0;
+  if (dyn)
+    cudaFuncSetAttribute(decode_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)dyn);
+  decode_kernel<LAT, K><<<dim3((unsigned)a.n_groups), dim3(kDecThreads), dyn, st>>>(a);
+}
+
 template <int LAT>
 static void launch_dec_lat(const DecodeArgs &a, cudaStream_t st) {
-  dim3 grid((unsigned)a.n_groups), block(kDecThreads);
   switch (a.rice_k) {
-    case 0: decode_kernel<LAT, 0><<<grid, block, 0, st>>>(a); break;
-    case 1: decode_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
-    case 2: decode_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
-    case 3: decode_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
-    case 4: decode_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
-    case 5: decode_kernel<LAT, 5><<<grid, block, 0, st>>>(a); break;
-    case 6: decode_kernel<LAT, 6><<<grid, block, 0, st>>>(a); break;
-    case 7: decode_kernel<LAT, 7><<<grid, block, 0, st>>>(a); break;
-    case 8: decode_kernel<LAT, 8><<<grid, block, 0, st>>>(a); break;
-    default: decode_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+    case 0: launch_dec_one<LAT, 0>(a, st); break;
+    case 1: launch_dec_one<LAT, 1>(a, st); break;
+    case 2: launch_dec_one<LAT, 2>(a, st); break;
+    case 3: launch_dec_one<LAT, 3>(a, st); break;
+    case 4: launch_dec_one<LAT, 4>(a, st); break;
+    case 5: launch_dec_one<LAT, 5>(a, st); break;
+    case 6: launch_dec_one<LAT, 6>(a, st); break;
+    case 7: launch_dec_one<LAT, 7>(a, st); break;
+    case 8: launch_dec_one<LAT, 8>(a, st); break;
+    default: launch_dec_one<LAT, -1>(a, st); break;
   }
 }
 

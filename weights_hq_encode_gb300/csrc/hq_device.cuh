@@ -73,6 +73,28 @@ __device__ __forceinline__ void fwht128(float x[128]) {
   }
 }
 
+// x <- R x for one 128-vector held by one thread (R row-major, global): one
+// fused multiply-add chain over j = 0..127 per output, from +0.
+__device__ __forceinline__ void rotate128(const float *R, float x[128]) {
+  float z[128];
+#pragma unroll 1
+  for (int i = 0; i < 128; ++i) {
+    float acc = 0.0f;
+    const float4 *row = reinterpret_cast<const float4 *>(R + i * 128);
+#pragma unroll
+    for (int j4 = 0; j4 < 32; ++j4) {
+      const float4 q = __ldg(row + j4);
+      acc = __fmaf_rn(q.x, x[4 * j4], acc);
+      acc = __fmaf_rn(q.y, x[4 * j4 + 1], acc);
+      acc = __fmaf_rn(q.z, x[4 * j4 + 2], acc);
+      acc = __fmaf_rn(q.w, x[4 * j4 + 3], acc);
+    }
+    z[i] = acc;
+  }
+#pragma unroll
+  for (int i = 0; i < 128; ++i) x[i] = z[i];
+}
+
 // The same transform with a tile spread over 8 consecutive lanes, lane r of
 // the tile holding coordinates 16r .. 16r+15: stages h = 1, 2, 4, 8 stay in
 // registers, stages 16, 32, 64 pair lane r with lane r ^ 1, r ^ 2, r ^ 4.

@@ -23,6 +23,10 @@ namespace hq {
 constexpr int kEncThreads = 256;                 // one group of 32 tiles
 constexpr int kStageWords = 4096;                // 16 KiB of output per window
 constexpr int kKmaxTemplated = 8;                // Rice k specialised at compile time
+// Dense rotation (optional): the group's tiles as fp32 [32][128] and the
+// segment's R transposed, rows padded to 132 floats.
+constexpr int kRotTStride = kTile + 4;
+constexpr size_t kEncRotSmemBytes = (size_t)(kGroupTiles * kTile + kTile * kRotTStride) * 4;
 
 constexpr uint64_t kFlagAgg = 1ull << 62;        // look-back state: [63:62] flag
 constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] words
@@ -267,9 +271,46 @@ encode_kernel(EncodeArgs a) {
   }
   __syncthreads();
 
-  // ---- sign mask, FWHT
+  // ---- optional dense rotation R x (before the sign mask)
   float x[16];
-  if (valid) {
+  if (a.rot != nullptr) {                        // uniform over the grid
+    extern __shared__ __align__(16) float s_dyn[];
+    float *s_x = s_dyn;                          // [32][128]
+    float *s_rt = s_dyn + kGroupTiles * kTile;   // [128][kRotTStride]: R transposed
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float4 *dx = reinterpret_cast<float4 *>(s_x + tl * kTile + 16 * r);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      dx[c] = make_float4(__uint_as_float(w[2 * c] << 16), __uint_as_float(w[2 * c] & 0xFFFF0000u),
+                          __uint_as_float(w[2 * c + 1] << 16),
+                          __uint_as_float(w[2 * c + 1] & 0xFFFF0000u));
+    const float *R = a.rot + seg0 * (int64_t)(kTile * kTile);   // the group is in one segment
+    for (int idx = tid; idx < kTile * kTile; idx += kEncThreads)
+      s_rt[(idx & (kTile - 1)) * kRotTStride + (idx >> 7)] = __ldg(R + idx);
+    __syncthreads();
+    float z[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) z[c] = 0.0f;
+    for (int j = 0; j < kTile; ++j) {            // (R x)_i: one FMA chain over j
+      const float xj = s_x[tl * kTile + j];
+      const float4 *rt = reinterpret_cast<const float4 *>(s_rt + j * kRotTStride + 16 * r);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 q = rt[c];
+        z[4 * c] = __fmaf_rn(q.x, xj, z[4 * c]);
+        z[4 * c + 1] = __fmaf_rn(q.y, xj, z[4 * c + 1]);
+        z[4 * c + 2] = __fmaf_rn(q.z, xj, z[4 * c + 2]);
+        z[4 * c + 3] = __fmaf_rn(q.w, xj, z[4 * c + 3]);
+      }
+    }
+    const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
+    const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {                // bf16-pair sign bits 15 / 31 -> fp32 bit 31
+      x[2 * q] = __uint_as_float(__float_as_uint(z[2 * q]) ^ (sw[q] << 16));
+      x[2 * q + 1] = __uint_as_float(__float_as_uint(z[2 * q + 1]) ^ (sw[q] & 0x80000000u));
+    }
+  } else if (valid) {
     uint32_t sw[8];
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
       const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
@@ -490,20 +531,28 @@ encode_kernel(EncodeArgs a) {
   }
 }
 
+template <int LAT, int K>
+static void launch_one(const EncodeArgs &a, cudaStream_t st) {
+  const size_t dyn = a.rot != nullptr ? kEncRotSmemBytes : 0;
+  if (dyn)
+    cudaFuncSetAttribute(encode_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)dyn);
+  encode_kernel<LAT, K><<<dim3((unsigned)a.n_blocks), dim3(kEncThreads), dyn, st>>>(a);
+}
+
 template <int LAT>
 static void launch_lat(const EncodeArgs &a, cudaStream_t st) {
-  dim3 grid((unsigned)a.n_blocks), block(kEncThreads);
   switch (a.rice_k) {
-    case 0: encode_kernel<LAT, 0><<<grid, block, 0, st>>>(a); break;
-    case 1: encode_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
-    case 2: encode_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
-    case 3: encode_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
-    case 4: encode_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
-    case 5: encode_kernel<LAT, 5><<<grid, block, 0, st>>>(a); break;
-    case 6: encode_kernel<LAT, 6><<<grid, block, 0, st>>>(a); break;
-    case 7: encode_kernel<LAT, 7><<<grid, block, 0, st>>>(a); break;
-    case 8: encode_kernel<LAT, 8><<<grid, block, 0, st>>>(a); break;
-    default: encode_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+    case 0: launch_one<LAT, 0>(a, st); break;
+    case 1: launch_one<LAT, 1>(a, st); break;
+    case 2: launch_one<LAT, 2>(a, st); break;
+    case 3: launch_one<LAT, 3>(a, st); break;
+    case 4: launch_one<LAT, 4>(a, st); break;
+    case 5: launch_one<LAT, 5>(a, st); break;
+    case 6: launch_one<LAT, 6>(a, st); break;
+    case 7: launch_one<LAT, 7>(a, st); break;
+    case 8: launch_one<LAT, 8>(a, st); break;
+    default: launch_one<LAT, -1>(a, st); break;
   }
 }
 

@@ -40,6 +40,7 @@ struct EncodeArgs {
   uint32_t spins;
   unsigned long long *payload_bits;   // non-null: add each group's Rice bits here
   int use_ticket;           // groups from the workspace's ticket counter, not blockIdx
+  const float *rot;         // nullptr, or [n_segments][128][128] row-major rotations
 };
 
 struct DecodeArgs {
@@ -61,6 +62,7 @@ struct DecodeArgs {
   int rice_k;
   int rbits;
   int dither;
+  const float *rot;         // nullptr, or [n_segments][128][128] row-major rotations
 };
 
 struct QkArgs {

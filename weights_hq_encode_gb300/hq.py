@@ -35,7 +35,8 @@ class hq_params(ctypes.Structure):
                 ("alpha", ctypes.c_float), ("dither", ctypes.c_int32),
                 ("dither_seed", ctypes.c_uint64), ("tile_base", ctypes.c_uint64),
                 ("d_signs", ctypes.c_void_p), ("tiles_per_segment", ctypes.c_int64),
-                ("lookback_spins", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+                ("lookback_spins", ctypes.c_uint32), ("flags", ctypes.c_uint32),
+                ("d_rot", ctypes.c_void_p)]
 
 
 class hq_calibration(ctypes.Structure):
@@ -118,14 +119,19 @@ def _check(rc: int, name: str):
 
 
 def make_params(lattice, rice_k, alpha, dither, dither_seed, signs: torch.Tensor,
-                tiles_per_segment, tile_base=0, lookback_spins=0, flags=0) -> hq_params:
-    """hq_params with d_signs pointing at a device uint32 tensor [n_segments, 4]."""
+                tiles_per_segment, tile_base=0, lookback_spins=0, flags=0,
+                rot: torch.Tensor | None = None) -> hq_params:
+    """hq_params with d_signs pointing at a device uint32 tensor [n_segments, 4]
+    and, optionally, d_rot at a device fp32 tensor [n_segments, 128, 128]."""
     if signs.dtype not in (torch.int32, torch.uint32) or not signs.is_cuda:
         raise TypeError("signs must be a CUDA int32/uint32 tensor [n_segments, 4]")
+    if rot is not None and (rot.dtype != torch.float32 or not rot.is_cuda or
+                            not rot.is_contiguous()):
+        raise TypeError("rot must be a contiguous CUDA fp32 tensor [n_segments, 128, 128]")
     p = hq_params(int(lattice), int(rice_k), float(alpha), int(dither), int(dither_seed),
                   int(tile_base), signs.data_ptr(), int(tiles_per_segment), int(lookback_spins),
-                  int(flags))
-    p._signs = signs      # keep the masks alive as long as the params
+                  int(flags), rot.data_ptr() if rot is not None else None)
+    p._signs, p._rot = signs, rot      # keep the arrays alive as long as the params
     return p
 
 
