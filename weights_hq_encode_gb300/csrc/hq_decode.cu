@@ -330,29 +330,48 @@ decode_kernel(DecodeArgs a) {
     }
   }
   if (a.rot != nullptr) {                        // uniform: x_hat = R^T y, chains over i
+    // [32 tiles x 128] x [128 x 128] in shared memory: y transposed [128][36]
+    // (later reused for the result [32][132]) and R row-major [128][132]
+    constexpr int kYS = kGroupTiles + 4, kRS = kTile + 4;
     extern __shared__ __align__(16) float s_dyn[];
-    float *s_y = s_dyn;                          // [32][128]
-    float *s_r = s_dyn + kGroupTiles * kTile;    // [128][128] R of the group's segment
-    float4 *dy = reinterpret_cast<float4 *>(s_y + tl * kTile + 16 * r);
+    float *s_yt = s_dyn;
+    float *s_r = s_dyn + kTile * kYS;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) dy[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    for (int c = 0; c < 16; ++c) s_yt[(16 * r + c) * kYS + tl] = e[c];
     const float4 *R4 = reinterpret_cast<const float4 *>(a.rot + seg0 * (int64_t)(kTile * kTile));
     for (int idx = tid; idx < kTile * kTile / 4; idx += kDecThreads)
-      reinterpret_cast<float4 *>(s_r)[idx] = __ldg(R4 + idx);
+      *reinterpret_cast<float4 *>(s_r + (idx >> 5) * kRS + 4 * (idx & 31)) = __ldg(R4 + idx);
+    __syncthreads();
+    const int tb = tid >> 5, ob = tid & 31;     // tiles 4tb.., outputs 4ob..
+    float acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < kTile; ++i) {
+      const float4 yv = *reinterpret_cast<const float4 *>(s_yt + i * kYS + 4 * tb);
+      const float4 rv = *reinterpret_cast<const float4 *>(s_r + i * kRS + 4 * ob);
+      const float ys[4] = {yv.x, yv.y, yv.z, yv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rs[c], ys[u], acc[u][c]);
+    }
+    __syncthreads();
+    float *s_o = s_dyn;                          // [32][132]
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<float4 *>(s_o + (4 * tb + u) * kRS + 4 * ob) =
+          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
     __syncthreads();
 #pragma unroll
-    for (int c = 0; c < 16; ++c) e[c] = 0.0f;
-    for (int i = 0; i < kTile; ++i) {
-      const float yi = s_y[tl * kTile + i];
-      const float4 *rr = reinterpret_cast<const float4 *>(s_r + i * kTile + 16 * r);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 q = rr[c];
-        e[4 * c] = __fmaf_rn(q.x, yi, e[4 * c]);
-        e[4 * c + 1] = __fmaf_rn(q.y, yi, e[4 * c + 1]);
-        e[4 * c + 2] = __fmaf_rn(q.z, yi, e[4 * c + 2]);
-        e[4 * c + 3] = __fmaf_rn(q.w, yi, e[4 * c + 3]);
-      }
+    for (int c = 0; c < 4; ++c) {
+      const float4 q = *reinterpret_cast<const float4 *>(s_o + tl * kRS + 16 * r + 4 * c);
+      e[4 * c] = q.x;
+      e[4 * c + 1] = q.y;
+      e[4 * c + 2] = q.z;
+      e[4 * c + 3] = q.w;
     }
     if (!tvalid) return;
   }
@@ -732,7 +751,7 @@ __global__ void gemm_reduce_kernel(GemmArgs a) {
   if (lane == 0) a.y[b * a.rows + o] = s;
 }
 
-constexpr size_t kDecRotSmemBytes = (size_t)(kGroupTiles * kTile + kTile * kTile) * 4;
+constexpr size_t kDecRotSmemBytes = (size_t)(kTile * (kGroupTiles + 4) + kTile * (kTile + 4)) * 4;
 
 template <int LAT, int K>
 static void launch_dec_one(const DecodeArgs &a, cudaStream_t st) {

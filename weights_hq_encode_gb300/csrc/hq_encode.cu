@@ -23,10 +23,14 @@ namespace hq {
 constexpr int kEncThreads = 256;                 // one group of 32 tiles
 constexpr int kStageWords = 4096;                // 16 KiB of output per window
 constexpr int kKmaxTemplated = 8;                // Rice k specialised at compile time
-// Dense rotation (optional): the group's tiles as fp32 [32][128] and the
-// segment's R transposed, rows padded to 132 floats.
-constexpr int kRotTStride = kTile + 4;
-constexpr size_t kEncRotSmemBytes = (size_t)(kGroupTiles * kTile + kTile * kRotTStride) * 4;
+// Dense rotation (optional), as a [32 tiles x 128] x [128 x 128] product in
+// shared memory: the tiles transposed [128][36] (later reused for the result
+// [32][132]) and the segment's R transposed [128][132].
+constexpr int kRotXStride = kGroupTiles + 4;
+constexpr int kRotStride = kTile + 4;
+constexpr int kRotXFloats = kTile * kRotXStride;                    // >= 32 * kRotStride
+constexpr size_t kEncRotSmemBytes = (size_t)(kRotXFloats + kTile * kRotStride) * 4;
+static_assert(kRotXFloats >= kGroupTiles * kRotStride, "result fits the tile area");
 
 constexpr uint64_t kFlagAgg = 1ull << 62;        // look-back state: [63:62] flag
 constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] words
@@ -275,33 +279,50 @@ encode_kernel(EncodeArgs a) {
   float x[16];
   if (a.rot != nullptr) {                        // uniform over the grid
     extern __shared__ __align__(16) float s_dyn[];
-    float *s_x = s_dyn;                          // [32][128]
-    float *s_rt = s_dyn + kGroupTiles * kTile;   // [128][kRotTStride]: R transposed
+    float *s_xt = s_dyn;                         // [128][36]: coordinate j of tile t at [j][t]
+    float *s_rt = s_dyn + kRotXFloats;           // [128][132]: R[i][j] at [j][i]
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float4 *dx = reinterpret_cast<float4 *>(s_x + tl * kTile + 16 * r);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      dx[c] = make_float4(__uint_as_float(w[2 * c] << 16), __uint_as_float(w[2 * c] & 0xFFFF0000u),
-                          __uint_as_float(w[2 * c + 1] << 16),
-                          __uint_as_float(w[2 * c + 1] & 0xFFFF0000u));
+    for (int q = 0; q < 8; ++q) {
+      s_xt[(16 * r + 2 * q) * kRotXStride + tl] = __uint_as_float(w[q] << 16);
+      s_xt[(16 * r + 2 * q + 1) * kRotXStride + tl] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
     const float *R = a.rot + seg0 * (int64_t)(kTile * kTile);   // the group is in one segment
     for (int idx = tid; idx < kTile * kTile; idx += kEncThreads)
-      s_rt[(idx & (kTile - 1)) * kRotTStride + (idx >> 7)] = __ldg(R + idx);
+      s_rt[(idx & (kTile - 1)) * kRotStride + (idx >> 7)] = __ldg(R + idx);
+    __syncthreads();
+    // thread (tb, ob): tiles 4tb..4tb+3 x outputs 4ob..4ob+3, one chain over j each
+    const int tb = tid >> 5, ob = tid & 31;
+    float acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < kTile; ++j) {
+      const float4 xv = *reinterpret_cast<const float4 *>(s_xt + j * kRotXStride + 4 * tb);
+      const float4 rv = *reinterpret_cast<const float4 *>(s_rt + j * kRotStride + 4 * ob);
+      const float xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rs[c], xs[u], acc[u][c]);
+    }
+    __syncthreads();                             // the tile area becomes the result area
+    float *s_z = s_dyn;                          // [32][132]
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<float4 *>(s_z + (4 * tb + u) * kRotStride + 4 * ob) =
+          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
     __syncthreads();
     float z[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) z[c] = 0.0f;
-    for (int j = 0; j < kTile; ++j) {            // (R x)_i: one FMA chain over j
-      const float xj = s_x[tl * kTile + j];
-      const float4 *rt = reinterpret_cast<const float4 *>(s_rt + j * kRotTStride + 16 * r);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 q = rt[c];
-        z[4 * c] = __fmaf_rn(q.x, xj, z[4 * c]);
-        z[4 * c + 1] = __fmaf_rn(q.y, xj, z[4 * c + 1]);
-        z[4 * c + 2] = __fmaf_rn(q.z, xj, z[4 * c + 2]);
-        z[4 * c + 3] = __fmaf_rn(q.w, xj, z[4 * c + 3]);
-      }
+    for (int c = 0; c < 4; ++c) {
+      const float4 q = *reinterpret_cast<const float4 *>(s_z + tl * kRotStride + 16 * r + 4 * c);
+      z[4 * c] = q.x;
+      z[4 * c + 1] = q.y;
+      z[4 * c + 2] = q.z;
+      z[4 * c + 3] = q.w;
     }
     const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
     const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
