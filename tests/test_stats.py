@@ -101,3 +101,25 @@ def test_calibrated_rates_recorded_within_tolerance():
             for rate, c in rates.items():
                 for entry in (c if isinstance(c, list) else [c]):
                     assert abs(entry["bps"] - float(rate)) <= 0.002 + 1e-9, (name, lname, rate)
+
+
+def test_compression_at_3_bps_matches_the_stated_context(oracle):
+    """HyperQuant summary, Experimental results (KV cache): about 81% less memory at
+    3 bps than bf16 (1 - 3/16 = 81.25%).  The whole stream (payload, group padding and
+    the 64-bit group index) of fresh KV tokens at the frozen 3-bps setting
+    lands within half a point of it."""
+    from weights_hq_encode_gb300 import inputs as I
+    C = I.KV8B
+    c = calibration()["kv_cache_8b"]["E8"]["3.0"]
+    xs, ms = [], []
+    for layer in range(0, C["layers"], 4):
+        for kv in (0, 1):
+            x = I.kv_slab(I.slab_seed(C["data_seed"], layer, kv), C["kv_heads"], 384, "cpu")
+            xs.append(I.bf16_bits(x[:, 256:]).reshape(-1, 128))
+            ms.append(oracle.make_signs(C["sign_seed"], 0) ^ oracle.make_signs(C["layer_sign_seed"], layer))
+    x = np.concatenate(xs)
+    P = oracle.make_params(8, c["k"], c["alpha"], 1, C["dither_seed"], np.stack(ms), xs[0].shape[0])
+    enc = oracle.encode(P, x)
+    total_bits = enc["total_words"] * 32 + 64 * (oracle.n_groups(x.shape[0]) + 1)
+    compression = 1 - total_bits / (x.size * 16)
+    assert abs(compression - 0.8125) < 0.005, compression
