@@ -181,6 +181,28 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_kernel(AttnArgs a) {
 // group outside head h (a group that straddles two heads) get p = 0.
 constexpr int kPvEStride = kTile + 4;
 constexpr int kPvPStride = kPvRows + 4;
+
+// This thread's 8 probabilities of group g (element i = tid + 256 k of the
+// group's 64 rows x 32 tokens, row-major): consecutive threads read
+// consecutive tokens of one row; tokens outside head h or rows past the end
+// read as 0.
+__device__ __forceinline__ void pv_load_p(const AttnArgs &a, int64_t g, int h, int row0, int G,
+                                          int rows, int64_t tile_lo, int64_t tile_hi,
+                                          float p[8]) {
+  const int64_t T = a.qk.n_tokens;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = threadIdx.x + k * kDecThreads;
+    const int rr = i >> 5, j = i & 31;
+    const int64_t tile = g * kGroupTiles + j;
+    const int row = row0 + rr;
+    p[k] = 0.0f;
+    if (tile >= tile_lo && tile < tile_hi && row < rows) {
+      const int b = row / G, gq = row - b * G;
+      p[k] = a.qk.scores[((int64_t)b * a.qk.Hq + (int64_t)h * G + gq) * T + (tile - tile_lo)];
+    }
+  }
+}
 template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
@@ -201,6 +223,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  // the probabilities of a group are loaded one group ahead, so that their
+  // latency hides behind the decoding and the contraction of the current one
+  float pn[8];
+  if (gb < ge) pv_load_p(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
   for (int64_t g = gb; g < ge; ++g) {            // block-uniform bounds
     float e[16];
     const bool ok = decode_lane<LAT, K>(a.v, g, e, s_start, s_warp);   // barriers inside
@@ -208,18 +234,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
     float4 *de = reinterpret_cast<float4 *>(&s_e[tl * kPvEStride + 16 * r]);
 #pragma unroll
     for (int c = 0; c < 4; ++c) de[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
-    // probabilities: consecutive threads read consecutive tokens of one row
-    for (int i = tid; i < kGroupTiles * kPvRows; i += kDecThreads) {
-      const int rr = i >> 5, j = i & 31;
-      const int64_t tile = g * kGroupTiles + j;
-      const int row = row0 + rr;
-      float pv = 0.0f;
-      if (tile >= tile_lo && tile < tile_hi && row < rows) {
-        const int b = row / G, gq = row - b * G;
-        pv = a.qk.scores[((int64_t)b * Hq + (int64_t)h * G + gq) * T + (tile - tile_lo)];
-      }
-      s_p[j * kPvPStride + rr] = pv;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = tid + k * kDecThreads;
+      s_p[(i & 31) * kPvPStride + (i >> 5)] = pn[k];
     }
+    if (g + 1 < ge) pv_load_p(a, g + 1, h, row0, G, rows, tile_lo, tile_hi, pn);
     __syncthreads();
 #pragma unroll 4
     for (int j = 0; j < kGroupTiles; ++j) {
