@@ -79,7 +79,7 @@ struct QkArgs {
 // Decode attention: the K side is the scores pass (qk), the V side another
 // stream; probabilities overwrite qk.scores, partial P.E sums go to partials.
 constexpr int kPvRows = 64;           // query rows per contraction tile
-constexpr int kPvGroupsPerChunk = 16; // groups of 32 tokens per block
+constexpr int kPvGroupsPerChunk = 8;  // groups of 32 tokens per block
 struct AttnArgs {
   QkArgs qk;                // K stream, queries, rotated queries, scores -> probabilities
   DecodeArgs v;             // V stream
