@@ -282,7 +282,7 @@ namespace {
 // then the partial P . E rows of every (head, chunk, row tile).
 struct AttnGeometry {
   int64_t chunks = 0, rowtiles = 0;
-  size_t qrot = 0, scores = 0, partials = 0;
+  size_t qrot = 0, scores = 0, partials = 0, stats = 0;
 };
 
 bool attn_geometry(int n_kv, int64_t n_tokens, int B, int Hq, AttnGeometry *g) {
@@ -297,6 +297,7 @@ bool attn_geometry(int n_kv, int64_t n_tokens, int B, int Hq, AttnGeometry *g) {
   g->qrot = round256((size_t)B * Hq * HQ_TILE * sizeof(float));
   g->scores = round256((size_t)B * Hq * (size_t)n_tokens * sizeof(float));
   g->partials = (size_t)n_kv * g->chunks * g->rowtiles * hq::kPvRows * HQ_TILE * sizeof(float);
+  g->stats = (size_t)n_kv * g->chunks * g->rowtiles * hq::kPvRows * 2 * sizeof(float);
   return true;
 }
 
@@ -305,7 +306,7 @@ bool attn_geometry(int n_kv, int64_t n_tokens, int B, int Hq, AttnGeometry *g) {
 size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int B, int Hq) {
   AttnGeometry g;
   if (!attn_geometry(n_kv_heads, n_tokens, B, Hq, &g)) return 0;
-  return g.qrot + g.scores + g.partials;
+  return g.qrot + g.scores + g.partials + g.stats;
 }
 
 int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_t k_words,
@@ -323,7 +324,8 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
   if (pk->tiles_per_segment % n_tokens != 0 || pv->tiles_per_segment % n_tokens != 0)
     return HQ_ERR_INVALID;
   if (!d_k_stream || !d_k_offsets || !d_v_stream || !d_v_offsets || !d_q || !d_out || !d_ws ||
-      ws_bytes < g.qrot + g.scores + g.partials || !aligned(d_ws, 16) || !aligned(d_out, 16) ||
+      ws_bytes < g.qrot + g.scores + g.partials + g.stats || !aligned(d_ws, 16) ||
+      !aligned(d_out, 16) ||
       !aligned(d_k_offsets, 8) || !aligned(d_v_offsets, 8) || (d_probs && !aligned(d_probs, 4)))
     return HQ_ERR_INVALID;
   char *ws = reinterpret_cast<char *>(d_ws);
@@ -343,10 +345,13 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
   a.v.out_kind = -1;
   a.scale = scale;
   a.partials = reinterpret_cast<float *>(ws + g.qrot + g.scores);
+  a.stats = reinterpret_cast<float2 *>(ws + g.qrot + g.scores + g.partials);
   a.chunks = (int)g.chunks;
   a.rowtiles = (int)g.rowtiles;
   a.out = d_out;
-  return hq::launch_decode_attention(a, pk->lattice, pv->lattice, st) == 0 ? HQ_OK : HQ_ERR_CUDA;
+  return hq::launch_decode_attention(a, pk->lattice, pv->lattice, d_probs != nullptr, st) == 0
+             ? HQ_OK
+             : HQ_ERR_CUDA;
 }
 
 namespace {

@@ -182,13 +182,13 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_kernel(AttnArgs a) {
 constexpr int kPvEStride = kTile + 4;
 constexpr int kPvPStride = kPvRows + 4;
 
-// This thread's 8 probabilities of group g (element i = tid + 256 k of the
-// group's 64 rows x 32 tokens, row-major): consecutive threads read
-// consecutive tokens of one row; tokens outside head h or rows past the end
-// read as 0.
-__device__ __forceinline__ void pv_load_p(const AttnArgs &a, int64_t g, int h, int row0, int G,
+// This thread's 8 scaled scores z = fl(scale s) of group g (element
+// i = tid + 256 k of the group's 64 rows x 32 tokens, row-major): consecutive
+// threads read consecutive tokens of one row; tokens outside head h or rows
+// past the end read as -inf (probability 0).
+__device__ __forceinline__ void pv_load_z(const AttnArgs &a, int64_t g, int h, int row0, int G,
                                           int rows, int64_t tile_lo, int64_t tile_hi,
-                                          float p[8]) {
+                                          float z[8]) {
   const int64_t T = a.qk.n_tokens;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -196,10 +196,11 @@ __device__ __forceinline__ void pv_load_p(const AttnArgs &a, int64_t g, int h, i
     const int rr = i >> 5, j = i & 31;
     const int64_t tile = g * kGroupTiles + j;
     const int row = row0 + rr;
-    p[k] = 0.0f;
+    z[k] = -INFINITY;
     if (tile >= tile_lo && tile < tile_hi && row < rows) {
       const int b = row / G, gq = row - b * G;
-      p[k] = a.qk.scores[((int64_t)b * a.qk.Hq + (int64_t)h * G + gq) * T + (tile - tile_lo)];
+      z[k] = __fmul_rn(a.qk.scores[((int64_t)b * a.qk.Hq + (int64_t)h * G + gq) * T +
+                                   (tile - tile_lo)], a.scale);
     }
   }
 }
@@ -223,10 +224,37 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-  // the probabilities of a group are loaded one group ahead, so that their
-  // latency hides behind the decoding and the contraction of the current one
+  // this chunk's softmax statistics per row: m = max z over its tokens and
+  // l = sum exp(z - m) (four threads per row, then a fixed shuffle tree)
+  __shared__ float s_m[kPvRows];
+  {
+    const int rr = tid >> 2, q = tid & 3, row = row0 + rr;
+    const int64_t c_lo = max(gb * kGroupTiles, tile_lo), c_hi = min(ge * kGroupTiles, tile_hi);
+    const float *srow = nullptr;
+    if (row < rows) {
+      const int b = row / G, gq = row - b * G;
+      srow = a.qk.scores + ((int64_t)b * Hq + (int64_t)h * G + gq) * T - tile_lo;
+    }
+    float m = -INFINITY, l = 0.0f;
+    if (srow != nullptr)
+      for (int64_t t = c_lo + q; t < c_hi; t += 4) m = fmaxf(m, __fmul_rn(srow[t], a.scale));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    if (srow != nullptr && m != -INFINITY)
+      for (int64_t t = c_lo + q; t < c_hi; t += 4)
+        l = __fadd_rn(l, expf(__fsub_rn(__fmul_rn(srow[t], a.scale), m)));
+    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 1));
+    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 2));
+    if (q == 0) {
+      s_m[rr] = m;
+      a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(m, l);
+    }
+  }
+  __syncthreads();
+  // the scores of a group are loaded one group ahead, so that their latency
+  // hides behind the decoding and the contraction of the current one
   float pn[8];
-  if (gb < ge) pv_load_p(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
+  if (gb < ge) pv_load_z(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
   for (int64_t g = gb; g < ge; ++g) {            // block-uniform bounds
     float e[16];
     const bool ok = decode_lane<LAT, K>(a.v, g, e, s_start, s_warp);   // barriers inside
@@ -235,11 +263,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) de[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 8; ++k) {                // p = exp(z - m), 0 for z = -inf
       const int i = tid + k * kDecThreads;
-      s_p[(i & 31) * kPvPStride + (i >> 5)] = pn[k];
+      const float mm = s_m[i >> 5];
+      s_p[(i & 31) * kPvPStride + (i >> 5)] =
+          pn[k] == -INFINITY ? 0.0f : expf(__fsub_rn(pn[k], mm));
     }
-    if (g + 1 < ge) pv_load_p(a, g + 1, h, row0, G, rows, tile_lo, tile_hi, pn);
+    if (g + 1 < ge) pv_load_z(a, g + 1, h, row0, G, rows, tile_lo, tile_hi, pn);
     __syncthreads();
 #pragma unroll 4
     for (int j = 0; j < kGroupTiles; ++j) {
@@ -265,19 +295,29 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
   }
 }
 
-// out[b][hq] = D_h * fl(H (sum over chunks of the partial rows) * s_dec), the
-// chunks summed in order; one block of 128 threads per query row.
+// out[b][hq] = D_h * fl(H (sum_c w_c acc_c / sum_c w_c l_c) * s_dec) with
+// w_c = exp(m_c - max_c m_c): the chunks' softmax pieces rescaled to a common
+// maximum and summed in chunk order; one block of 128 threads per query row.
 __global__ void __launch_bounds__(kTile) pv_finish_kernel(AttnArgs a) {
   __shared__ float x[kTile];
   const int row = blockIdx.x, d = threadIdx.x;
   const int Hq = a.qk.Hq, G = Hq / a.qk.n_kv;
   const int b = row / Hq, hq = row - b * Hq, h = hq / G;
   const int rr = b * G + (hq - h * G), rt = rr / kPvRows, rl = rr - rt * kPvRows;
-  float s = 0.0f;
-  for (int c = 0; c < a.chunks; ++c)
-    s = __fadd_rn(s, a.partials[((((int64_t)h * a.chunks + c) * a.rowtiles + rt) * kPvRows + rl) *
-                                    kTile + d]);
-  x[d] = s;
+  const float2 *st = a.stats + ((int64_t)h * a.chunks * a.rowtiles + rt) * kPvRows + rl;
+  const int64_t cstride = (int64_t)a.rowtiles * kPvRows;
+  float M = -INFINITY;
+  for (int c = 0; c < a.chunks; ++c) M = fmaxf(M, st[c * cstride].x);
+  float L = 0.0f, s = 0.0f;
+  for (int c = 0; c < a.chunks; ++c) {
+    const float2 ml = st[c * cstride];
+    if (ml.x == -INFINITY) continue;             // a chunk without tokens of this head
+    const float w = expf(__fsub_rn(ml.x, M));
+    L = __fadd_rn(L, __fmul_rn(w, ml.y));
+    s = __fadd_rn(s, __fmul_rn(w, a.partials[((((int64_t)h * a.chunks + c) * a.rowtiles + rt) *
+                                                  kPvRows + rl) * kTile + d]));
+  }
+  x[d] = __fdiv_rn(s, L);
   __syncthreads();
 #pragma unroll
   for (int hh = 1; hh < kTile; hh <<= 1) {
@@ -436,11 +476,10 @@ int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 
-int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cudaStream_t st) {
+int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, bool want_probs,
+                            cudaStream_t st) {
   if (launch_decode_qk(a.qk, k_lattice, st) != 0) return 1;   // scores into a.qk.scores
   const unsigned rows = (unsigned)(a.qk.B * a.qk.Hq);
-  softmax_kernel<<<rows, kSoftmaxThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return 1;
   switch (v_lattice) {
     case 8: launch_pv_lat<8>(a, st); break;
     case 4: launch_pv_lat<4>(a, st); break;
@@ -449,7 +488,12 @@ int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cud
   }
   if (cudaGetLastError() != cudaSuccess) return 1;
   pv_finish_kernel<<<rows, kTile, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+  if (cudaGetLastError() != cudaSuccess) return 1;
+  if (want_probs) {                              // the scores become probabilities in place
+    softmax_kernel<<<rows, kSoftmaxThreads, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return 1;
+  }
+  return 0;
 }
 
 int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {

@@ -77,7 +77,8 @@ struct QkArgs {
 };
 
 // Decode attention: the K side is the scores pass (qk), the V side another
-// stream; probabilities overwrite qk.scores, partial P.E sums go to partials.
+// stream; each chunk of tokens keeps its own softmax maximum and sum (stats)
+// beside its partial sums of exp(z - max) e (partials).
 constexpr int kPvRows = 64;           // query rows per contraction tile
 constexpr int kPvGroupsPerChunk = 8;  // groups of 32 tokens per block
 struct AttnArgs {
@@ -85,6 +86,7 @@ struct AttnArgs {
   DecodeArgs v;             // V stream
   float scale;              // softmax scale applied to the scores
   float *partials;          // [n_kv][chunks][rowtiles][kPvRows][128]
+  float2 *stats;            // [n_kv][chunks][rowtiles][kPvRows]: (max z, sum exp(z - max))
   int chunks, rowtiles;
   float *out;               // [B][Hq][128] fp32
 };
@@ -118,7 +120,8 @@ int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st);
 int encode_tiles_per_block();
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st);
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);
-int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, cudaStream_t st);
+int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, bool want_probs,
+                            cudaStream_t st);
 int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st);
 
 }  // namespace hq
