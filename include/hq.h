@@ -214,8 +214,9 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
                  hq_stream_t stream);
 
 /* Bytes of device workspace hq_decode_attention needs: the rotated queries
- * (B * Hq * 128 fp32), the scores / probabilities (B * Hq * n_tokens fp32)
- * and the partial sums of the value contraction.  0 for invalid sizes. */
+ * (B * Hq * 128 fp32), the scores (B * Hq * n_tokens fp32), and per chunk of
+ * tokens the partial sums of the value contraction and the softmax maximum
+ * and sum of each query row.  0 for invalid sizes. */
 size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int B, int Hq);
 
 /* One decode step of attention read straight from compressed K and V
@@ -226,11 +227,12 @@ size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int
  * with Khat / Vhat the decodes of tile h * n_tokens + t of the K / V stream
  * (each with its own params pk / pv).  Neither K nor V is written out: the
  * value side is accumulated in the lattice domain and transformed once per
- * query row.
+ * query row; the softmax is formed per chunk of tokens (maximum and sum) and
+ * the chunks are combined in a fixed order, so the result is deterministic.
  *   d_q        [B][Hq][128] bf16, device.
  *   d_out      [B][Hq][128] fp32, device, 16-byte aligned.
- *   d_probs    optional [B][Hq][n_tokens] fp32 output of p (NULL: kept in
- *              the workspace only).
+ *   d_probs    optional [B][Hq][n_tokens] fp32 output of p (NULL: p is not
+ *              formed; the scores stay in the workspace).
  *   d_ws       >= hq_decode_attention_workspace_bytes() bytes, 16-byte aligned.
  *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group of either stream.
  * Requires Hq % n_kv_heads == 0 and every head's tiles in one sign segment of
