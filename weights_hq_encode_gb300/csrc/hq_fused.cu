@@ -125,7 +125,8 @@ scores_kernel(QkArgs a) {
 }
 
 // ---------------------------------------------------------------- attention
-// Softmax over the tokens of one query row, in place: p = exp(z - m) / l with
+// Softmax over the tokens of one query row, in place (only when the caller
+// asks for the probabilities): p = exp(z - m) / l with
 // z = fl(scale * s), m = max z and l = sum of exp(z - m) (per-thread running
 // maximum and rescaled sum, then combined over the block).
 constexpr int kSoftmaxThreads = 256;
@@ -171,14 +172,17 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_kernel(AttnArgs a) {
   }
 }
 
-// Partial sums P . E of one KV head over a chunk of its token groups, in the
-// lattice domain: V's tiles are decoded only to e = v - u (no inverse
-// transform per token), since sum_t p_t Vhat_t = D s_dec H (sum_t p_t e_t)
-// up to rounding; pv_finish_kernel applies H, s_dec and D once per query
-// row.  The group's e (32 tokens x 128) and probabilities (32 tokens x 64
+// Partial sums of one KV head over a chunk of its token groups, in the
+// lattice domain and in flash-decoding form: the block reduces the chunk's
+// scaled scores z to m = max z and l = sum exp(z - m) per query row, then
+// accumulates sum_t exp(z_t - m) e_t with V's tiles decoded only to
+// e = v - u (no inverse transform per token), since
+// sum_t p_t Vhat_t = D s_dec H (sum_t p_t e_t) up to rounding;
+// pv_finish_kernel combines the chunks and applies H, s_dec and D once per
+// query row.  The group's e (32 tokens x 128) and weights (32 tokens x 64
 // rows) are staged in shared memory; thread (rb, db) accumulates rows
 // 4rb..4rb+3 x dims 8db..8db+7 over all tokens of the chunk.  Tokens of the
-// group outside head h (a group that straddles two heads) get p = 0.
+// group outside head h (a group that straddles two heads) get weight 0.
 constexpr int kPvEStride = kTile + 4;
 constexpr int kPvPStride = kPvRows + 4;
 
