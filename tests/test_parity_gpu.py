@@ -225,6 +225,28 @@ def test_lookback_timeout_is_reported(hq, oracle):
     _check_case(hq, oracle, c, check_decode=False)
 
 
+def test_prepared_workspace_codes_identically(hq, oracle):
+    """With HQ_FLAG_WORKSPACE_READY the blocks take their groups from the
+    (caller-zeroed) ticket counter instead of their launch index: the stream,
+    index and status are the same bit for bit."""
+    rng = np.random.default_rng(6)
+    x = _rand_bits(rng, 777)
+    c = Case(x, 8, 2, 2.0, 1, 12, oracle.make_signs(6, 0), 1 << 40)
+    ref = oracle.encode(c.oracle_params(oracle), c.x_bits)
+    p = c.gpu_params(hq, flags=hq.HQ_FLAG_WORKSPACE_READY)
+    xt = bits_to_torch(x)
+    offsets = torch.zeros(hq.hq_num_groups(c.n) + 1, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.full((ref["total_words"] + 8,), -1, dtype=torch.int32, device="cuda")
+    for _ in range(2):                                  # the caller re-zeroes between calls
+        ws = torch.zeros(hq.hq_encode_workspace_bytes(c.n), dtype=torch.uint8, device="cuda")
+        assert hq.hq_encode(p, xt, c.n, stream, ref["total_words"], offsets, ws, status) == hq.HQ_OK
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert (offsets.cpu().numpy().view(np.uint64) == ref["offsets"]).all()
+        assert (u32(stream)[:ref["total_words"]] == ref["stream"][:ref["total_words"]]).all()
+
+
 def test_invalid_arguments(hq, oracle):
     x = bits_to_torch(np.zeros((4, 128), np.uint16))
     c = Case(np.zeros((4, 128), np.uint16), 8, 2, 1.0, 1, 0, oracle.make_signs(0, 0), 1 << 40)
