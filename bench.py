@@ -114,12 +114,17 @@ def oracle_sample_time(budget_s: float = 12.0, max_s: float = 30.0):
     mask = (O.make_signs(C["sign_seed"], 0) ^ O.make_signs(C["layer_sign_seed"], 0)).reshape(1, 4)
     threads = O.default_threads()
     elems, t0, reps = 0, time.perf_counter(), 0
+    t_enc = t_dec = 0.0
     while True:
         for r in RATES:
             c = cal["kv_cache_8b"]["E8"][r]
             P = O.make_params(8, c["k"], c["alpha"], 1, C["dither_seed"], mask, 1 << 40)
+            ta = time.perf_counter()
             enc = O.encode(P, x, threads=threads)
+            tb = time.perf_counter()
             O.decode(P, enc["stream"], enc["offsets"], x.shape[0], out="bf16", threads=threads)
+            t_enc += tb - ta
+            t_dec += time.perf_counter() - tb
             elems += 2 * x.size
         reps += 1
         dt = time.perf_counter() - t0
@@ -128,6 +133,24 @@ def oracle_sample_time(budget_s: float = 12.0, max_s: float = 30.0):
     gbs = 2.0 * elems / dt / 1e9
     sample = (f"{reps} x (encode+decode at 2 and 3 bps) of {x.shape[0]} tiles "
               f"(layer 0 K, 8 heads x 2048 tokens) in {dt:.1f} s")
+    half = elems / 2                                # elements encoded (= decoded)
+    detail = {"encode_GBps": round(2.0 * half / t_enc / 1e9, 4),
+              "decode_GBps": round(2.0 * half / t_dec / 1e9, 4),
+              "encode_ns_per_elem": round(t_enc / half * 1e9, 2),
+              "decode_ns_per_elem": round(t_dec / half * 1e9, 2)}
+    # one core on a smaller slice (a fixed 1024 tiles at 3 bps)
+    c = cal["kv_cache_8b"]["E8"]["3.0"]
+    P = O.make_params(8, c["k"], c["alpha"], 1, C["dither_seed"], mask, 1 << 40)
+    xs = x[:1024]
+    ta = time.perf_counter()
+    enc = O.encode(P, xs, threads=1)
+    tb = time.perf_counter()
+    O.decode(P, enc["stream"], enc["offsets"], xs.shape[0], out="bf16", threads=1)
+    tc = time.perf_counter()
+    detail["single_core"] = {"encode_ns_per_elem": round((tb - ta) / xs.size * 1e9, 2),
+                             "decode_ns_per_elem": round((tc - tb) / xs.size * 1e9, 2),
+                             "sample": "1024 tiles at 3 bps, one thread"}
+    oracle_sample_time.detail = detail
     return gbs, threads, sample, dt / reps
 
 
@@ -266,7 +289,8 @@ def run_ours(args, rank, world):
         traffic = tr["kernels"][dom]
     roof = {"bound": "hbm", "kernel": dom, "achieved": op_report[dom]["achieved_GBps"],
             "peak": peak, "unit": "GB/s", "frac": op_report[dom]["roofline_frac"],
-            "traffic": traffic, "peak_kind": peak_kind}
+            "traffic": traffic, "peak_kind": peak_kind,
+            "frac_of_nominal_8TBps": round(op_report[dom]["achieved_GBps"] / 8000.0, 4)}
 
     # ---- end to end through the C ABI with host buffers
     e2e = None if args.skip_e2e else run_e2e(args, hq, params, xt, n, ng, total, dev, world)
@@ -275,12 +299,13 @@ def run_ours(args, rank, world):
     fused = run_fused(hq, I, cal, dev, args) if rank == 0 and not args.skip_fused else None
     attn = run_attention(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
     gemm = run_gemm(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
+    extra = run_extra_workloads(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, sample, _ = oracle_sample_time()
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": sample}
+               "sample": sample, **getattr(oracle_sample_time, "detail", {})}
     if rank == 0:
         res = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -293,7 +318,7 @@ def run_ours(args, rank, world):
                           "parallelism": f"{world} independent replicas (tile shards)"},
                "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
                "gpu_launches": len(order) * args.steps, "fused_scores": fused,
-               "fused_attention": attn, "fused_gemm": gemm,
+               "fused_attention": attn, "fused_gemm": gemm, "other_workloads": extra,
                "cpu_baseline": cpu, "source_hash": source_hash()}
         print(json.dumps(res), flush=True)
 
@@ -485,6 +510,87 @@ def run_attention(hq, I, cal, dev):
             "achieved_GBps": round(alg / (ms * 1e-3) / 1e9, 1),
             "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
             "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2), "status": int(st.item())}
+
+
+def _time_codec(hq, p, xt, n, dev, reps=5):
+    """(encode ms, decode ms, realized payload+padding bps) of one call over
+    xt with params p; CUDA events on the current stream, 3 warm-ups."""
+    import torch
+    ng = hq.hq_num_groups(n)
+    offs = torch.zeros(ng + 1, dtype=torch.int64, device=dev)
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert hq.hq_encode(p, xt, n, None, 0, offs, ws, st) == 0
+    torch.cuda.synchronize()
+    tot = int(offs[-1].item())
+    buf = torch.empty(tot + 1, dtype=torch.int32, device=dev)
+    out = torch.empty((n, 128), dtype=torch.bfloat16, device=dev)
+    st.zero_()
+    res = []
+    for f in (lambda: hq.hq_encode(p, xt, n, buf, tot, offs, ws, st),
+              lambda: hq.hq_decode(p, buf, tot, offs, n, out, hq.HQ_OUT_BF16, st)):
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b) / reps)
+    if int(st.item()):
+        raise RuntimeError(f"status {hq.hq_status_string(int(st.item()))}")
+    return res[0], res[1], tot * 32.0 / (n * 128)
+
+
+def run_extra_workloads(hq, I, cal, dev):
+    """The other stand-in workloads, timed beside the step: the four
+    Llama-3.1-8B-shaped weight matrices (E8, no dither, 3/4/5 bps, one call
+    per matrix) and one long-context layer (K and V, 8 heads x 131072 tokens)
+    for every lattice and rate of the frozen calibration."""
+    import numpy as np
+    import torch
+    out = {}
+    C = I.WEIGHTS8B
+    m = hq.hq_make_signs(C["sign_seed"], 0)
+    signs = torch.from_numpy(np.asarray(m, np.uint32).view(np.int32).reshape(1, 4)).to(dev)
+    mats = [hq.as_tiles(I.weight_matrix(i, dev)) for i in range(len(C["shapes"]))]
+    elems = sum(t.shape[0] * 128 for t in mats)
+    w = {}
+    for rate in ("3.0", "4.0", "5.0"):
+        te = td = bits = 0.0
+        for i, xt in enumerate(mats):
+            c = cal["weights_8b"]["E8"][rate][i]
+            p = hq.make_params(8, c["k"], c["alpha"], 0, 0, signs, 1 << 40)
+            e, d, bps = _time_codec(hq, p, xt, xt.shape[0], dev)
+            te, td, bits = te + e, td + d, bits + bps * xt.shape[0] * 128
+        w[rate] = {"encode_ms": round(te, 4), "decode_ms": round(td, 4),
+                   "encode_GBps_bf16eq": round(2.0 * elems / (te * 1e-3) / 1e9, 1),
+                   "decode_GBps_bf16eq": round(2.0 * elems / (td * 1e-3) / 1e9, 1),
+                   "realized_bps": round(bits / elems, 4)}
+    out["weights_8b"] = {"workload": "4096x4096, 1024x4096, 4096x14336, 14336x4096 bf16 "
+                                     "(138 M elements), one call per matrix", **w}
+    del mats
+    L = I.LONGCTX
+    x = I.long_context_layer(dev)
+    xt = hq.as_tiles(x)
+    n = xt.shape[0]
+    mask = [a ^ b for a, b in zip(hq.hq_make_signs(L["sign_seed"], 0),
+                                  hq.hq_make_signs(L["layer_sign_seed"], 0))]
+    lsigns = torch.from_numpy(np.asarray(mask, np.uint32).view(np.int32).reshape(1, 4)).to(dev)
+    lc = {}
+    for name, lat in (("Z", 1), ("A2", 2), ("D4", 4), ("E8", 8)):
+        for rate, c in cal["long_context"].get(name, {}).items():
+            p = hq.make_params(lat, c["k"], c["alpha"], 1, L["dither_seed"], lsigns, 1 << 40)
+            e, d, bps = _time_codec(hq, p, xt, n, dev)
+            lc[f"{name}@{rate}"] = {"encode_ms": round(e, 4), "decode_ms": round(d, 4),
+                                    "encode_GBps_bf16eq": round(2.0 * n * 128 / (e * 1e-3) / 1e9, 1),
+                                    "decode_GBps_bf16eq": round(2.0 * n * 128 / (d * 1e-3) / 1e9, 1),
+                                    "realized_bps": round(bps, 4)}
+    out["long_context"] = {"workload": "one layer's K and V, 8 heads x 131072 tokens (512 MiB bf16), "
+                                       "dither on", **lc}
+    return out
 
 
 def run_gemm(hq, I, cal, dev):
