@@ -40,6 +40,7 @@ __global__ void rotate_queries_kernel(QkArgs a) {
 // read distinct banks; tiles of another head read their rows from global.
 constexpr int kQkRowsSmem = 64;
 constexpr int kQkLaneStride = 20;                // 16 values + 4 floats of padding
+constexpr int kQkEStride = kTile + 4;            // the group's e in the common case
 template <int LAT, int K>
 __global__ void __launch_bounds__(kDecThreads, 3)
 scores_kernel(QkArgs a) {
@@ -70,6 +71,54 @@ scores_kernel(QkArgs a) {
   const int h = valid ? (int)div_by(tile, a.n_tokens, a.tok_shift) : h0;
   const int64_t tok = valid ? tile - (int64_t)h * a.n_tokens : 0;
   const bool from_smem = staged && h == h0;
+  // Common case: every query row staged and all 32 tiles tokens of head h0.
+  // The group's e goes to shared memory and the 32 x rows block of scores is
+  // a small product there: thread (tt, rq) computes tokens tt and tt + 16
+  // for rows 4rq .. 4rq+3, each score one chain over d.
+  const int64_t last = min(g * kGroupTiles + kGroupTiles, a.dec.n_tiles) - 1;
+  if (staged && (int)div_by(last, a.n_tokens, a.tok_shift) == h0) {   // uniform
+    __shared__ __align__(16) float s_et[kGroupTiles * kQkEStride];
+    float4 *de = reinterpret_cast<float4 *>(&s_et[tl * kQkEStride + 16 * r]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) de[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    __syncthreads();
+    const int tt = tid & 15, rq = tid >> 4;
+    if (4 * rq < rows) {
+      float acc[4][2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.0f;
+      const int rlim = min(4, rows - 4 * rq);
+#pragma unroll 2
+      for (int k = 0; k < kTile; k += 4) {
+        const float4 e0 = *reinterpret_cast<const float4 *>(&s_et[tt * kQkEStride + k]);
+        const float4 e1 = *reinterpret_cast<const float4 *>(&s_et[(tt + 16) * kQkEStride + k]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * rq + (i < rlim ? i : 0);
+          const float4 qv = *reinterpret_cast<const float4 *>(
+              &s_q[(rr * 8 + (k >> 4)) * kQkLaneStride + (k & 15)]);
+          acc[i][0] = __fmaf_rn(qv.x, e0.x, acc[i][0]);
+          acc[i][0] = __fmaf_rn(qv.y, e0.y, acc[i][0]);
+          acc[i][0] = __fmaf_rn(qv.z, e0.z, acc[i][0]);
+          acc[i][0] = __fmaf_rn(qv.w, e0.w, acc[i][0]);
+          acc[i][1] = __fmaf_rn(qv.x, e1.x, acc[i][1]);
+          acc[i][1] = __fmaf_rn(qv.y, e1.y, acc[i][1]);
+          acc[i][1] = __fmaf_rn(qv.z, e1.z, acc[i][1]);
+          acc[i][1] = __fmaf_rn(qv.w, e1.w, acc[i][1]);
+        }
+      }
+      const int64_t t0 = g * kGroupTiles - (int64_t)h0 * a.n_tokens;   // token of tile 0
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i >= rlim) break;
+        const int rr = 4 * rq + i, b = rr / G, gq = rr - b * G;
+        float *dst = a.scores + ((int64_t)b * a.Hq + (int64_t)h0 * G + gq) * a.n_tokens + t0;
+        if (g * kGroupTiles + tt < a.dec.n_tiles) dst[tt] = acc[i][0];
+        if (g * kGroupTiles + tt + 16 < a.dec.n_tiles) dst[tt + 16] = acc[i][1];
+      }
+    }
+    return;
+  }
   for (int r0 = 0; r0 < rows; r0 += 8) {
     float p[8];
 #pragma unroll
