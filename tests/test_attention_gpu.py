@@ -11,8 +11,13 @@ transform stages and one scaling) with e, so |dz_t| <= (128 + 8) u zeta,
 zeta = scale |q| max_t |Khat_t| (the transform is orthogonal, so
 |q'| |e_t| = |q| |Khat_t|).  Softmax turns that into a relative error of
 p_t of at most 2 max|dz| plus a few u for exp and the division.  The value
-side sums p_t e_t in fp32 over at most 256 tokens per chunk and 129 chunks
-per head, adding (256 + 129) u < 400 u relative to sum_t p_t |Vhat_t,d|.  So an
+side sums p_t e_t over at most 256 tokens per chunk on the tensor cores:
+both operands split into two tf32 parts (|x - hi - lo| <= 2^-22 |x| = 4 u |x|,
+so each product of the parts is within 8 u of p_t e_t), the products exact,
+accumulated in fp32 tensor memory over 64 MMA steps per chunk (2 u per step
+even if the accumulation truncates: 128 u), the two halves of the split
+added once (u), then 129 chunks per head combined in fp32 (129 u): together
+(8 + 128 + 1 + 129) u < 400 u relative to sum_t p_t |Vhat_t,d|.  So an
 element of out is held to (2 * 136 u zeta + 600 u) of sum_t p_t |Vhat_t,d|,
 i.e. (1.7e-5 zeta + 3.6e-5), and p_t to (1.7e-5 zeta + 1e-6) of p_t plus
 1e-38 for values below the fp32 normal range."""

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "hq_decode_lane.cuh"
+#include "hq_umma.cuh"
 
 namespace hq {
 
@@ -228,12 +229,26 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_kernel(AttnArgs a) {
 // e = v - u (no inverse transform per token), since
 // sum_t p_t Vhat_t = D s_dec H (sum_t p_t e_t) up to rounding;
 // pv_finish_kernel combines the chunks and applies H, s_dec and D once per
-// query row.  The group's e (32 tokens x 128) and weights (32 tokens x 64
-// rows) are staged in shared memory; thread (rb, db) accumulates rows
-// 4rb..4rb+3 x dims 8db..8db+7 over all tokens of the chunk.  Tokens of the
-// group outside head h (a group that straddles two heads) get weight 0.
-constexpr int kPvEStride = kTile + 4;
-constexpr int kPvPStride = kPvRows + 4;
+// query row.  Tokens of the group outside head h (a group that straddles two
+// heads) get weight 0.
+//
+// The contraction runs on the tensor cores (tcgen05, kind::tf32, fp32
+// accumulator in tensor memory): per group, D[d][n] += sum_t E^T[d][t] B[n][t]
+// with M = 128 dimensions d, K = 32 tokens and N = 128 columns that stack the
+// tf32 split of the weights, B = [p_hi (64 rows); p_lo (64 rows)], each issued
+// twice (A = e_hi^T, then e_lo^T).  The four partial products of the split
+// operands give an fp32-level result: column n of D holds (e_hi + e_lo) p_hi
+// and column 64 + n holds (e_hi + e_lo) p_lo of row n, added once at the end.
+// The block's 256 threads decode group g + 1 while the MMAs of group g run.
+constexpr int kPvAKStride = 2304;                // bytes between K-cores of e^T (16 d-groups of 144)
+constexpr int kPvAGStride = 144;                 // bytes between 8-dimension groups (16 B of padding)
+constexpr int kPvBKStride = 144;                 // bytes between K-cores of B (16 B of padding)
+constexpr int kPvBGStride = 1152;                // bytes between 8-row groups of B
+constexpr int kPvOpBytes = 8 * kPvAKStride;      // 18432 per operand (e_hi^T, e_lo^T, B)
+constexpr int kPvSmemBytes = 3 * kPvOpBytes;
+constexpr uint32_t kPvIdesc = umma_idesc_tf32(128, 128);
+constexpr uint32_t kPvTmemCols = 128;
+constexpr uint32_t kPvWaitLimit = 1u << 22;
 
 // This thread's 8 scaled scores z = fl(scale s) of group g (element
 // i = tid + 256 k of the group's 64 rows x 32 tokens, row-major): consecutive
@@ -258,12 +273,14 @@ __device__ __forceinline__ void pv_load_z(const AttnArgs &a, int64_t g, int h, i
   }
 }
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
-  __shared__ __align__(16) float s_e[kGroupTiles * kPvEStride];
-  __shared__ __align__(16) float s_p[kGroupTiles * kPvPStride];
-  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
+  __shared__ float s_m[kPvRows];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ uint32_t s_taddr;
+  extern __shared__ __align__(128) unsigned char s_ops[];   // e_hi^T | e_lo^T | B
+  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7, warp = tid >> 5;
   const int chunk = blockIdx.x, h = blockIdx.y, rt = blockIdx.z;
   const int64_t T = a.qk.n_tokens;
   const int Hq = a.qk.Hq, G = Hq / a.qk.n_kv, rows = a.qk.B * G, row0 = rt * kPvRows;
@@ -271,15 +288,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
   const int64_t g_first = tile_lo / kGroupTiles, g_end = (tile_hi - 1) / kGroupTiles + 1;
   const int64_t gb = g_first + (int64_t)chunk * kPvGroupsPerChunk;
   const int64_t ge = min(gb + (int64_t)kPvGroupsPerChunk, g_end);
-  const int rb = tid >> 4, db = tid & 15;
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  if (warp == 0) tmem_alloc(&s_taddr, kPvTmemCols);
+  if (tid == 32) mbar_init(&s_bar, 1);
   // this chunk's softmax statistics per row: m = max z over its tokens and
   // l = sum exp(z - m) (four threads per row, then a fixed shuffle tree)
-  __shared__ float s_m[kPvRows];
   {
     const int rr = tid >> 2, q = tid & 3, row = row0 + rr;
     const int64_t c_lo = max(gb * kGroupTiles, tile_lo), c_hi = min(ge * kGroupTiles, tile_hi);
@@ -303,48 +315,98 @@ __global__ void __launch_bounds__(kDecThreads, 2) pv_kernel(AttnArgs a) {
       a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(m, l);
     }
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = s_taddr;
+  const uint32_t a_hi = smem_addr(s_ops), a_lo = a_hi + kPvOpBytes, b_op = a_hi + 2 * kPvOpBytes;
+  // this thread's slots: e^T (d = 16 r + c, token tl) and B (row i >> 5, token i & 31)
+  float *const ehi = reinterpret_cast<float *>(s_ops) +
+                     (288 * r + (tl >> 2) * kPvAKStride + (tl & 3) * 4) / 4;
+  float *const elo = ehi + kPvOpBytes / 4;
+  float *const bp = reinterpret_cast<float *>(s_ops + 2 * kPvOpBytes) +
+                    ((tid >> 5) * 16 + ((tid & 31) >> 2) * kPvBKStride + (tid & 3) * 4) / 4;
+  bool ok_wait = true;                           // block-uniform
+  int committed = 0;                             // groups whose MMAs were issued
   // the scores of a group are loaded one group ahead, so that their latency
-  // hides behind the decoding and the contraction of the current one
+  // hides behind the decoding of the current one
   float pn[8];
   if (gb < ge) pv_load_z(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
   for (int64_t g = gb; g < ge; ++g) {            // block-uniform bounds
+    const int i = (int)(g - gb);
     float e[16];
     const bool ok = decode_lane<LAT, K>(a.v, g, e, s_start, s_warp);   // barriers inside
     if (!ok && tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_CORRUPT);
-    float4 *de = reinterpret_cast<float4 *>(&s_e[tl * kPvEStride + 16 * r]);
+    // the MMAs of the previous group must be done with the operands
+    if (i > 0 && ok_wait) ok_wait = mbar_wait(&s_bar, (uint32_t)(i - 1) & 1u, kPvWaitLimit);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) de[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    for (int c = 0; c < 16; ++c) {
+      float hi, lo;
+      split_tf32(e[c], hi, lo);
+      const int off = ((c >> 3) * kPvAGStride + (c & 7) * 16) / 4;
+      ehi[off] = hi;
+      elo[off] = lo;
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {                // p = exp(z - m), 0 for z = -inf
-      const int i = tid + k * kDecThreads;
-      const float mm = s_m[i >> 5];
-      s_p[(i & 31) * kPvPStride + (i >> 5)] =
-          pn[k] == -INFINITY ? 0.0f : expf(__fsub_rn(pn[k], mm));
+      const float mm = s_m[(tid >> 5) + 8 * k];
+      const float p = pn[k] == -INFINITY ? 0.0f : expf(__fsub_rn(pn[k], mm));
+      float hi, lo;
+      split_tf32(p, hi, lo);
+      bp[k * kPvBGStride / 4] = hi;              // rows (tid >> 5) + 8 k
+      bp[(k + 8) * kPvBGStride / 4] = lo;        // rows 64 + (tid >> 5) + 8 k
     }
     if (g + 1 < ge) pv_load_z(a, g + 1, h, row0, G, rows, tile_lo, tile_hi, pn);
-    __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < kGroupTiles; ++j) {
-      const float4 pj = *reinterpret_cast<const float4 *>(&s_p[j * kPvPStride + 4 * rb]);
-      const float4 e0 = *reinterpret_cast<const float4 *>(&s_e[j * kPvEStride + 8 * db]);
-      const float4 e1 = *reinterpret_cast<const float4 *>(&s_e[j * kPvEStride + 8 * db + 4]);
-      const float pr[4] = {pj.x, pj.y, pj.z, pj.w};
-      const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    fence_async_smem();
+    ok_wait = __syncthreads_and(ok_wait) != 0;
+    if (!ok_wait) continue;
+    ++committed;
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_tf32(taddr, umma_desc(a_hi + ks * 2 * kPvAKStride, kPvAKStride, kPvAGStride),
+                  umma_desc(b_op + ks * 2 * kPvBKStride, kPvBKStride, kPvBGStride), kPvIdesc,
+                  (i > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[i][c] = __fmaf_rn(pr[i], ev[c], acc[i][c]);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_tf32(taddr, umma_desc(a_lo + ks * 2 * kPvAKStride, kPvAKStride, kPvAGStride),
+                  umma_desc(b_op + ks * 2 * kPvBKStride, kPvBKStride, kPvBGStride), kPvIdesc, 1u);
+      umma_commit(&s_bar);
     }
-    __syncthreads();
   }
-  float *part = a.partials +
-                ((((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows) * kTile;
+  if (committed > 0) {
+    if (ok_wait) ok_wait = mbar_wait(&s_bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
+    ok_wait = __syncthreads_and(ok_wait) != 0;
+    if (ok_wait) {
+      tc_fence_after();
+      // warp w reads dimensions 32 (w % 4) + lane for rows 32 (w / 4) .. +31
+      const int qd = warp & 3, hf = warp >> 2, d = 32 * qd + (tid & 31);
+      float *part = a.partials +
+                    ((((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows) * kTile;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)(4 * rb + i) * kTile + 8 * db);
-    dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      for (int jj = 0; jj < 2; ++jj) {
+        float vh[16], vl[16];
+        const uint32_t lane_addr = taddr + ((uint32_t)(32 * qd) << 16);
+        tmem_ld16(lane_addr + (uint32_t)(32 * hf + 16 * jj), vh);
+        tmem_ld16(lane_addr + (uint32_t)(64 + 32 * hf + 16 * jj), vl);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          part[(int64_t)(32 * hf + 16 * jj + j) * kTile + d] = __fadd_rn(vh[j], vl[j]);
+      }
+    }
+  }
+  if (!ok_wait) {
+    if (tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_TIMEOUT);
+    // the operands' last MMAs may still be in flight: give them a bounded
+    // while before the tensor memory goes back
+    if (committed > 0) mbar_wait(&s_bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(taddr, kPvTmemCols);
   }
 }
 
@@ -494,14 +556,20 @@ static void launch_qk_lat(const QkArgs &a, cudaStream_t st) {
   }
 }
 
+template <int LAT, int K>
+static void launch_pv_one(const AttnArgs &a, dim3 grid, dim3 block, cudaStream_t st) {
+  cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
+  pv_kernel<LAT, K><<<grid, block, kPvSmemBytes, st>>>(a);
+}
+
 template <int LAT>
 static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
   dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kDecThreads);
   switch (a.v.rice_k) {
-    case 1: pv_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
-    case 2: pv_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
-    case 3: pv_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
-    default: pv_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+    case 1: launch_pv_one<LAT, 1>(a, grid, block, st); break;
+    case 2: launch_pv_one<LAT, 2>(a, grid, block, st); break;
+    case 3: launch_pv_one<LAT, 3>(a, grid, block, st); break;
+    default: launch_pv_one<LAT, -1>(a, grid, block, st); break;
   }
 }
 
