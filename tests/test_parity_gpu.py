@@ -402,8 +402,10 @@ def _scores_case(hq, oracle, n_kv, T, B, Hq, seed_tok):
     return K, q, p, stream, offsets, total, scores, mask, cal
 
 
-def test_decode_qk_against_oracle_scores(hq, oracle):
-    n_kv, T, B, Hq = 2, 200, 3, 8
+@pytest.mark.parametrize("n_kv,T,B,Hq", [(2, 200, 3, 8), (2, 200, 20, 8), (3, 77, 1, 3)])
+def test_decode_qk_against_oracle_scores(hq, oracle, n_kv, T, B, Hq):
+    """Heads that start inside a group (T not a multiple of 32), more query
+    rows per head than one 64-row tile (20 x 4 = 80), one row per head."""
     K, q, p, stream, offsets, total, scores, mask, cal = _scores_case(hq, oracle, n_kv, T, B, Hq,
                                                                       500)
     P = oracle.make_params(8, cal["k"], cal["alpha"], 1, 500, mask, n_kv * T)

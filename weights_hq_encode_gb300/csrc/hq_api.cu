@@ -335,7 +335,6 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
   a.qk.dec.out_kind = -1;
   a.qk.n_kv = n_kv_heads;
   a.qk.n_tokens = n_tokens;
-  a.qk.tok_shift = pow2_shift(n_tokens);
   a.qk.q = d_q;
   a.qk.B = B;
   a.qk.Hq = Hq;
@@ -425,7 +424,6 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
   a.dec.out_kind = -1;
   a.n_kv = n_kv_heads;
   a.n_tokens = n_tokens;
-  a.tok_shift = pow2_shift(n_tokens);
   a.q = d_q;
   a.B = B;
   a.Hq = Hq;

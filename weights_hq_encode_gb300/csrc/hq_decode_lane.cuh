@@ -20,6 +20,44 @@ namespace hq {
 
 constexpr int kDecThreads = 256;
 
+// Synchronisation of the 256 threads that decode one group: the whole block
+// (BlockBar), or team t = threadIdx.x / 256 of a larger block on named
+// barrier 1 + t (TeamBar), so that several teams decode different groups
+// independently.
+struct BlockBar {
+  __device__ static int tid() { return threadIdx.x; }
+  __device__ static void sync() { __syncthreads(); }
+  __device__ static int sync_or(int p) { return __syncthreads_or(p); }
+  __device__ static int sync_and(int p) { return __syncthreads_and(p); }
+};
+struct TeamBar {
+  __device__ static int tid() { return threadIdx.x & (kDecThreads - 1); }
+  __device__ static uint32_t id() { return 1u + (threadIdx.x / kDecThreads); }
+  __device__ static void sync() {
+    asm volatile("bar.sync %0, %1;" ::"r"(id()), "n"(kDecThreads) : "memory");
+  }
+  __device__ static int sync_or(int p) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(p), "r"(id()), "n"(kDecThreads)
+        : "memory");
+    return r;
+  }
+  __device__ static int sync_and(int p) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(p), "r"(id()), "n"(kDecThreads)
+        : "memory");
+    return r;
+  }
+};
+
 // nb (1..64) bits starting at bit `pos` of W, MSB-first, right-aligned.
 __device__ __forceinline__ uint64_t read_bits(const uint32_t *W, uint64_t pos, int nb) {
   const uint64_t w = pos >> 5;
@@ -99,12 +137,12 @@ __device__ __forceinline__ Quot8<P> unary8_general(const uint32_t *W, P pos, P n
 // below 2^31 bits (every group of a sane stream), 64-bit otherwise.  The
 // return value is block-uniform: false when the group is corrupt (e is then
 // all zeros).
-template <int LAT, int K, class P>
+template <int LAT, int K, class P, class Bar>
 __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, int nt,
                                               const uint32_t *W, P nwords, bool bad,
                                               float e[16], P *s_start,
                                               uint32_t (*s_warp)[kDecThreads / 32]) {
-  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7, lane = tid & 31, warp = tid >> 5;
+  const int tid = Bar::tid(), tl = tid >> 3, r = tid & 7, lane = tid & 31, warp = tid >> 5;
   const int k = K >= 0 ? K : a.rice_k;
   const P R = (P)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
   const P ustart = (P)nt * R;
@@ -132,7 +170,7 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
         }
       }
       if (lane == 31) s_warp[par][warp] = incl;
-      __syncthreads();
+      Bar::sync();
       static_assert(kDecThreads / 32 == 8, "two 16-byte reads of the warp totals");
       const uint4 q0 = reinterpret_cast<const uint4 *>(s_warp[par])[0];
       const uint4 q1 = reinterpret_cast<const uint4 *>(s_warp[par])[1];
@@ -158,7 +196,7 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
     }
   }
   if (tid == 0) s_start[0] = ustart;
-  __syncthreads();
+  Bar::sync();
   if (!bad && (ones != want || ((s_start[8 * nt] + 31) >> 5) != nwords)) bad = true;
 
   // ---- this lane's symbols: remainder bits first, then the quotients
@@ -257,7 +295,7 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
     }
     if (slow && posj != stop) lbad = true;       // bit after the last code
   }
-  const int any_bad = __syncthreads_or((bad || lbad) ? 1 : 0);
+  const int any_bad = Bar::sync_or((bad || lbad) ? 1 : 0);
   if (any_bad || !valid) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) e[i] = 0.0f;
@@ -267,7 +305,7 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
 
 // Dispatch on the group's size: 32-bit bit positions unless the group holds
 // 2^31 bits or more.
-template <int LAT, int K>
+template <int LAT, int K, class Bar = BlockBar>
 __device__ __forceinline__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16],
                                             uint64_t *s_start64,
                                             uint32_t (*s_warp)[kDecThreads / 32]) {
@@ -278,9 +316,9 @@ __device__ __forceinline__ bool decode_lane(const DecodeArgs &a, int64_t g, floa
   const uint64_t nwords = bad ? 0 : end - base;
   const uint32_t *W = a.stream + (bad ? 0 : base);
   if (nwords < (1ull << 26))
-    return decode_lane_p<LAT, K, uint32_t>(a, g, nt, W, (uint32_t)nwords, bad, e,
+    return decode_lane_p<LAT, K, uint32_t, Bar>(a, g, nt, W, (uint32_t)nwords, bad, e,
                                            reinterpret_cast<uint32_t *>(s_start64), s_warp);
-  return decode_lane_p<LAT, K, uint64_t>(a, g, nt, W, nwords, bad, e, s_start64, s_warp);
+  return decode_lane_p<LAT, K, uint64_t, Bar>(a, g, nt, W, nwords, bad, e, s_start64, s_warp);
 }
 
 }  // namespace hq

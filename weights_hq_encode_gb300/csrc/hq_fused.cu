@@ -33,144 +33,173 @@ __global__ void rotate_queries_kernel(QkArgs a) {
   for (int i = 0; i < 128; ++i) a.qrot[(int64_t)row * kTile + i] = __fmul_rn(x[i], a.dec.s_dec);
 }
 
-// Scores of one group of K tiles.  Lane r holds 16 lattice-domain values of
-// its tile; partial dots with 8 query rows at a time are reduced over the
-// tile's 8 lanes by a butterfly that leaves one finished row on each lane.
-// The rotated query rows of the head of the group's first tile are staged in
-// shared memory, laid out [row][lane r][16 + 4] so that the 8 lanes of a tile
-// read distinct banks; tiles of another head read their rows from global.
-constexpr int kQkRowsSmem = 64;
-constexpr int kQkLaneStride = 20;                // 16 values + 4 floats of padding
-constexpr int kQkEStride = kTile + 4;            // the group's e in the common case
+// Scores of one KV head over a chunk of its token groups for one tile of
+// up to 64 query rows, on the tensor cores (tcgen05, kind::tf32, fp32
+// accumulator in tensor memory).  The fp32-level product of the split
+// operands is laid along K: with q' = q_hi + q_lo and e = e_hi + e_lo (each
+// part tf32), A = [q_hi | q_lo | q_hi] and B = [e_hi | e_hi | e_lo] over
+// K = 3 x 128, so one accumulator lane per query row receives
+// q_hi e_hi + q_lo e_hi + q_hi e_lo (the dropped q_lo e_lo is below 2^-22 of
+// each product).  M = 128 with rows 64..127 of A aliasing the next K-core
+// (their results are never read), N = 32 tokens of a group.
+//
+// The block holds the split query rows once and runs four independent teams
+// of 256 threads (named barriers), each decoding every fourth group of the
+// chunk into its own B and accumulator columns: a team decodes its next group
+// while the MMAs of its previous one run, then writes that group's scores
+// from tensor memory.  Dimensions are permuted consistently in A and B
+// (16-byte block 4 r + c of d goes to K-core 8 c + r) so that the eight lanes
+// of a tile store e to distinct banks.
+constexpr int kQkRows = 64;                      // query rows per block
+constexpr int kQkTeams = 4;
+constexpr int kQkThreads = kQkTeams * kDecThreads;
+constexpr int kQkGroupsPerChunk = 2 * kQkTeams;  // groups of 32 tokens per block
+constexpr int kQkAKStride = 1024;                // bytes between K-cores of A (8 row groups)
+constexpr int kQkAGStride = 128;                 // bytes between 8-row groups of A
+constexpr int kQkBKStride = 528;                 // bytes between K-cores of B (4 token groups + 16)
+constexpr int kQkBGStride = 128;                 // bytes between 8-token groups of B
+constexpr int kQkABytes = 64 * kQkAKStride + 1024;   // [q_hi | q_lo] + the aliased rows' reach
+constexpr int kQkBBytes = 64 * kQkBKStride;          // [e_hi | e_lo] of one team
+constexpr int kQkSmemBytes = kQkABytes + kQkTeams * kQkBBytes;
+constexpr uint32_t kQkIdesc = umma_idesc_tf32(128, 32);
+constexpr uint32_t kQkTmemCols = 32 * kQkTeams;
+
+// K-core of the 16-byte block db (0..31) of the 128 dimensions.
+__device__ __forceinline__ int qk_kcore(int db) { return 8 * (db & 3) + (db >> 2); }
+
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 3)
-scores_kernel(QkArgs a) {
-  __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
-  __shared__ __align__(16) float s_q[kQkRowsSmem * 8 * kQkLaneStride];
-  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
-  const int64_t g = blockIdx.x;
-  const int G = a.Hq / a.n_kv;
-  const int rows = a.B * G;                     // query rows that read one head
-  const int h0 = (int)div_by(g * kGroupTiles, a.n_tokens, a.tok_shift);
-  const bool staged = rows <= kQkRowsSmem;
-  if (staged) {
-    for (int i = tid; i < rows * 32; i += kDecThreads) {   // float4 units
-      const int rr = i >> 5, c4 = i & 31;                   // row, 4-float chunk
-      const int b = rr / G, gq = rr - b * G;
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(
-          a.qrot + ((int64_t)b * a.Hq + (int64_t)h0 * G + gq) * kTile) + c4);
-      const int rl = c4 >> 2, cc = (c4 & 3) * 4;
-      *reinterpret_cast<float4 *>(&s_q[(rr * 8 + rl) * kQkLaneStride + cc]) = v;
+__global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
+  __shared__ uint64_t s_start[kQkTeams][kDecThreads + 1];
+  __shared__ __align__(16) uint32_t s_warp[kQkTeams][2][kDecThreads / 32];
+  __shared__ __align__(8) uint64_t s_bar[kQkTeams];
+  __shared__ uint32_t s_taddr;
+  extern __shared__ __align__(128) unsigned char s_ops[];   // A | B of team 0 | ... | B of team 3
+  const int team = threadIdx.x / kDecThreads, tid = TeamBar::tid();
+  const int tl = tid >> 3, r = tid & 7, warp = tid >> 5;
+  const int chunk = blockIdx.x, h = blockIdx.y, row0 = blockIdx.z * kQkRows;
+  const int64_t T = a.n_tokens;
+  const int G = a.Hq / a.n_kv, rows = a.B * G;
+  const int64_t tile_lo = (int64_t)h * T, tile_hi = tile_lo + T;
+  const int64_t g_first = tile_lo / kGroupTiles, g_end = (tile_hi - 1) / kGroupTiles + 1;
+  const int64_t gb = g_first + (int64_t)chunk * kQkGroupsPerChunk;
+  const int64_t ge = min(gb + (int64_t)kQkGroupsPerChunk, g_end);
+  if (gb >= ge) return;                          // uniform: nothing of head h here
+  if (threadIdx.x < 32) tmem_alloc(&s_taddr, kQkTmemCols);
+  if (tid == 32) mbar_init(&s_bar[team], 1);
+  // A: the block's rotated query rows split into tf32 parts (rows past the
+  // end are zeros)
+  for (int u = threadIdx.x; u < kQkRows * 32; u += kQkThreads) {
+    const int q = u >> 5, db = u & 31, row = row0 + q;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < rows) {
+      const int b = row / G, gq = row - b * G;
+      v = __ldg(reinterpret_cast<const float4 *>(
+                    a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile) + db);
     }
+    float4 hi, lo;
+    split_tf32(v.x, hi.x, lo.x);
+    split_tf32(v.y, hi.y, lo.y);
+    split_tf32(v.z, hi.z, lo.z);
+    split_tf32(v.w, hi.w, lo.w);
+    unsigned char *dst = s_ops + (q >> 3) * kQkAGStride + qk_kcore(db) * kQkAKStride + (q & 7) * 16;
+    *reinterpret_cast<float4 *>(dst) = hi;
+    *reinterpret_cast<float4 *>(dst + 32 * kQkAKStride) = lo;
   }
-  float e[16];
-  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);   // barriers inside
-  if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-  const int64_t tile = g * kGroupTiles + tl;
-  const bool valid = tile < a.dec.n_tiles;
-  const int h = valid ? (int)div_by(tile, a.n_tokens, a.tok_shift) : h0;
-  const int64_t tok = valid ? tile - (int64_t)h * a.n_tokens : 0;
-  const bool from_smem = staged && h == h0;
-  // Common case: every query row staged and all 32 tiles tokens of head h0.
-  // The group's e goes to shared memory and the 32 x rows block of scores is
-  // a small product there: thread (tt, rq) computes tokens tt and tt + 16
-  // for rows 4rq .. 4rq+3, each score one chain over d.
-  const int64_t last = min(g * kGroupTiles + kGroupTiles, a.dec.n_tiles) - 1;
-  if (staged && (int)div_by(last, a.n_tokens, a.tok_shift) == h0) {   // uniform
-    __shared__ __align__(16) float s_et[kGroupTiles * kQkEStride];
-    float4 *de = reinterpret_cast<float4 *>(&s_et[tl * kQkEStride + 16 * r]);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) de[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
-    __syncthreads();
-    const int tt = tid & 15, rq = tid >> 4;
-    if (4 * rq < rows) {
-      float acc[4][2];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.0f;
-      const int rlim = min(4, rows - 4 * rq);
-#pragma unroll 2
-      for (int k = 0; k < kTile; k += 4) {
-        const float4 e0 = *reinterpret_cast<const float4 *>(&s_et[tt * kQkEStride + k]);
-        const float4 e1 = *reinterpret_cast<const float4 *>(&s_et[(tt + 16) * kQkEStride + k]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = 4 * rq + (i < rlim ? i : 0);
-          const float4 qv = *reinterpret_cast<const float4 *>(
-              &s_q[(rr * 8 + (k >> 4)) * kQkLaneStride + (k & 15)]);
-          acc[i][0] = __fmaf_rn(qv.x, e0.x, acc[i][0]);
-          acc[i][0] = __fmaf_rn(qv.y, e0.y, acc[i][0]);
-          acc[i][0] = __fmaf_rn(qv.z, e0.z, acc[i][0]);
-          acc[i][0] = __fmaf_rn(qv.w, e0.w, acc[i][0]);
-          acc[i][1] = __fmaf_rn(qv.x, e1.x, acc[i][1]);
-          acc[i][1] = __fmaf_rn(qv.y, e1.y, acc[i][1]);
-          acc[i][1] = __fmaf_rn(qv.z, e1.z, acc[i][1]);
-          acc[i][1] = __fmaf_rn(qv.w, e1.w, acc[i][1]);
-        }
-      }
-      const int64_t t0 = g * kGroupTiles - (int64_t)h0 * a.n_tokens;   // token of tile 0
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i >= rlim) break;
-        const int rr = 4 * rq + i, b = rr / G, gq = rr - b * G;
-        float *dst = a.scores + ((int64_t)b * a.Hq + (int64_t)h0 * G + gq) * a.n_tokens + t0;
-        if (g * kGroupTiles + tt < a.dec.n_tiles) dst[tt] = acc[i][0];
-        if (g * kGroupTiles + tt + 16 < a.dec.n_tiles) dst[tt + 16] = acc[i][1];
-      }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t dcol = s_taddr + (uint32_t)(32 * team);
+  const uint32_t a_op = smem_addr(s_ops), b_op = a_op + kQkABytes + team * kQkBBytes;
+  unsigned char *const bdst =
+      s_ops + kQkABytes + team * kQkBBytes + (tl >> 3) * kQkBGStride + (tl & 7) * 16;
+  uint64_t *const bar = &s_bar[team];
+  // epilogue geometry: team warps 0, 1, 4, 5 read lanes (query rows)
+  // 32 (w % 4) + lane, tokens 16 (w / 4) .. +15 of the group
+  const bool reader = (warp & 2) == 0;
+  const int q_row = 32 * (warp & 1) + (tid & 31), row = row0 + q_row, tcol = 16 * (warp >> 2);
+  float *srow = nullptr;
+  if (reader && row < rows) {
+    const int b = row / G, gq = row - b * G;
+    srow = a.scores + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * T - tile_lo;
+  }
+  bool ok_wait = true;                           // team-uniform
+  int committed = 0;
+  // this team's groups gb + team, gb + team + 4, ...; the step past the last
+  // one only drains
+  for (int64_t g = gb + team; g < ge + kQkTeams; g += kQkTeams) {
+    const bool has = g < ge;
+    float e[16];
+    if (has) {
+      const bool ok = decode_lane<LAT, K, TeamBar>(a.dec, g, e, s_start[team], s_warp[team]);
+      if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
     }
-    return;
-  }
-  for (int r0 = 0; r0 < rows; r0 += 8) {
-    float p[8];
+    if (committed > 0) {                         // the previous group: wait, then its scores
+      if (ok_wait) ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22);
+      ok_wait = TeamBar::sync_and(ok_wait) != 0;
+      if (ok_wait && reader) {
+        tc_fence_after();
+        float v[16];
+        tmem_ld16(dcol + ((uint32_t)(32 * (warp & 1)) << 16) + (uint32_t)tcol, v);
+        const int64_t t0 = (g - kQkTeams) * kGroupTiles + tcol;
+        if (srow != nullptr) {
+          if (t0 >= tile_lo && t0 + 16 <= tile_hi) {
+            float4 *dst = reinterpret_cast<float4 *>(srow + t0);
+            if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = r0 + i;
-      float acc = 0.0f;
-      if (rr < rows) {
-        if (from_smem) {
-          const float4 *qr = reinterpret_cast<const float4 *>(&s_q[(rr * 8 + r) * kQkLaneStride]);
+              for (int c = 0; c < 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 qv = qr[c];
-            acc = __fmaf_rn(qv.x, e[4 * c], acc);
-            acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
-            acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
-            acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
-          }
-        } else {
-          const int b = rr / G, gq = rr - b * G;
-          const float4 *qr = reinterpret_cast<const float4 *>(
-              a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile + 16 * r);
+              for (int j = 0; j < 16; ++j) srow[t0 + j] = v[j];
+            }
+          } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 qv = __ldg(qr + c);
-            acc = __fmaf_rn(qv.x, e[4 * c], acc);
-            acc = __fmaf_rn(qv.y, e[4 * c + 1], acc);
-            acc = __fmaf_rn(qv.z, e[4 * c + 2], acc);
-            acc = __fmaf_rn(qv.w, e[4 * c + 3], acc);
+            for (int j = 0; j < 16; ++j)
+              if (t0 + j >= tile_lo && t0 + j < tile_hi) srow[t0 + j] = v[j];
           }
         }
       }
-      p[i] = acc;
     }
-    // reduce-scatter over the 8 lanes: after the step with mask m a lane keeps
-    // the half of its slots whose bit m matches its own lane bit
+    if (!has || !ok_wait) continue;
+    // B: this lane's 16 values split into tf32 parts, four 16-byte blocks each
 #pragma unroll
-    for (int m = 4; m >= 1; m >>= 1) {
+    for (int c = 0; c < 4; ++c) {
+      float4 hi, lo;
+      split_tf32(e[4 * c], hi.x, lo.x);
+      split_tf32(e[4 * c + 1], hi.y, lo.y);
+      split_tf32(e[4 * c + 2], hi.z, lo.z);
+      split_tf32(e[4 * c + 3], hi.w, lo.w);
+      unsigned char *dst = bdst + (8 * c + r) * kQkBKStride;
+      *reinterpret_cast<float4 *>(dst) = hi;
+      *reinterpret_cast<float4 *>(dst + 32 * kQkBKStride) = lo;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    TeamBar::sync();
+    ++committed;
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < m; ++i) {
-        const bool upper = (r & m) != 0;
-        const float send = upper ? p[i] : p[i + m];
-        const float keep = upper ? p[i + m] : p[i];
-        const float got = __shfl_xor_sync(0xffffffffu, send, m);
-        p[i] = __fadd_rn(keep, got);
+      for (int part = 0; part < 3; ++part) {
+        const int ka = part == 1 ? 32 : 0, kb = part == 2 ? 32 : 0;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          umma_tf32(dcol, umma_desc(a_op + (ka + 2 * ks) * kQkAKStride, kQkAKStride, kQkAGStride),
+                    umma_desc(b_op + (kb + 2 * ks) * kQkBKStride, kQkBKStride, kQkBGStride), kQkIdesc,
+                    (part > 0 || ks > 0) ? 1u : 0u);
       }
+      umma_commit(bar);
     }
-    const int rr = r0 + r;                       // slot kept by lane r is row r0 + r
-    if (valid && rr < rows) {
-      const int b = rr / G, gq = rr - b * G;
-      a.scores[((int64_t)b * a.Hq + (int64_t)h * G + gq) * a.n_tokens + tok] = p[0];
-    }
+  }
+  if (!ok_wait) {
+    if (tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_TIMEOUT);
+    if (committed > 0) mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(s_taddr, kQkTmemCols);
   }
 }
 
@@ -545,14 +574,26 @@ __global__ void gemm_reduce_kernel(GemmArgs a) {
   if (lane == 0) a.y[b * a.rows + o] = s;
 }
 
+template <int LAT, int K>
+static void launch_qk_one(const QkArgs &a, dim3 grid, dim3 block, cudaStream_t st) {
+  cudaFuncSetAttribute(scores_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
+  scores_kernel<LAT, K><<<grid, block, kQkSmemBytes, st>>>(a);
+}
+
 template <int LAT>
 static void launch_qk_lat(const QkArgs &a, cudaStream_t st) {
-  dim3 grid((unsigned)a.dec.n_groups), block(kDecThreads);
+  // a head's tokens touch at most T / 32 + 1 groups (one more when it
+  // starts inside a group)
+  const int64_t groups = a.n_tokens / kGroupTiles + 2;
+  const int rows = a.B * (a.Hq / a.n_kv);
+  dim3 grid((unsigned)((groups + kQkGroupsPerChunk - 1) / kQkGroupsPerChunk), (unsigned)a.n_kv,
+            (unsigned)((rows + kQkRows - 1) / kQkRows)),
+      block(kQkThreads);
   switch (a.dec.rice_k) {
-    case 1: scores_kernel<LAT, 1><<<grid, block, 0, st>>>(a); break;
-    case 2: scores_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
-    case 3: scores_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
-    default: scores_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+    case 1: launch_qk_one<LAT, 1>(a, grid, block, st); break;
+    case 2: launch_qk_one<LAT, 2>(a, grid, block, st); break;
+    case 3: launch_qk_one<LAT, 3>(a, grid, block, st); break;
+    default: launch_qk_one<LAT, -1>(a, grid, block, st); break;
   }
 }
 

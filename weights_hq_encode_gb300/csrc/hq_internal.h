@@ -69,7 +69,6 @@ struct QkArgs {
   DecodeArgs dec;           // K stream
   int n_kv;
   int64_t n_tokens;
-  int tok_shift;            // log2(n_tokens) when a power of two, else -1
   const uint16_t *q;        // [B][Hq][128] bf16
   int B, Hq;
   float *qrot;              // [B][Hq][128] fp32 workspace: s_dec * H * D_h * q
