@@ -289,7 +289,8 @@ bool attn_geometry(int n_kv, int64_t n_tokens, int B, int Hq, AttnGeometry *g) {
   if (n_kv <= 0 || n_tokens <= 0 || B <= 0 || Hq <= 0 || Hq % n_kv != 0) return false;
   const int64_t rows = (int64_t)B * (Hq / n_kv);
   const int64_t groups = (n_tokens + HQ_GROUP_TILES - 1) / HQ_GROUP_TILES + 1;   // a head's groups
-  g->chunks = (groups + hq::kPvGroupsPerChunk - 1) / hq::kPvGroupsPerChunk;
+  // sized for the smallest chunk the launch may pick
+  g->chunks = (groups + hq::kPvMinGroupsPerChunk - 1) / hq::kPvMinGroupsPerChunk;
   g->rowtiles = (rows + hq::kPvRows - 1) / hq::kPvRows;
   if (g->chunks > 0x7FFFFFFF || g->rowtiles > 65535 || n_kv > 65535) return false;
   // every region starts on a 256-byte boundary (the kernels use 16-byte vectors)
@@ -345,7 +346,7 @@ int hq_decode_attention(const hq_params *pk, const uint32_t *d_k_stream, uint64_
   a.scale = scale;
   a.partials = reinterpret_cast<float *>(ws + g.qrot + g.scores);
   a.stats = reinterpret_cast<float2 *>(ws + g.qrot + g.scores + g.partials);
-  a.chunks = (int)g.chunks;
+  a.chunks = (int)g.chunks;                     // the launch lowers it to its chunk size
   a.rowtiles = (int)g.rowtiles;
   a.out = d_out;
   return hq::launch_decode_attention(a, pk->lattice, pv->lattice, d_probs != nullptr, st) == 0

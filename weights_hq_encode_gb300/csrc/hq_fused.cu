@@ -8,6 +8,8 @@
 // attention output rows are transformed back once per row.
 #include <cuda_runtime.h>
 
+#include <cmath>
+
 #include "hq_decode_lane.cuh"
 #include "hq_umma.cuh"
 
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
   // A: the block's rotated query rows split into tf32 parts (rows past the
   // end are zeros)
   for (int u = threadIdx.x; u < kQkRows * 32; u += kQkThreads) {
-    const int q = u >> 5, db = u & 31, row = row0 + q;
+    const int q = u & (kQkRows - 1), db = u >> 6, row = row0 + q;   // 8 rows per 128-byte phase
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (row < rows) {
       const int b = row / G, gq = row - b * G;
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
     const int b = row / G, gq = row - b * G;
     srow = a.scores + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * T - tile_lo;
   }
-  bool ok_wait = true;                           // team-uniform
+  bool ok_wait = true;                           // team-uniform after each barrier
   int committed = 0;
   // this team's groups gb + team, gb + team + 4, ...; the step past the last
   // one only drains
@@ -134,9 +136,9 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
       const bool ok = decode_lane<LAT, K, TeamBar>(a.dec, g, e, s_start[team], s_warp[team]);
       if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
     }
-    if (committed > 0) {                         // the previous group: wait, then its scores
-      if (ok_wait) ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22);
-      ok_wait = TeamBar::sync_and(ok_wait) != 0;
+    if (committed > 0 && ok_wait) {              // the previous group: wait, then its scores
+      // warp-uniform for the tensor-memory loads; team-uniform at the next barrier
+      ok_wait = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22));
       if (ok_wait && reader) {
         tc_fence_after();
         float v[16];
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
         }
       }
     }
-    if (!has || !ok_wait) continue;
+    if (!has) continue;
     // B: this lane's 16 values split into tf32 parts, four 16-byte blocks each
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -175,7 +177,8 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
     }
     fence_async_smem();
     tc_fence_before();
-    TeamBar::sync();
+    ok_wait = TeamBar::sync_and(ok_wait) != 0;
+    if (!ok_wait) continue;
     ++committed;
     if (tid == 0) {
       tc_fence_after();
@@ -315,8 +318,8 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   const int Hq = a.qk.Hq, G = Hq / a.qk.n_kv, rows = a.qk.B * G, row0 = rt * kPvRows;
   const int64_t tile_lo = (int64_t)h * T, tile_hi = tile_lo + T;
   const int64_t g_first = tile_lo / kGroupTiles, g_end = (tile_hi - 1) / kGroupTiles + 1;
-  const int64_t gb = g_first + (int64_t)chunk * kPvGroupsPerChunk;
-  const int64_t ge = min(gb + (int64_t)kPvGroupsPerChunk, g_end);
+  const int64_t gb = g_first + (int64_t)chunk * a.pv_chunk;
+  const int64_t ge = min(gb + (int64_t)a.pv_chunk, g_end);
   if (warp == 0) tmem_alloc(&s_taddr, kPvTmemCols);
   if (tid == 32) mbar_init(&s_bar, 1);
   // this chunk's softmax statistics per row: m = max z over its tokens and
@@ -603,14 +606,59 @@ static void launch_pv_one(const AttnArgs &a, dim3 grid, dim3 block, cudaStream_t
   pv_kernel<LAT, K><<<grid, block, kPvSmemBytes, st>>>(a);
 }
 
+// Blocks of one pv_kernel instance resident per SM, times the SM count.
+template <int LAT, int K>
+static int pv_capacity() {
+  static int cap = 0;                            // per instance; the same on every call
+  if (cap == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kDecThreads,
+                                                  kPvSmemBytes);
+    cap = sms * per_sm > 0 ? sms * per_sm : 1;
+  }
+  return cap;
+}
+
+// The chunk size (groups per block) whose grid fills the most of its last
+// wave of `cap` resident blocks; ties go to the larger chunk (fewer
+// partial sums to combine).  a.chunks arrives as the workspace's chunk count
+// (that of the smallest chunk size, with the same bound on a head's groups)
+// and no choice may exceed it.
+static void pick_pv_chunk(AttnArgs &a, int cap) {
+  const int64_t groups = (a.qk.n_tokens + kGroupTiles - 1) / kGroupTiles + 1;   // a head's, at most
+  const int room = a.chunks;
+  double best = -1.0;
+  for (int cs = kPvMaxGroupsPerChunk; cs >= kPvMinGroupsPerChunk; --cs) {
+    const int64_t chunks = (groups + cs - 1) / cs;
+    if (chunks > room) continue;
+    const double blocks = (double)chunks * a.qk.n_kv * a.rowtiles;
+    const double waves = blocks / cap, fill = waves / std::ceil(waves);
+    if (fill > best + 1e-9) {
+      best = fill;
+      a.pv_chunk = cs;
+      a.chunks = (int)chunks;
+    }
+  }
+}
+
+template <int LAT, int K>
+static void launch_pv_k(AttnArgs a, cudaStream_t st) {
+  pick_pv_chunk(a, pv_capacity<LAT, K>());
+  dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kDecThreads);
+  launch_pv_one<LAT, K>(a, grid, block, st);
+  pv_finish_kernel<<<(unsigned)(a.qk.B * a.qk.Hq), kTile, 0, st>>>(a);
+}
+
 template <int LAT>
 static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
-  dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kDecThreads);
   switch (a.v.rice_k) {
-    case 1: launch_pv_one<LAT, 1>(a, grid, block, st); break;
-    case 2: launch_pv_one<LAT, 2>(a, grid, block, st); break;
-    case 3: launch_pv_one<LAT, 3>(a, grid, block, st); break;
-    default: launch_pv_one<LAT, -1>(a, grid, block, st); break;
+    case 1: launch_pv_k<LAT, 1>(a, st); break;
+    case 2: launch_pv_k<LAT, 2>(a, st); break;
+    case 3: launch_pv_k<LAT, 3>(a, st); break;
+    default: launch_pv_k<LAT, -1>(a, st); break;
   }
 }
 
@@ -648,8 +696,6 @@ int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, boo
     case 2: launch_pv_lat<2>(a, st); break;
     default: launch_pv_lat<1>(a, st); break;
   }
-  if (cudaGetLastError() != cudaSuccess) return 1;
-  pv_finish_kernel<<<rows, kTile, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return 1;
   if (want_probs) {                              // the scores become probabilities in place
     softmax_kernel<<<rows, kSoftmaxThreads, 0, st>>>(a);

@@ -79,7 +79,8 @@ struct QkArgs {
 // stream; each chunk of tokens keeps its own softmax maximum and sum (stats)
 // beside its partial sums of exp(z - max) e (partials).
 constexpr int kPvRows = 64;           // query rows per contraction tile
-constexpr int kPvGroupsPerChunk = 8;  // groups of 32 tokens per block
+constexpr int kPvMaxGroupsPerChunk = 8;  // groups of 32 tokens per block: the launch picks
+constexpr int kPvMinGroupsPerChunk = 4;  // a chunk size in this range that fills whole waves
 struct AttnArgs {
   QkArgs qk;                // K stream, queries, rotated queries, scores -> probabilities
   DecodeArgs v;             // V stream
@@ -87,6 +88,7 @@ struct AttnArgs {
   float *partials;          // [n_kv][chunks][rowtiles][kPvRows][128]
   float2 *stats;            // [n_kv][chunks][rowtiles][kPvRows]: (max z, sum exp(z - max))
   int chunks, rowtiles;
+  int pv_chunk;             // groups per chunk (set by the launch)
   float *out;               // [B][Hq][128] fp32
 };
 
