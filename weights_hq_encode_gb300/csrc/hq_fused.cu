@@ -322,29 +322,33 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   const int64_t ge = min(gb + (int64_t)a.pv_chunk, g_end);
   if (warp == 0) tmem_alloc(&s_taddr, kPvTmemCols);
   if (tid == 32) mbar_init(&s_bar, 1);
-  // this chunk's softmax statistics per row: m = max z over its tokens and
-  // l = sum exp(z - m) (four threads per row, then a fixed shuffle tree)
+  // this chunk's softmax maximum per row, m = max z over its tokens: warp w
+  // takes rows w, w + 8, ..., its lanes consecutive tokens (a chunk holds at
+  // most 256 of a head's tokens, 8 per lane); l = sum exp(z - m) is summed
+  // from the weights of the main loop below
   {
-    const int rr = tid >> 2, q = tid & 3, row = row0 + rr;
+    const int lane = tid & 31;
     const int64_t c_lo = max(gb * kGroupTiles, tile_lo), c_hi = min(ge * kGroupTiles, tile_hi);
-    const float *srow = nullptr;
-    if (row < rows) {
-      const int b = row / G, gq = row - b * G;
-      srow = a.qk.scores + ((int64_t)b * Hq + (int64_t)h * G + gq) * T - tile_lo;
-    }
-    float m = -INFINITY, l = 0.0f;
-    if (srow != nullptr)
-      for (int64_t t = c_lo + q; t < c_hi; t += 4) m = fmaxf(m, __fmul_rn(srow[t], a.scale));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    if (srow != nullptr && m != -INFINITY)
-      for (int64_t t = c_lo + q; t < c_hi; t += 4)
-        l = __fadd_rn(l, expf(__fsub_rn(__fmul_rn(srow[t], a.scale), m)));
-    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 1));
-    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 2));
-    if (q == 0) {
-      s_m[rr] = m;
-      a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(m, l);
+    for (int rr = warp; rr < kPvRows; rr += kDecThreads / 32) {
+      const int row = row0 + rr;
+      float m = -INFINITY;
+      if (row < rows) {
+        const int b = row / G, gq = row - b * G;
+        const float *srow = a.qk.scores + ((int64_t)b * Hq + (int64_t)h * G + gq) * T - tile_lo;
+        for (int64_t t0 = c_lo; t0 < c_hi; t0 += 256) {
+          float z[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int64_t t = t0 + lane + 32 * j;
+            z[j] = t < c_hi ? __fmul_rn(srow[t], a.scale) : -INFINITY;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = fmaxf(m, z[j]);
+        }
+      }
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+      if (lane == 0) s_m[rr] = m;
     }
   }
   tc_fence_before();
@@ -362,7 +366,9 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   int committed = 0;                             // groups whose MMAs were issued
   // the scores of a group are loaded one group ahead, so that their latency
   // hides behind the decoding of the current one
-  float pn[8];
+  float pn[8], lsum[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) lsum[k] = 0.0f;
   if (gb < ge) pv_load_z(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
   for (int64_t g = gb; g < ge; ++g) {            // block-uniform bounds
     const int i = (int)(g - gb);
@@ -383,6 +389,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
     for (int k = 0; k < 8; ++k) {                // p = exp(z - m), 0 for z = -inf
       const float mm = s_m[(tid >> 5) + 8 * k];
       const float p = pn[k] == -INFINITY ? 0.0f : expf(__fsub_rn(pn[k], mm));
+      lsum[k] = __fadd_rn(lsum[k], p);           // this lane's token column, in group order
       float hi, lo;
       split_tf32(p, hi, lo);
       bp[k * kPvBGStride / 4] = hi;              // rows (tid >> 5) + 8 k
@@ -406,6 +413,16 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
                   umma_desc(b_op + ks * 2 * kPvBKStride, kPvBKStride, kPvBGStride), kPvIdesc, 1u);
       umma_commit(&s_bar);
     }
+  }
+  // l per row: the lanes' column sums combined by a fixed butterfly
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float l = lsum[k];
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, d));
+    const int rr = warp + 8 * k;
+    if ((tid & 31) == 0)
+      a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(s_m[rr], l);
   }
   if (committed > 0) {
     if (ok_wait) ok_wait = mbar_wait(&s_bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
