@@ -57,7 +57,7 @@ enum {
   HQ_ERR_CAPACITY = 4,  /* stream larger than cap_words: words past the cap
                            were not written; offsets are still complete */
   HQ_ERR_CORRUPT = 8,   /* a group failed a format check: its tiles decode to 0 */
-  HQ_ERR_TIMEOUT = 16,  /* a cross-block wait ran out (encode look-back) */
+  HQ_ERR_TIMEOUT = 16,  /* a bounded wait ran out (encode look-back, tensor-core completion) */
   HQ_ERR_RANGE = 32     /* non-finite input or |alpha * RHT(x)| > 2^20: the tile
                            was coded as an all-zero tile */
 };
@@ -202,9 +202,15 @@ size_t hq_decode_qk_workspace_bytes(int B, int Hq);
 /* Attention scores from compressed K (closing section, fused decode + MMA):
  *   scores[b][hq][t] = sum_d q[b][hq][d] * Khat[h][t][d],  h = hq / (Hq / n_kv_heads),
  * with Khat the decode of K tile h * n_tokens + t; K itself is never written.
+ * The products run on the tensor cores: both operands are split into two
+ * tf32 parts (|x - hi - lo| <= 2^-22 |x|) and the partial products summed in
+ * an fp32 accumulator, an fp32-level result.
  *   d_q        [B][Hq][128] bf16, device.
  *   d_scores   [B][Hq][n_tokens] fp32, device.
  *   d_ws       >= hq_decode_qk_workspace_bytes(B, Hq) bytes, device.
+ *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group, HQ_ERR_TIMEOUT
+ *              if a tensor-core completion wait ran out (its scores are then
+ *              not written).
  * Requires Hq % n_kv_heads == 0 and every head's tiles in one sign segment
  * (tiles_per_segment a multiple of n_tokens).  Returns HQ_OK, HQ_ERR_INVALID
  * or HQ_ERR_CUDA.  Asynchronous. */
@@ -216,7 +222,8 @@ int hq_decode_qk(const hq_params *p, const uint32_t *d_k_stream, uint64_t stream
 /* Bytes of device workspace hq_decode_attention needs: the rotated queries
  * (B * Hq * 128 fp32), the scores (B * Hq * n_tokens fp32), and per chunk of
  * tokens the partial sums of the value contraction and the softmax maximum
- * and sum of each query row.  0 for invalid sizes. */
+ * and sum of each query row (sized for the smallest chunk, 4 groups of 32
+ * tokens; the launch may use larger ones).  0 for invalid sizes. */
 size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int B, int Hq);
 
 /* One decode step of attention read straight from compressed K and V
@@ -229,12 +236,15 @@ size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int
  * value side is accumulated in the lattice domain and transformed once per
  * query row; the softmax is formed per chunk of tokens (maximum and sum) and
  * the chunks are combined in a fixed order, so the result is deterministic.
+ * Both contractions run on the tensor cores with split tf32 operands and
+ * fp32 accumulators (as for hq_decode_qk).
  *   d_q        [B][Hq][128] bf16, device.
  *   d_out      [B][Hq][128] fp32, device, 16-byte aligned.
  *   d_probs    optional [B][Hq][n_tokens] fp32 output of p (NULL: p is not
  *              formed; the scores stay in the workspace).
  *   d_ws       >= hq_decode_attention_workspace_bytes() bytes, 16-byte aligned.
- *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group of either stream.
+ *   d_status   OR-ed with HQ_ERR_CORRUPT for a damaged group of either stream,
+ *              HQ_ERR_TIMEOUT if a tensor-core completion wait ran out.
  * Requires Hq % n_kv_heads == 0 and every head's tiles in one sign segment of
  * each stream (tiles_per_segment of pk and pv multiples of n_tokens).
  * Returns HQ_OK, HQ_ERR_INVALID or HQ_ERR_CUDA.  Asynchronous. */
