@@ -623,20 +623,23 @@ static void launch_pv_one(const AttnArgs &a, dim3 grid, dim3 block, cudaStream_t
   pv_kernel<LAT, K><<<grid, block, kPvSmemBytes, st>>>(a);
 }
 
-// Blocks of one pv_kernel instance resident per SM, times the SM count.
+// Blocks of one pv_kernel instance resident per SM, times the SM count of
+// the current device (kept per instance and device after the first query).
 template <int LAT, int K>
 static int pv_capacity() {
-  static int cap = 0;                            // per instance; the same on every call
-  if (cap == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kDecThreads,
-                                                  kPvSmemBytes);
-    cap = sms * per_sm > 0 ? sms * per_sm : 1;
-  }
-  return cap;
+  constexpr int kDevices = 64;
+  static int cap[kDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kDevices && cap[dev] > 0) return cap[dev];
+  int sms = 0, per_sm = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kDecThreads,
+                                                kPvSmemBytes);
+  const int c = sms * per_sm > 0 ? sms * per_sm : 1;
+  if (dev >= 0 && dev < kDevices) cap[dev] = c;
+  return c;
 }
 
 // The chunk size (groups per block) whose grid fills the most of its last
