@@ -13,8 +13,10 @@
 
 namespace hq {
 
-template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 8)
+// ROT: the dense-rotation variant (an instance of its own, 2 blocks per SM
+// with the registers of its 4 x 8 product tile; runtime k only).
+template <int LAT, int K, bool ROT>
+__global__ void __launch_bounds__(kDecThreads, ROT ? 2 : 8)
 decode_kernel(DecodeArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
@@ -27,6 +29,11 @@ decode_kernel(DecodeArgs a) {
     reinterpret_cast<float *>(s_scale)[tid] =
         __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
   }
+  constexpr int kRS = kTile + 4;                 // row stride of the rotation's operands
+  extern __shared__ __align__(16) float s_dyn[];  // ROT: y [32][kRS], then R [128][kRS]
+  if constexpr (ROT)                             // R arrives while the group is decoded
+    rot_load_async(s_dyn + kGroupTiles * kRS, a.rot + seg0 * (int64_t)(kTile * kTile), kRS, tid,
+                   kDecThreads);
   float e[16];
   const bool ok = decode_lane<LAT, K>(a, g, e, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
@@ -34,7 +41,7 @@ decode_kernel(DecodeArgs a) {
   // the transform runs on every lane of the block (shuffles need full warps)
   fwht128_x8(e, r);
   const bool tvalid = t < a.n_tiles;
-  if (a.rot == nullptr && !tvalid) return;
+  if (!ROT && !tvalid) return;
   if (ok && tvalid) {
     // x = D fl(z s_dec) = fl(z (D s_dec)): the sign commutes with rounding
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
@@ -54,45 +61,51 @@ decode_kernel(DecodeArgs a) {
         e[i] = __fmul_rn(e[i], __uint_as_float(__float_as_uint(a.s_dec) ^ (((mw >> i) & 1u) << 31)));
     }
   }
-  if (a.rot != nullptr) {                        // uniform: x_hat = R^T y, chains over i
-    // [32 tiles x 128] x [128 x 128] in shared memory: y transposed [128][36]
-    // (later reused for the result [32][132]) and R row-major [128][132]
-    constexpr int kYS = kGroupTiles + 4, kRS = kTile + 4;
-    extern __shared__ __align__(16) float s_dyn[];
-    float *s_yt = s_dyn;
-    float *s_r = s_dyn + kTile * kYS;
+  if constexpr (ROT) {                           // x_hat = R^T y, chains over i
+    // [32 tiles x 128] x [128 x 128] in shared memory: y row-major [32][132]
+    // (later reused for the result) and R row-major [128][132]
+    float *s_y = s_dyn;
+    const float *s_r = s_dyn + kGroupTiles * kRS;
+    float4 *dy = reinterpret_cast<float4 *>(s_y + tl * kRS + 16 * r);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) s_yt[(16 * r + c) * kYS + tl] = e[c];
-    const float4 *R4 = reinterpret_cast<const float4 *>(a.rot + seg0 * (int64_t)(kTile * kTile));
-    for (int idx = tid; idx < kTile * kTile / 4; idx += kDecThreads)
-      *reinterpret_cast<float4 *>(s_r + (idx >> 5) * kRS + 4 * (idx & 31)) = __ldg(R4 + idx);
+    for (int c = 0; c < 4; ++c) dy[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    rot_wait();
     __syncthreads();
-    const int tb = tid >> 5, ob = tid & 31;     // tiles 4tb.., outputs 4ob..
+    // thread (tg, oh, l16): tiles 4 tg .. 4 tg + 3 x outputs 64 oh + 4 l16 .. +3,
+    // each one fma chain over i = 0..127 from +0
+    const int tg = (tid >> 4) & 7, ob = 64 * (tid >> 7) + 4 * (tid & 15);
     float acc[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-#pragma unroll 4
-    for (int i = 0; i < kTile; ++i) {
-      const float4 yv = *reinterpret_cast<const float4 *>(s_yt + i * kYS + 4 * tb);
-      const float4 rv = *reinterpret_cast<const float4 *>(s_r + i * kRS + 4 * ob);
-      const float ys[4] = {yv.x, yv.y, yv.z, yv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll 2
+    for (int i = 0; i < kTile; i += 4) {
+      float4 yv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
+        yv[u] = *reinterpret_cast<const float4 *>(s_y + (4 * tg + u) * kRS + i);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rs[c], ys[u], acc[u][c]);
+      for (int ii = 0; ii < 4; ++ii) {
+        const float4 rr = *reinterpret_cast<const float4 *>(s_r + (i + ii) * kRS + ob);
+        const float rs[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float yu = ii == 0 ? yv[u].x : ii == 1 ? yv[u].y : ii == 2 ? yv[u].z : yv[u].w;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rs[c], yu, acc[u][c]);
+        }
+      }
     }
-    __syncthreads();
-    float *s_o = s_dyn;                          // [32][132]
+    __syncthreads();                             // the y area becomes the result area
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      *reinterpret_cast<float4 *>(s_o + (4 * tb + u) * kRS + 4 * ob) =
+      *reinterpret_cast<float4 *>(s_y + (4 * tg + u) * kRS + ob) =
           make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
     __syncthreads();
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 q = *reinterpret_cast<const float4 *>(s_o + tl * kRS + 16 * r + 4 * c);
+      const float4 q = *reinterpret_cast<const float4 *>(s_y + tl * kRS + 16 * r + 4 * c);
       e[4 * c] = q.x;
       e[4 * c + 1] = q.y;
       e[4 * c + 2] = q.z;
@@ -118,19 +131,23 @@ decode_kernel(DecodeArgs a) {
   }
 }
 
-constexpr size_t kDecRotSmemBytes = (size_t)(kTile * (kGroupTiles + 4) + kTile * (kTile + 4)) * 4;
+constexpr size_t kDecRotSmemBytes = (size_t)((kGroupTiles + kTile) * (kTile + 4)) * 4;
 
-template <int LAT, int K>
+template <int LAT, int K, bool ROT = false>
 static void launch_dec_one(const DecodeArgs &a, cudaStream_t st) {
-  const size_t dyn = a.rot != nullptr ? kDecRotSmemBytes : 0;
+  const size_t dyn = ROT ? kDecRotSmemBytes : 0;
   if (dyn)
-    cudaFuncSetAttribute(decode_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(decode_kernel<LAT, K, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)dyn);
-  decode_kernel<LAT, K><<<dim3((unsigned)a.n_groups), dim3(kDecThreads), dyn, st>>>(a);
+  decode_kernel<LAT, K, ROT><<<dim3((unsigned)a.n_groups), dim3(kDecThreads), dyn, st>>>(a);
 }
 
 template <int LAT>
 static void launch_dec_lat(const DecodeArgs &a, cudaStream_t st) {
+  if (a.rot != nullptr) {                        // the rotation variant takes k at run time
+    launch_dec_one<LAT, -1, true>(a, st);
+    return;
+  }
   switch (a.rice_k) {
     case 0: launch_dec_one<LAT, 0>(a, st); break;
     case 1: launch_dec_one<LAT, 1>(a, st); break;

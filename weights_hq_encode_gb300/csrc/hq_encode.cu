@@ -26,11 +26,9 @@ constexpr int kKmaxTemplated = 8;                // Rice k specialised at compil
 // Dense rotation (optional), as a [32 tiles x 128] x [128 x 128] product in
 // shared memory: the tiles transposed [128][36] (later reused for the result
 // [32][132]) and the segment's R transposed [128][132].
-constexpr int kRotXStride = kGroupTiles + 4;
 constexpr int kRotStride = kTile + 4;
-constexpr int kRotXFloats = kTile * kRotXStride;                    // >= 32 * kRotStride
+constexpr int kRotXFloats = kGroupTiles * kRotStride;               // the group's tiles, then R x
 constexpr size_t kEncRotSmemBytes = (size_t)(kRotXFloats + kTile * kRotStride) * 4;
-static_assert(kRotXFloats >= kGroupTiles * kRotStride, "result fits the tile area");
 
 constexpr uint64_t kFlagAgg = 1ull << 62;        // look-back state: [63:62] flag
 constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] words
@@ -224,8 +222,10 @@ __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int k
   }
 }
 
-template <int LAT, int K>
-__global__ void __launch_bounds__(kEncThreads, 6)
+// ROT: the dense-rotation variant (an instance of its own, 2 blocks per SM
+// with the registers of its 4 x 8 product tile; runtime k only).
+template <int LAT, int K, bool ROT>
+__global__ void __launch_bounds__(kEncThreads, ROT ? 2 : 6)
 encode_kernel(EncodeArgs a) {
   __shared__ uint32_t s_stage[kStageWords];
   __shared__ uint32_t s_tile_u[kGroupTiles];
@@ -268,6 +268,11 @@ encode_kernel(EncodeArgs a) {
   }
   // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
   const int64_t seg0 = div_by(t0, a.tiles_per_segment, a.seg_shift);
+  if constexpr (ROT) {                           // R arrives while the tiles are staged
+    extern __shared__ __align__(16) float s_dyn_r[];   // the group is in one segment
+    rot_load_async(s_dyn_r + kRotXFloats, a.rot + seg0 * (int64_t)(kTile * kTile), kRotStride, tid,
+                   kEncThreads);
+  }
   if (tid < kTile / 2) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
     reinterpret_cast<uint32_t *>(s_signx)[tid] =
@@ -277,43 +282,54 @@ encode_kernel(EncodeArgs a) {
 
   // ---- optional dense rotation R x (before the sign mask)
   float x[16];
-  if (a.rot != nullptr) {                        // uniform over the grid
+  if constexpr (ROT) {
     extern __shared__ __align__(16) float s_dyn[];
-    float *s_xt = s_dyn;                         // [128][36]: coordinate j of tile t at [j][t]
-    float *s_rt = s_dyn + kRotXFloats;           // [128][132]: R[i][j] at [j][i]
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float *s_x = s_dyn;                          // [32][132]: coordinate j of tile t at [t][j]
+    const float *s_r = s_dyn + kRotXFloats;      // [128][132]: R[i][j] at [i][j]
+    {
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float4 *dst = reinterpret_cast<float4 *>(s_x + tl * kRotStride + 16 * r);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      s_xt[(16 * r + 2 * q) * kRotXStride + tl] = __uint_as_float(w[q] << 16);
-      s_xt[(16 * r + 2 * q + 1) * kRotXStride + tl] = __uint_as_float(w[q] & 0xFFFF0000u);
+      for (int c = 0; c < 4; ++c)
+        dst[c] = make_float4(__uint_as_float(w[2 * c] << 16), __uint_as_float(w[2 * c] & 0xFFFF0000u),
+                             __uint_as_float(w[2 * c + 1] << 16),
+                             __uint_as_float(w[2 * c + 1] & 0xFFFF0000u));
     }
-    const float *R = a.rot + seg0 * (int64_t)(kTile * kTile);   // the group is in one segment
-    for (int idx = tid; idx < kTile * kTile; idx += kEncThreads)
-      s_rt[(idx & (kTile - 1)) * kRotStride + (idx >> 7)] = __ldg(R + idx);
+    rot_wait();                                  // R was issued at the start of the block
     __syncthreads();
-    // thread (tb, ob): tiles 4tb..4tb+3 x outputs 4ob..4ob+3, one chain over j each
-    const int tb = tid >> 5, ob = tid & 31;
+    // thread (tg, oh, l16): tiles 4 tg .. 4 tg + 3 x outputs 64 oh + l16 + 16 c
+    // (c = 0..3), each output one fma chain over j = 0..127 from +0
+    const int tg = (tid >> 4) & 7, ob = 64 * (tid >> 7) + (tid & 15);
     float acc[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < kTile; ++j) {
-      const float4 xv = *reinterpret_cast<const float4 *>(s_xt + j * kRotXStride + 4 * tb);
-      const float4 rv = *reinterpret_cast<const float4 *>(s_rt + j * kRotStride + 4 * ob);
-      const float xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll 2
+    for (int j = 0; j < kTile; j += 4) {
+      float4 xv[4], rv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        xv[u] = *reinterpret_cast<const float4 *>(s_x + (4 * tg + u) * kRotStride + j);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        rv[c] = *reinterpret_cast<const float4 *>(s_r + (ob + 16 * c) * kRotStride + j);
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rs[c], xs[u], acc[u][c]);
+        for (int c = 0; c < 4; ++c) {
+          acc[u][c] = __fmaf_rn(rv[c].x, xv[u].x, acc[u][c]);
+          acc[u][c] = __fmaf_rn(rv[c].y, xv[u].y, acc[u][c]);
+          acc[u][c] = __fmaf_rn(rv[c].z, xv[u].z, acc[u][c]);
+          acc[u][c] = __fmaf_rn(rv[c].w, xv[u].w, acc[u][c]);
+        }
     }
     __syncthreads();                             // the tile area becomes the result area
     float *s_z = s_dyn;                          // [32][132]
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      *reinterpret_cast<float4 *>(s_z + (4 * tb + u) * kRotStride + 4 * ob) =
-          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s_z[(4 * tg + u) * kRotStride + ob + 16 * c] = acc[u][c];
     __syncthreads();
     float z[16];
 #pragma unroll
@@ -552,17 +568,21 @@ encode_kernel(EncodeArgs a) {
   }
 }
 
-template <int LAT, int K>
+template <int LAT, int K, bool ROT = false>
 static void launch_one(const EncodeArgs &a, cudaStream_t st) {
-  const size_t dyn = a.rot != nullptr ? kEncRotSmemBytes : 0;
+  const size_t dyn = ROT ? kEncRotSmemBytes : 0;
   if (dyn)
-    cudaFuncSetAttribute(encode_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(encode_kernel<LAT, K, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)dyn);
-  encode_kernel<LAT, K><<<dim3((unsigned)a.n_blocks), dim3(kEncThreads), dyn, st>>>(a);
+  encode_kernel<LAT, K, ROT><<<dim3((unsigned)a.n_blocks), dim3(kEncThreads), dyn, st>>>(a);
 }
 
 template <int LAT>
 static void launch_lat(const EncodeArgs &a, cudaStream_t st) {
+  if (a.rot != nullptr) {                        // the rotation variant takes k at run time
+    launch_one<LAT, -1, true>(a, st);
+    return;
+  }
   switch (a.rice_k) {
     case 0: launch_one<LAT, 0>(a, st); break;
     case 1: launch_one<LAT, 1>(a, st); break;
