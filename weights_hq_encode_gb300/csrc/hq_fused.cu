@@ -270,29 +270,42 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_kernel(AttnArgs a) {
 // tf32 split of the weights, B = [p_hi (64 rows); p_lo (64 rows)], each issued
 // twice (A = e_hi^T, then e_lo^T).  The four partial products of the split
 // operands give an fp32-level result: column n of D holds (e_hi + e_lo) p_hi
-// and column 64 + n holds (e_hi + e_lo) p_lo of row n, added once at the end.
-// The block's 256 threads decode group g + 1 while the MMAs of group g run.
-constexpr int kPvAKStride = 2304;                // bytes between K-cores of e^T (16 d-groups of 144)
-constexpr int kPvAGStride = 144;                 // bytes between 8-dimension groups (16 B of padding)
-constexpr int kPvBKStride = 144;                 // bytes between K-cores of B (16 B of padding)
-constexpr int kPvBGStride = 1152;                // bytes between 8-row groups of B
-constexpr int kPvOpBytes = 8 * kPvAKStride;      // 18432 per operand (e_hi^T, e_lo^T, B)
-constexpr int kPvSmemBytes = 3 * kPvOpBytes;
+// and column 64 + n holds (e_hi + e_lo) p_lo of row n.
+//
+// A block runs four independent teams of 256 threads (named barriers), each
+// decoding every fourth group of the chunk into operands and an accumulator
+// of its own, and decoding its next group while the MMAs of the previous one
+// run; at the end the teams' sums are added in team order (deterministic).
+// Operand layout: K-cores 2064 bytes apart (eight 8-row groups of 128 bytes
+// plus 16), so that consecutive K-cores fall on rotated banks without
+// padding; the rows of e^T are permuted (dimension 16 r + c of lane r goes to
+// row 8 (2 r + c / 8) + (c + r) % 8) so that the eight lanes of a tile store
+// to distinct banks.  The permutation is undone when the sums are read.
+constexpr int kPvTeams = 4;
+constexpr int kPvThreads = kPvTeams * kDecThreads;
+constexpr int kPvKStride = 2064;                 // bytes between K-cores
+constexpr int kPvGStride = 128;                  // bytes between 8-row groups
+constexpr int kPvOpBytes = 7 * kPvKStride + 16 * kPvGStride;   // 16496 per operand
+constexpr int kPvTeamBytes = 3 * kPvOpBytes;     // e_hi^T | e_lo^T | B
+constexpr int kPvSmemBytes = kPvTeams * kPvTeamBytes;
+static_assert(kPvTeams * kPvRows * kTile * 4 <= kPvSmemBytes, "team sums fit the operand area");
 constexpr uint32_t kPvIdesc = umma_idesc_tf32(128, 128);
-constexpr uint32_t kPvTmemCols = 128;
+constexpr uint32_t kPvTmemCols = 128 * kPvTeams;
 constexpr uint32_t kPvWaitLimit = 1u << 22;
+constexpr int kPvChunkMax = 32;                  // largest chunk the launch may pick (groups)
 
 // This thread's 8 scaled scores z = fl(scale s) of group g (element
-// i = tid + 256 k of the group's 64 rows x 32 tokens, row-major): consecutive
-// threads read consecutive tokens of one row; tokens outside head h or rows
-// past the end read as -inf (probability 0).
+// i = tid + 256 k of the group's 64 rows x 32 tokens, row-major, tid the
+// thread's index in its team): consecutive threads read consecutive tokens
+// of one row; tokens outside head h or rows past the end read as -inf
+// (probability 0).
 __device__ __forceinline__ void pv_load_z(const AttnArgs &a, int64_t g, int h, int row0, int G,
-                                          int rows, int64_t tile_lo, int64_t tile_hi,
+                                          int rows, int64_t tile_lo, int64_t tile_hi, int tid,
                                           float z[8]) {
   const int64_t T = a.qk.n_tokens;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const int i = threadIdx.x + k * kDecThreads;
+    const int i = tid + k * kDecThreads;
     const int rr = i >> 5, j = i & 31;
     const int64_t tile = g * kGroupTiles + j;
     const int row = row0 + rr;
@@ -305,14 +318,16 @@ __device__ __forceinline__ void pv_load_z(const AttnArgs &a, int64_t g, int h, i
   }
 }
 template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
-  __shared__ uint64_t s_start[kDecThreads + 1];
-  __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
+__global__ void __launch_bounds__(kPvThreads, 1) pv_kernel(AttnArgs a) {
+  __shared__ uint64_t s_start[kPvTeams][kDecThreads + 1];
+  __shared__ __align__(16) uint32_t s_warp[kPvTeams][2][kDecThreads / 32];
   __shared__ float s_m[kPvRows];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ float s_l[kPvTeams][kPvRows];
+  __shared__ __align__(8) uint64_t s_bar[kPvTeams];
   __shared__ uint32_t s_taddr;
-  extern __shared__ __align__(128) unsigned char s_ops[];   // e_hi^T | e_lo^T | B
-  const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7, warp = tid >> 5;
+  extern __shared__ __align__(128) unsigned char s_ops[];   // team 0 | ... | team 3
+  const int team = threadIdx.x / kDecThreads, tid = TeamBar::tid();
+  const int tl = tid >> 3, r = tid & 7, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, h = blockIdx.y, rt = blockIdx.z;
   const int64_t T = a.qk.n_tokens;
   const int Hq = a.qk.Hq, G = Hq / a.qk.n_kv, rows = a.qk.B * G, row0 = rt * kPvRows;
@@ -320,16 +335,15 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   const int64_t g_first = tile_lo / kGroupTiles, g_end = (tile_hi - 1) / kGroupTiles + 1;
   const int64_t gb = g_first + (int64_t)chunk * a.pv_chunk;
   const int64_t ge = min(gb + (int64_t)a.pv_chunk, g_end);
-  if (warp == 0) tmem_alloc(&s_taddr, kPvTmemCols);
-  if (tid == 32) mbar_init(&s_bar, 1);
-  // this chunk's softmax maximum per row, m = max z over its tokens: warp w
-  // takes rows w, w + 8, ..., its lanes consecutive tokens (a chunk holds at
-  // most 256 of a head's tokens, 8 per lane); l = sum exp(z - m) is summed
-  // from the weights of the main loop below
+  if (threadIdx.x < 32) tmem_alloc(&s_taddr, kPvTmemCols);
+  if (tid == 32) mbar_init(&s_bar[team], 1);
+  // this chunk's softmax maximum per row, m = max z over its tokens: block
+  // warp w takes rows w and w + 32, its lanes consecutive tokens, 256 at a
+  // time; l = sum exp(z - m) is summed from the weights of the main loop
+  // below
   {
-    const int lane = tid & 31;
     const int64_t c_lo = max(gb * kGroupTiles, tile_lo), c_hi = min(ge * kGroupTiles, tile_hi);
-    for (int rr = warp; rr < kPvRows; rr += kDecThreads / 32) {
+    for (int rr = threadIdx.x >> 5; rr < kPvRows; rr += kPvThreads / 32) {
       const int row = row0 + rr;
       float m = -INFINITY;
       if (row < rows) {
@@ -354,108 +368,131 @@ __global__ void __launch_bounds__(kDecThreads, 3) pv_kernel(AttnArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t taddr = s_taddr;
-  const uint32_t a_hi = smem_addr(s_ops), a_lo = a_hi + kPvOpBytes, b_op = a_hi + 2 * kPvOpBytes;
-  // this thread's slots: e^T (d = 16 r + c, token tl) and B (row i >> 5, token i & 31)
-  float *const ehi = reinterpret_cast<float *>(s_ops) +
-                     (288 * r + (tl >> 2) * kPvAKStride + (tl & 3) * 4) / 4;
-  float *const elo = ehi + kPvOpBytes / 4;
-  float *const bp = reinterpret_cast<float *>(s_ops + 2 * kPvOpBytes) +
-                    ((tid >> 5) * 16 + ((tid & 31) >> 2) * kPvBKStride + (tid & 3) * 4) / 4;
-  bool ok_wait = true;                           // block-uniform
+  const uint32_t dcol = s_taddr + (uint32_t)(128 * team);
+  unsigned char *const tops = s_ops + team * kPvTeamBytes;
+  const uint32_t a_hi = smem_addr(tops), a_lo = a_hi + kPvOpBytes, b_op = a_hi + 2 * kPvOpBytes;
+  // e^T slots of this lane (token tl, rows of dimensions 16 r .. 16 r + 15)
+  unsigned char *const ebase = tops + 256 * r + (tl >> 2) * kPvKStride + (tl & 3) * 4;
+  // B slots: rows (tid >> 5) + 8 k (p_hi) and 64 + (tid >> 5) + 8 k (p_lo), token lane
+  float *const bp = reinterpret_cast<float *>(tops + 2 * kPvOpBytes + 16 * warp +
+                                              (lane >> 2) * kPvKStride + (lane & 3) * 4);
+  uint64_t *const bar = &s_bar[team];
+  bool ok_wait = true;                           // team-uniform after each barrier
   int committed = 0;                             // groups whose MMAs were issued
-  // the scores of a group are loaded one group ahead, so that their latency
-  // hides behind the decoding of the current one
   float pn[8], lsum[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) lsum[k] = 0.0f;
-  if (gb < ge) pv_load_z(a, gb, h, row0, G, rows, tile_lo, tile_hi, pn);
-  for (int64_t g = gb; g < ge; ++g) {            // block-uniform bounds
-    const int i = (int)(g - gb);
+  if (gb + team < ge) pv_load_z(a, gb + team, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
+  for (int64_t g = gb + team; g < ge; g += kPvTeams) {   // team-uniform bounds
     float e[16];
-    const bool ok = decode_lane<LAT, K>(a.v, g, e, s_start, s_warp);   // barriers inside
+    const bool ok = decode_lane<LAT, K, TeamBar>(a.v, g, e, s_start[team], s_warp[team]);
     if (!ok && tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_CORRUPT);
-    // the MMAs of the previous group must be done with the operands
-    if (i > 0 && ok_wait) ok_wait = mbar_wait(&s_bar, (uint32_t)(i - 1) & 1u, kPvWaitLimit);
+    // the MMAs of the team's previous group must be done with the operands
+    if (committed > 0 && ok_wait) ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       float hi, lo;
       split_tf32(e[c], hi, lo);
-      const int off = ((c >> 3) * kPvAGStride + (c & 7) * 16) / 4;
-      ehi[off] = hi;
-      elo[off] = lo;
+      const int off = 128 * (c >> 3) + ((16 * r + 16 * c) & 0x70);   // permuted row
+      *reinterpret_cast<float *>(ebase + off) = hi;
+      *reinterpret_cast<float *>(ebase + kPvOpBytes + off) = lo;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {                // p = exp(z - m), 0 for z = -inf
-      const float mm = s_m[(tid >> 5) + 8 * k];
+      const float mm = s_m[warp + 8 * k];
       const float p = pn[k] == -INFINITY ? 0.0f : expf(__fsub_rn(pn[k], mm));
       lsum[k] = __fadd_rn(lsum[k], p);           // this lane's token column, in group order
       float hi, lo;
       split_tf32(p, hi, lo);
-      bp[k * kPvBGStride / 4] = hi;              // rows (tid >> 5) + 8 k
-      bp[(k + 8) * kPvBGStride / 4] = lo;        // rows 64 + (tid >> 5) + 8 k
+      bp[k * kPvGStride / 4] = hi;
+      bp[(k + 8) * kPvGStride / 4] = lo;
     }
-    if (g + 1 < ge) pv_load_z(a, g + 1, h, row0, G, rows, tile_lo, tile_hi, pn);
+    if (g + kPvTeams < ge) pv_load_z(a, g + kPvTeams, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
     fence_async_smem();
-    ok_wait = __syncthreads_and(ok_wait) != 0;
+    ok_wait = TeamBar::sync_and(ok_wait) != 0;
     if (!ok_wait) continue;
+    const bool first = committed == 0;
     ++committed;
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_tf32(taddr, umma_desc(a_hi + ks * 2 * kPvAKStride, kPvAKStride, kPvAGStride),
-                  umma_desc(b_op + ks * 2 * kPvBKStride, kPvBKStride, kPvBGStride), kPvIdesc,
-                  (i > 0 || ks > 0) ? 1u : 0u);
+        umma_tf32(dcol, umma_desc(a_hi + ks * 2 * kPvKStride, kPvKStride, kPvGStride),
+                  umma_desc(b_op + ks * 2 * kPvKStride, kPvKStride, kPvGStride), kPvIdesc,
+                  (!first || ks > 0) ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_tf32(taddr, umma_desc(a_lo + ks * 2 * kPvAKStride, kPvAKStride, kPvAGStride),
-                  umma_desc(b_op + ks * 2 * kPvBKStride, kPvBKStride, kPvBGStride), kPvIdesc, 1u);
-      umma_commit(&s_bar);
+        umma_tf32(dcol, umma_desc(a_lo + ks * 2 * kPvKStride, kPvKStride, kPvGStride),
+                  umma_desc(b_op + ks * 2 * kPvKStride, kPvKStride, kPvGStride), kPvIdesc, 1u);
+      umma_commit(bar);
     }
   }
-  // l per row: the lanes' column sums combined by a fixed butterfly
+  // the team's l per row: its lanes' column sums combined by a fixed butterfly
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     float l = lsum[k];
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, d));
-    const int rr = warp + 8 * k;
-    if ((tid & 31) == 0)
-      a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(s_m[rr], l);
+    if (lane == 0) s_l[team][warp + 8 * k] = l;
   }
-  if (committed > 0) {
-    if (ok_wait) ok_wait = mbar_wait(&s_bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
-    ok_wait = __syncthreads_and(ok_wait) != 0;
-    if (ok_wait) {
-      tc_fence_after();
-      // warp w reads dimensions 32 (w % 4) + lane for rows 32 (w / 4) .. +31
-      const int qd = warp & 3, hf = warp >> 2, d = 32 * qd + (tid & 31);
-      float *part = a.partials +
-                    ((((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows) * kTile;
+  if (committed > 0 && ok_wait)                  // the team's last MMAs
+    ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
+  ok_wait = __all_sync(0xffffffffu, ok_wait) != 0;   // warp-uniform for the tensor-memory loads
+  tc_fence_before();
+  __syncthreads();                               // every team's operands are free
+  tc_fence_after();
+  // the team's sums, hi + lo halves added, as S[team][row][d] in the operand
+  // area: warp w reads tensor-memory lanes (permuted rows of e^T)
+  // 32 (w % 4) .. +31 for query rows 32 (w / 4) .. +31
+  {
+    float *S = reinterpret_cast<float *>(s_ops) + team * (kPvRows * kTile);
+    const int L = 32 * (warp & 3) + lane, Gr = L >> 3, rr = Gr >> 1;
+    const int d = 16 * rr + 8 * (Gr & 1) + (((L & 7) - rr) & 7);
+    const int hf = warp >> 2;
+    if (committed > 0 && ok_wait) {
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         float vh[16], vl[16];
-        const uint32_t lane_addr = taddr + ((uint32_t)(32 * qd) << 16);
+        const uint32_t lane_addr = dcol + ((uint32_t)(32 * (warp & 3)) << 16);
         tmem_ld16(lane_addr + (uint32_t)(32 * hf + 16 * jj), vh);
         tmem_ld16(lane_addr + (uint32_t)(64 + 32 * hf + 16 * jj), vl);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          part[(int64_t)(32 * hf + 16 * jj + j) * kTile + d] = __fadd_rn(vh[j], vl[j]);
+        for (int j = 0; j < 16; ++j) S[(32 * hf + 16 * jj + j) * kTile + d] = __fadd_rn(vh[j], vl[j]);
       }
+    } else {                                     // no group of this team (or a lost wait)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) S[(32 * hf + j) * kTile + d] = 0.0f;
     }
   }
   if (!ok_wait) {
-    if (tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_TIMEOUT);
-    // the operands' last MMAs may still be in flight: give them a bounded
+    atomicOr(a.v.status, (uint32_t)HQ_ERR_TIMEOUT);
+    // the team's last MMAs may still be in flight: give them a bounded
     // while before the tensor memory goes back
-    if (committed > 0) mbar_wait(&s_bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
+    if (committed > 0) mbar_wait(bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  // partial sums and statistics of the block: teams added in order
+  {
+    const float *S = reinterpret_cast<const float *>(s_ops);
+    float *part = a.partials + ((((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows) * kTile;
+    for (int i = threadIdx.x; i < kPvRows * kTile; i += kPvThreads) {
+      float v = S[i];
+#pragma unroll
+      for (int t = 1; t < kPvTeams; ++t) v = __fadd_rn(v, S[t * kPvRows * kTile + i]);
+      part[i] = v;
+    }
+    if (threadIdx.x < kPvRows) {
+      const int rr = threadIdx.x;
+      float l = s_l[0][rr];
+#pragma unroll
+      for (int t = 1; t < kPvTeams; ++t) l = __fadd_rn(l, s_l[t][rr]);
+      a.stats[(((int64_t)h * a.chunks + chunk) * a.rowtiles + rt) * kPvRows + rr] = make_float2(s_m[rr], l);
+    }
+  }
+  if (threadIdx.x < 32) {
     tc_fence_after();
-    tmem_dealloc(taddr, kPvTmemCols);
+    tmem_dealloc(s_taddr, kPvTmemCols);
   }
 }
 
@@ -635,7 +672,7 @@ static int pv_capacity() {
   int sms = 0, per_sm = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kDecThreads,
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kPvThreads,
                                                 kPvSmemBytes);
   const int c = sms * per_sm > 0 ? sms * per_sm : 1;
   if (dev >= 0 && dev < kDevices) cap[dev] = c;
@@ -651,7 +688,7 @@ static void pick_pv_chunk(AttnArgs &a, int cap) {
   const int64_t groups = (a.qk.n_tokens + kGroupTiles - 1) / kGroupTiles + 1;   // a head's, at most
   const int room = a.chunks;
   double best = -1.0;
-  for (int cs = kPvMaxGroupsPerChunk; cs >= kPvMinGroupsPerChunk; --cs) {
+  for (int cs = kPvChunkMax; cs >= kPvMinGroupsPerChunk; --cs) {
     const int64_t chunks = (groups + cs - 1) / cs;
     if (chunks > room) continue;
     const double blocks = (double)chunks * a.qk.n_kv * a.rowtiles;
@@ -667,7 +704,7 @@ static void pick_pv_chunk(AttnArgs &a, int cap) {
 template <int LAT, int K>
 static void launch_pv_k(AttnArgs a, cudaStream_t st) {
   pick_pv_chunk(a, pv_capacity<LAT, K>());
-  dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kDecThreads);
+  dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kPvThreads);
   launch_pv_one<LAT, K>(a, grid, block, st);
   pv_finish_kernel<<<(unsigned)(a.qk.B * a.qk.Hq), kTile, 0, st>>>(a);
 }
