@@ -55,7 +55,7 @@ __global__ void rotate_queries_kernel(QkArgs a) {
 constexpr int kQkRows = 64;                      // query rows per block
 constexpr int kQkTeams = 4;
 constexpr int kQkThreads = kQkTeams * kDecThreads;
-constexpr int kQkGroupsPerChunk = 2 * kQkTeams;  // groups of 32 tokens per block
+constexpr int kQkChunkMin = kQkTeams, kQkChunkMax = 32;   // groups of 32 tokens per block
 constexpr int kQkAKStride = 1024;                // bytes between K-cores of A (8 row groups)
 constexpr int kQkAGStride = 128;                 // bytes between 8-row groups of A
 constexpr int kQkBKStride = 528;                 // bytes between K-cores of B (4 token groups + 16)
@@ -70,7 +70,7 @@ constexpr uint32_t kQkTmemCols = 32 * kQkTeams;
 __device__ __forceinline__ int qk_kcore(int db) { return 8 * (db & 3) + (db >> 2); }
 
 template <int LAT, int K>
-__global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
+__global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chunk_groups) {
   __shared__ uint64_t s_start[kQkTeams][kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[kQkTeams][2][kDecThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[kQkTeams];
@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a) {
   const int G = a.Hq / a.n_kv, rows = a.B * G;
   const int64_t tile_lo = (int64_t)h * T, tile_hi = tile_lo + T;
   const int64_t g_first = tile_lo / kGroupTiles, g_end = (tile_hi - 1) / kGroupTiles + 1;
-  const int64_t gb = g_first + (int64_t)chunk * kQkGroupsPerChunk;
-  const int64_t ge = min(gb + (int64_t)kQkGroupsPerChunk, g_end);
+  const int64_t gb = g_first + (int64_t)chunk * chunk_groups;
+  const int64_t ge = min(gb + (int64_t)chunk_groups, g_end);
   if (gb >= ge) return;                          // uniform: nothing of head h here
   if (threadIdx.x < 32) tmem_alloc(&s_taddr, kQkTmemCols);
   if (tid == 32) mbar_init(&s_bar[team], 1);
@@ -631,81 +631,76 @@ __global__ void gemm_reduce_kernel(GemmArgs a) {
   if (lane == 0) a.y[b * a.rows + o] = s;
 }
 
+// The chunk size in [lo, hi] groups whose grid (chunks x `other` blocks)
+// fills the most of its last wave of `cap` resident blocks; ties go to the
+// larger chunk.  Chunks above max_chunks (when positive) are not allowed.
+static int pick_chunk(int64_t groups, int64_t other, int cap, int lo, int hi, int64_t max_chunks) {
+  double best = -1.0;
+  int pick = lo;
+  for (int cs = hi; cs >= lo; --cs) {
+    const int64_t chunks = (groups + cs - 1) / cs;
+    if (max_chunks > 0 && chunks > max_chunks) continue;
+    const double waves = (double)(chunks * other) / cap, fill = waves / std::ceil(waves);
+    if (fill > best + 1e-9) {
+      best = fill;
+      pick = cs;
+    }
+  }
+  return pick;
+}
+
+// Resident blocks of a kernel instance per SM, times the SM count of the
+// current device (kept per call site and device after the first query).
+template <class F>
+static int capacity(int *cache, F kernel, int threads, int smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0, per_sm = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  const int c = sms * per_sm > 0 ? sms * per_sm : 1;
+  if (dev >= 0 && dev < 64) cache[dev] = c;
+  return c;
+}
+
 template <int LAT, int K>
-static void launch_qk_one(const QkArgs &a, dim3 grid, dim3 block, cudaStream_t st) {
-  cudaFuncSetAttribute(scores_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
-  scores_kernel<LAT, K><<<grid, block, kQkSmemBytes, st>>>(a);
+static void launch_qk_one(const QkArgs &a, cudaStream_t st) {
+  static int cache[64] = {};
+  const int cap = capacity(cache, scores_kernel<LAT, K>, kQkThreads, kQkSmemBytes);
+  // a head's tokens touch at most ceil(T / 32) + 1 groups
+  const int64_t groups = (a.n_tokens + kGroupTiles - 1) / kGroupTiles + 1;
+  const int rowtiles = (a.B * (a.Hq / a.n_kv) + kQkRows - 1) / kQkRows;
+  const int cs = pick_chunk(groups, (int64_t)a.n_kv * rowtiles, cap, kQkChunkMin, kQkChunkMax, 0);
+  dim3 grid((unsigned)((groups + cs - 1) / cs), (unsigned)a.n_kv, (unsigned)rowtiles),
+      block(kQkThreads);
+  scores_kernel<LAT, K><<<grid, block, kQkSmemBytes, st>>>(a, cs);
 }
 
 template <int LAT>
 static void launch_qk_lat(const QkArgs &a, cudaStream_t st) {
-  // a head's tokens touch at most T / 32 + 1 groups (one more when it
-  // starts inside a group)
-  const int64_t groups = a.n_tokens / kGroupTiles + 2;
-  const int rows = a.B * (a.Hq / a.n_kv);
-  dim3 grid((unsigned)((groups + kQkGroupsPerChunk - 1) / kQkGroupsPerChunk), (unsigned)a.n_kv,
-            (unsigned)((rows + kQkRows - 1) / kQkRows)),
-      block(kQkThreads);
   switch (a.dec.rice_k) {
-    case 1: launch_qk_one<LAT, 1>(a, grid, block, st); break;
-    case 2: launch_qk_one<LAT, 2>(a, grid, block, st); break;
-    case 3: launch_qk_one<LAT, 3>(a, grid, block, st); break;
-    default: launch_qk_one<LAT, -1>(a, grid, block, st); break;
+    case 1: launch_qk_one<LAT, 1>(a, st); break;
+    case 2: launch_qk_one<LAT, 2>(a, st); break;
+    case 3: launch_qk_one<LAT, 3>(a, st); break;
+    default: launch_qk_one<LAT, -1>(a, st); break;
   }
 }
 
-template <int LAT, int K>
-static void launch_pv_one(const AttnArgs &a, dim3 grid, dim3 block, cudaStream_t st) {
-  cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
-  pv_kernel<LAT, K><<<grid, block, kPvSmemBytes, st>>>(a);
-}
 
-// Blocks of one pv_kernel instance resident per SM, times the SM count of
-// the current device (kept per instance and device after the first query).
-template <int LAT, int K>
-static int pv_capacity() {
-  constexpr int kDevices = 64;
-  static int cap[kDevices] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < kDevices && cap[dev] > 0) return cap[dev];
-  int sms = 0, per_sm = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaFuncSetAttribute(pv_kernel<LAT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmemBytes);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pv_kernel<LAT, K>, kPvThreads,
-                                                kPvSmemBytes);
-  const int c = sms * per_sm > 0 ? sms * per_sm : 1;
-  if (dev >= 0 && dev < kDevices) cap[dev] = c;
-  return c;
-}
-
-// The chunk size (groups per block) whose grid fills the most of its last
-// wave of `cap` resident blocks; ties go to the larger chunk (fewer
-// partial sums to combine).  a.chunks arrives as the workspace's chunk count
-// (that of the smallest chunk size, with the same bound on a head's groups)
-// and no choice may exceed it.
-static void pick_pv_chunk(AttnArgs &a, int cap) {
-  const int64_t groups = (a.qk.n_tokens + kGroupTiles - 1) / kGroupTiles + 1;   // a head's, at most
-  const int room = a.chunks;
-  double best = -1.0;
-  for (int cs = kPvChunkMax; cs >= kPvMinGroupsPerChunk; --cs) {
-    const int64_t chunks = (groups + cs - 1) / cs;
-    if (chunks > room) continue;
-    const double blocks = (double)chunks * a.qk.n_kv * a.rowtiles;
-    const double waves = blocks / cap, fill = waves / std::ceil(waves);
-    if (fill > best + 1e-9) {
-      best = fill;
-      a.pv_chunk = cs;
-      a.chunks = (int)chunks;
-    }
-  }
-}
-
+// The chunk size is picked for whole waves (pick_chunk); the workspace holds
+// the chunks of the smallest chunk size, a.chunks on entry.
 template <int LAT, int K>
 static void launch_pv_k(AttnArgs a, cudaStream_t st) {
-  pick_pv_chunk(a, pv_capacity<LAT, K>());
+  static int cache[64] = {};
+  const int cap = capacity(cache, pv_kernel<LAT, K>, kPvThreads, kPvSmemBytes);
+  const int64_t groups = (a.qk.n_tokens + kGroupTiles - 1) / kGroupTiles + 1;   // a head's, at most
+  a.pv_chunk = pick_chunk(groups, (int64_t)a.qk.n_kv * a.rowtiles, cap, kPvMinGroupsPerChunk,
+                          kPvChunkMax, a.chunks);
+  a.chunks = (int)((groups + a.pv_chunk - 1) / a.pv_chunk);
   dim3 grid((unsigned)a.chunks, (unsigned)a.qk.n_kv, (unsigned)a.rowtiles), block(kPvThreads);
-  launch_pv_one<LAT, K>(a, grid, block, st);
+  pv_kernel<LAT, K><<<grid, block, kPvSmemBytes, st>>>(a);
   pv_finish_kernel<<<(unsigned)(a.qk.B * a.qk.Hq), kTile, 0, st>>>(a);
 }
 
