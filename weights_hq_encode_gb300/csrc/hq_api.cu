@@ -6,7 +6,7 @@
 
 #include <cuda_runtime.h>
 
-#include "hq_internal.h"
+#include "hq_fused.h"
 
 namespace {
 

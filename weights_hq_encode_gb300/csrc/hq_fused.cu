@@ -11,6 +11,7 @@
 #include <cmath>
 
 #include "hq_decode_lane.cuh"
+#include "hq_fused.h"
 #include "hq_umma.cuh"
 
 namespace hq {

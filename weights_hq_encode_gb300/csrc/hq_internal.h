@@ -65,47 +65,6 @@ struct DecodeArgs {
   const float *rot;         // nullptr, or [n_segments][128][128] row-major rotations
 };
 
-struct QkArgs {
-  DecodeArgs dec;           // K stream
-  int n_kv;
-  int64_t n_tokens;
-  const uint16_t *q;        // [B][Hq][128] bf16
-  int B, Hq;
-  float *qrot;              // [B][Hq][128] fp32 workspace: s_dec * H * D_h * q
-  float *scores;            // [B][Hq][n_tokens]
-};
-
-// Decode attention: the K side is the scores pass (qk), the V side another
-// stream; each chunk of tokens keeps its own softmax maximum and sum (stats)
-// beside its partial sums of exp(z - max) e (partials).
-constexpr int kPvRows = 64;           // query rows per contraction tile
-constexpr int kPvMaxGroupsPerChunk = 8;  // groups of 32 tokens per block: the launch picks
-constexpr int kPvMinGroupsPerChunk = 4;  // a chunk size in this range that fills whole waves
-struct AttnArgs {
-  QkArgs qk;                // K stream, queries, rotated queries, scores -> probabilities
-  DecodeArgs v;             // V stream
-  float scale;              // softmax scale applied to the scores
-  float *partials;          // [n_kv][chunks][rowtiles][kPvRows][128]
-  float2 *stats;            // [n_kv][chunks][rowtiles][kPvRows]: (max z, sum exp(z - max))
-  int chunks, rowtiles;
-  int pv_chunk;             // groups per chunk (set by the launch)
-  float *out;               // [B][Hq][128] fp32
-};
-
-// Product with a compressed weight matrix W [rows][cols] (row-major tiles):
-// y[b][o] = sum_i What[o][i] x[b][i].
-struct GemmArgs {
-  DecodeArgs dec;           // W stream
-  int64_t rows, cols;
-  int64_t tpr;              // tiles per row = cols / 128
-  int tpr_shift;            // log2(tpr) when a power of two, else -1
-  const uint16_t *x;        // [B][cols] bf16
-  int B;
-  float *xrot;              // [B][cols] fp32: s_dec * H * D * x, per 128-column tile
-  float *partial;           // [B][n_tiles] fp32: one tile's share of y
-  float *y;                 // [B][rows] fp32
-};
-
 // Segment (or head) of tile t: a shift when the divisor is a power of two.
 __host__ __device__ __forceinline__ int64_t div_by(int64_t t, int64_t d, int shift) {
   return shift >= 0 ? (t >> shift) : t / d;
@@ -120,9 +79,5 @@ __host__ __device__ __forceinline__ int pow2_shift(int64_t d) {
 int launch_encode(const EncodeArgs &a, int lattice, cudaStream_t st);
 int encode_tiles_per_block();
 int launch_decode(const DecodeArgs &a, int lattice, cudaStream_t st);
-int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);
-int launch_decode_attention(const AttnArgs &a, int k_lattice, int v_lattice, bool want_probs,
-                            cudaStream_t st);
-int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st);
 
 }  // namespace hq
