@@ -383,10 +383,10 @@ __global__ void __launch_bounds__(kPvThreads, 1) pv_kernel(AttnArgs a) {
   float pn[8], lsum[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) lsum[k] = 0.0f;
-  if (gb + team < ge) pv_load_z(a, gb + team, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
   for (int64_t g = gb + team; g < ge; g += kPvTeams) {   // team-uniform bounds
     float e[16];
     const bool ok = decode_lane<LAT, K, TeamBar>(a.v, g, e, s_start[team], s_warp[team]);
+    pv_load_z(a, g, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
     if (!ok && tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_CORRUPT);
     // the MMAs of the team's previous group must be done with the operands
     if (committed > 0 && ok_wait) ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
@@ -408,7 +408,6 @@ __global__ void __launch_bounds__(kPvThreads, 1) pv_kernel(AttnArgs a) {
       bp[k * kPvGStride / 4] = hi;
       bp[(k + 8) * kPvGStride / 4] = lo;
     }
-    if (g + kPvTeams < ge) pv_load_z(a, g + kPvTeams, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
     fence_async_smem();
     ok_wait = TeamBar::sync_and(ok_wait) != 0;
     if (!ok_wait) continue;
