@@ -688,7 +688,6 @@ static void launch_qk_lat(const QkArgs &a, cudaStream_t st) {
   }
 }
 
-
 // The chunk size is picked for whole waves (pick_chunk); the workspace holds
 // the chunks of the smallest chunk size, a.chunks on entry.
 template <int LAT, int K>
