@@ -501,3 +501,40 @@ def test_scalar_special_case_is_textbook_uniform_quantizer(oracle):
     # reconstruction error bounded by the cell: |H^T(v - y)| / (alpha sqrt128) per coord
     err = dec["out"] - xf
     assert np.sqrt((err ** 2).mean()) < 0.5 / alpha * 1.05
+
+
+@pytest.mark.parametrize("lat,name", [(8, "E8"), (4, "D4"), (2, "A2"), (1, "Z")])
+def test_dithered_decode_error_is_the_cell_second_moment(oracle, lat, name):
+    """The oracle's decoder, end to end: with subtractive dither (Method 4,
+    "Bias correction": U is added before quantisation and subtracted after
+    reconstruction) the lattice-domain error v - u - y is uniform on the
+    Voronoi cell and independent of u, and the inverse transform is
+    orthonormal up to the 1/alpha scale, so alpha^2 mean((x_hat - x)^2) per
+    dimension equals G(Lambda) det^(2/n) (Method 2).  Reconstructing with
+    v + u instead adds 4 E[u^2] (five times the target), and with v alone
+    E[u^2] (twice the target), so both mistakes fail here.  The inputs are the
+    exact bf16 values, signs and segments are non-trivial, and |y| stays far
+    below the range limit."""
+    gold = {r[0]: float(r[3]) for r in _read_table("lattice_nsm.txt")}
+    rng = np.random.default_rng(17 + lat)
+    n_tiles = 512
+    xf = rng.standard_normal((n_tiles, 128)).astype(np.float32)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)       # bf16 bit patterns
+    xb = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    signs = np.stack([oracle.make_signs(3, s) for s in range(4)])
+    alpha = 6.0
+    P = oracle.make_params(lat, 3, alpha, 1, 4321, signs, 128)
+    enc = oracle.encode(P, x)
+    assert enc["status"] == 0
+    dec = oracle.decode(P, enc["stream"], enc["offsets"], n_tiles, out="f32")
+    assert dec["status"] == 0
+    err2 = (alpha ** 2) * (dec["out"].astype(np.float64) - xb) ** 2
+    dim = lat if lat > 1 else 1
+    per_vec = err2.reshape(-1, 128).reshape(-1, dim).mean(-1)
+    m, se = per_vec.mean(), per_vec.std() / np.sqrt(per_vec.size)
+    assert abs(m - gold[name]) < 4 * se, (m, gold[name], se)
+    # the decoder without dither on the same codes is a different, worse reconstruction
+    P0 = oracle.make_params(lat, 3, alpha, 0, 4321, signs, 128)
+    dec0 = oracle.decode(P0, enc["stream"], enc["offsets"], n_tiles, out="f32")
+    m0 = ((alpha ** 2) * (dec0["out"].astype(np.float64) - xb) ** 2).mean()
+    assert m0 > 1.5 * gold[name]
