@@ -20,13 +20,16 @@ __global__ void __launch_bounds__(kDecThreads, ROT ? 2 : 8)
 decode_kernel(DecodeArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
-  __shared__ float4 s_scale[kTile / 4];          // D_i * s_dec of the block's first segment
+  // D_i * s_dec of the block's first segment, coordinates 16r + j and 16r + j + 8
+  // side by side (the pairs a lane holds after the transform)
+  __shared__ float4 s_scale[kTile / 4];
+  __shared__ __align__(16) float s_tr[kGroupTiles * kTrTile];  // transposes of the transform
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t g = blockIdx.x;
   const int64_t seg0 = div_by(g * kGroupTiles, a.tiles_per_segment, a.seg_shift);
   if (tid < kTile) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 5));
-    reinterpret_cast<float *>(s_scale)[tid] =
+    reinterpret_cast<float *>(s_scale)[16 * (tid >> 4) + 2 * (tid & 7) + ((tid >> 3) & 1)] =
         __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
   }
   constexpr int kRS = kTile + 4;                 // row stride of the rotation's operands
@@ -38,8 +41,8 @@ decode_kernel(DecodeArgs a) {
   const bool ok = decode_lane<LAT, K>(a, g, e, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
   if (!ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
-  // the transform runs on every lane of the block (shuffles need full warps)
-  fwht128_x8(e, r);
+  // the transform runs on every lane of the block (its transposes synchronise whole warps)
+  fwht128_t8(e, s_tr + tl * kTrTile, r);
   const bool tvalid = t < a.n_tiles;
   if (!ROT && !tvalid) return;
   if (ok && tvalid) {
@@ -48,10 +51,8 @@ decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float4 sc = s_scale[4 * r + c];
-        e[4 * c] = __fmul_rn(e[4 * c], sc.x);
-        e[4 * c + 1] = __fmul_rn(e[4 * c + 1], sc.y);
-        e[4 * c + 2] = __fmul_rn(e[4 * c + 2], sc.z);
-        e[4 * c + 3] = __fmul_rn(e[4 * c + 3], sc.w);
+        upk2(mul2(pk2(e[2 * c], e[2 * c + 8]), pk2(sc.x, sc.y)), e[2 * c], e[2 * c + 8]);
+        upk2(mul2(pk2(e[2 * c + 1], e[2 * c + 9]), pk2(sc.z, sc.w)), e[2 * c + 1], e[2 * c + 9]);
       }
     } else {
       const uint32_t *mask = a.signs + 4 * (div_by(t, a.tiles_per_segment, a.seg_shift));

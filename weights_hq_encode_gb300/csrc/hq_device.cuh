@@ -111,31 +111,126 @@ __device__ __forceinline__ void rotate128(const float *R, float x[128]) {
   for (int i = 0; i < 128; ++i) x[i] = z[i];
 }
 
-// The same transform with a tile spread over 8 consecutive lanes, lane r of
-// the tile holding coordinates 16r .. 16r+15: stages h = 1, 2, 4, 8 stay in
-// registers, stages 16, 32, 64 pair lane r with lane r ^ 1, r ^ 2, r ^ 4.
-// The lower coordinate of a pair gets fl(a + b), the upper fl(a - b), exactly
-// as in the single-thread order (one rounding each, same stage order).
-__device__ __forceinline__ void fwht128_x8(float x[16], int r) {
+// ---------------------------------------------------------------- packed fp32 pairs
+// sm_100+ executes add / sub / mul / fma on a pair of fp32 values in one
+// instruction; each half rounds to nearest even exactly as the scalar
+// instruction does, so a pair operation equals two scalar ones bit for bit.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// (lo, hi) <- (lo + hi, lo - hi) on two pairs: the butterfly of two stages
+// positions at once.
+__device__ __forceinline__ void bfly2(float &a0, float &a1, float &b0, float &b1) {
+  const uint64_t A = pk2(a0, a1), B = pk2(b0, b1);
+  upk2(add2(A, B), a0, a1);
+  upk2(sub2(A, B), b0, b1);
+}
+
+// The transform with a tile spread over 8 consecutive lanes (lane r holds
+// coordinates 16r .. 16r+15) and the three cross-lane stages done in
+// registers after a transposition through shared memory.  Stages 1, 2, 4 run
+// on pairs (x[j], x[j+8]), stage 8 inside those pairs; each pair is stored to
+// row j of an 8-row table (coordinate i at row i mod 8, column i / 8, rows
+// kTrRow floats apart), lane c reads row c back (coordinates c + 8m,
+// m = 0..15) and runs stages 16, 32, 64 on pairs of adjacent columns, then
+// writes the row back: the result stays in the table.  Every coordinate goes
+// through the same additions in the same stage order as the single-thread
+// form.  `tile` is the tile's table (kTrTile floats, 16-byte aligned), private
+// to its 8 lanes; with rows of 20 floats and tables 176 floats apart, the
+// pair stores (16 lanes = two tiles) and the 16-byte row loads and stores
+// (8 lanes = one tile) of a warp are free of bank conflicts.  All 32 lanes of
+// the warp must call it.
+constexpr int kTrRow = 20;
+constexpr int kTrTile = 176;
+__device__ __forceinline__ void fwht128_t8_smem(float x[16], float *tile, int r) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      float a = x[i], b = x[i + h];
-      x[i] = __fadd_rn(a, b);
-      x[i + h] = __fsub_rn(a, b);
+    for (int j = 0; j < 8; ++j) {
+      if (j & h) continue;
+      bfly2(x[j], x[j + 8], x[j + h], x[j + h + 8]);
     }
   }
 #pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {
-    const float sg = (r & m) ? -1.0f : 1.0f;
+  for (int j = 0; j < 8; ++j) {
+    const float a = x[j], b = x[j + 8];
+    x[j] = __fadd_rn(a, b);
+    x[j + 8] = __fsub_rn(a, b);
+  }
+  // pair (x[j], x[j+8]) = coordinates 16r + j, 16r + j + 8: row j, columns 2r, 2r + 1
+  const uint32_t pa = (uint32_t)__cvta_generic_to_shared(tile + 2 * r);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-      x[i] = __fmaf_rn(x[i], sg, o);        // lower: mine + other; upper: other - mine
+  for (int j = 0; j < 8; ++j)
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pa + 4u * kTrRow * j), "f"(x[j]),
+                 "f"(x[j + 8])
+                 : "memory");
+  __syncwarp();
+  float y[16];
+  const uint32_t row = (uint32_t)__cvta_generic_to_shared(tile + kTrRow * r);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(y[4 * q]), "=f"(y[4 * q + 1]), "=f"(y[4 * q + 2]), "=f"(y[4 * q + 3])
+                 : "r"(row + 16u * q)
+                 : "memory");
+  // y[m] = coordinate r + 8m: stages 16, 32, 64 act on bits 1, 2, 3 of m
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      if (a & h) continue;
+      bfly2(y[2 * a], y[2 * a + 1], y[2 * (a + h)], y[2 * (a + h) + 1]);
     }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + 16u * q), "f"(y[4 * q]),
+                 "f"(y[4 * q + 1]), "f"(y[4 * q + 2]), "f"(y[4 * q + 3])
+                 : "memory");
+  __syncwarp();
+}
+// Coordinate 16r + 8v + c of the transformed tile (after fwht128_t8_smem).
+__device__ __forceinline__ float tr_coord(const float *tile, int r, int v, int c) {
+  float f;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f)
+               : "r"((uint32_t)__cvta_generic_to_shared(tile + 2 * r + v) + 4u * kTrRow * c)
+               : "memory");
+  return f;
+}
+// The whole transform back in registers: x[j], x[j + 8] = coordinates 16r + j, 16r + j + 8.
+__device__ __forceinline__ void fwht128_t8(float x[16], float *tile, int r) {
+  fwht128_t8_smem(x, tile, r);
+  const uint32_t pa = (uint32_t)__cvta_generic_to_shared(tile + 2 * r);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x[j]), "=f"(x[j + 8])
+                 : "r"(pa + 4u * kTrRow * j)
+                 : "memory");
 }
 
 // 1 << n for n < 32, and 0 for n >= 32 (PTX shl clamps the shift amount).
@@ -396,6 +491,90 @@ __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) 
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i] = zigzag(nearest_z(y[i]));
   }
+}
+
+// The E8 rule of quantize_fold8 for the lane's two 8-vectors at once
+// (y[i] and y[8 + i] are coordinate i of each): the roundings, errors, lattice
+// point and fold run on pairs (one vector per half), the per-vector decision
+// in scalar code; every value is the one quantize_fold8 computes.
+__device__ __forceinline__ void quantize_fold16_e8(const float y[16], uint32_t s[16]) {
+  float F[16], e[16];
+  uint32_t par[2] = {0u, 0u}, sx[2] = {0u, 0u};
+  const uint64_t M2 = pk2(kMagic2, kMagic2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t Y = pk2(y[i], y[8 + i]);
+    const uint64_t T = add2(Y, M2);
+    const uint64_t FF = sub2(T, M2);
+    upk2(sub2(Y, FF), e[i], e[8 + i]);
+    upk2(FF, F[i], F[8 + i]);
+    float t0, t1;
+    upk2(T, t0, t1);
+    par[0] ^= __float_as_uint(t0);
+    par[1] ^= __float_as_uint(t1);
+    sx[0] ^= __float_as_uint(e[i]);
+    sx[1] ^= __float_as_uint(e[8 + i]);
+  }
+  float c[16];
+  bool odd[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float *eh = e + 8 * h;
+    const uint32_t pA = par[h] & 1u, pB = pA ^ (sx[h] >> 31);
+    float S = fabsf(eh[0]), mx = fabsf(eh[0]), mn = fabsf(eh[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      const float ai = fabsf(eh[i]);
+      S = __fadd_rn(S, ai);
+      mx = fmaxf(mx, ai);
+      mn = fminf(mn, ai);
+    }
+    float D = __fmaf_rn(-2.0f, S, pA ? 4.0f : 8.0f);
+    if (pB) D = __fmaf_rn(4.0f, mn, D);
+    if (pA) D = __fmaf_rn(4.0f, mx, D);
+    odd[h] = D < 0.0f;
+    const float m = odd[h] ? mn : mx;
+    bool open = odd[h] ? (pB != 0u) : (pA != 0u);
+    const float wb = odd[h] ? 1.0f : 0.0f, wh = odd[h] ? -1.0f : 2.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool hit = open && fabsf(eh[i]) == m;
+      open = open && !hit;
+      c[8 * h + i] = __uint_as_float(__float_as_uint(hit ? wh : wb) ^
+                                     (__float_as_uint(eh[i]) & 0x80000000u));
+    }
+  }
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) upk2(add2(pk2(F[i], F[8 + i]), pk2(c[i], c[8 + i])), v[i], v[8 + i]);
+  // fold, as in quantize_fold8
+  uint64_t sum7 = pk2(v[0], v[8]);
+#pragma unroll
+  for (int i = 1; i < 7; ++i) sum7 = add2(sum7, pk2(v[i], v[8 + i]));
+  const uint64_t half = fma2(sum7, pk2(0.5f, 0.5f), pk2(odd[0] ? -3.5f : 0.0f, odd[1] ? -3.5f : 0.0f));
+  float hr0, hr1;
+  upk2(add2(half, pk2(kMagic1, kMagic1)), hr0, hr1);
+  const uint32_t r0 = __float_as_uint(hr0) & 1u, r1 = __float_as_uint(hr1) & 1u;
+  const uint64_t C1 = pk2(odd[0] ? -1.0f : 1.0f, odd[1] ? -1.0f : 1.0f);
+  const float cs0 = odd[0] ? kMagic1 : kMagic1 - 1.0f, cs1 = odd[1] ? kMagic1 : kMagic1 - 1.0f;
+  const uint64_t TWO = pk2(2.0f, 2.0f);
+#pragma unroll
+  for (int i = 0; i < 7; ++i) {
+    float a0, a1;
+    upk2(fma2(TWO, pk2(v[i], v[8 + i]), C1), a0, a1);
+    s[i] = __float_as_uint(__fadd_rn(fabsf(a0), cs0)) - 0x4B400000u;
+    s[8 + i] = __float_as_uint(__fadd_rn(fabsf(a1), cs1)) - 0x4B400000u;
+  }
+  const float p0 = odd[0] ? 1.0f : 0.0f, p1 = odd[1] ? 1.0f : 0.0f;
+  const float rf0 = r0 ? 1.0f : 0.0f, rf1 = r1 ? 1.0f : 0.0f;
+  float a0, a1;
+  upk2(fma2(TWO, pk2(v[7], v[15]),
+            fma2(pk2(-4.0f, -4.0f), pk2(rf0, rf1), pk2(2.0f - 2.0f * p0, 2.0f - 2.0f * p1))),
+       a0, a1);
+  float b0, b1;
+  upk2(fma2(TWO, pk2(rf0, rf1), pk2(p0 - 2.0f + kMagic1, p1 - 2.0f + kMagic1)), b0, b1);
+  s[7] = __float_as_uint(__fadd_rn(fabsf(a0), b0)) - 0x4B400000u;
+  s[15] = __float_as_uint(__fadd_rn(fabsf(a1), b1)) - 0x4B400000u;
 }
 
 // Number of low remainder bits of coordinate c (within its 8-group) fixed by

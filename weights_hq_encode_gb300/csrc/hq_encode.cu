@@ -4,8 +4,9 @@
 // r = 0..7 of a tile hold coordinates 16r .. 16r+15 (two 8-vectors), so the
 // 32-byte loads of a warp are contiguous.  Per tile (HyperQuant summary,
 // Method 1-4): apply the segment's sign mask to the bf16 input, FWHT-128
-// (stages 1-8 in registers, 16-64 by warp shuffles), scale by alpha/sqrt(128)
-// and add the subtractive dither in one fused multiply-add, snap each
+// (stages 1-8 in registers, then a transposition through shared memory so
+// that stages 16-64 run in registers too), scale by alpha/sqrt(128) and add
+// the subtractive dither in one fused multiply-add (on fp32 pairs), snap each
 // 8-vector to the nearest lattice point and fold it into Rice symbols.
 // Bit lengths are scanned across the 8 lanes of a tile and the 32 tiles of
 // the group; groups are chained by a decoupled look-back (Merrill & Garland
@@ -227,7 +228,8 @@ __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int k
 template <int LAT, int K, bool ROT>
 __global__ void __launch_bounds__(kEncThreads, ROT ? 2 : 6)
 encode_kernel(EncodeArgs a) {
-  __shared__ uint32_t s_stage[kStageWords];
+  // staging window of the group's words; before that, the tile transposes of the transform
+  __shared__ __align__(16) uint32_t s_stage[kStageWords > kGroupTiles * kTrTile ? kStageWords : kGroupTiles * kTrTile];
   __shared__ uint32_t s_tile_u[kGroupTiles];
   __shared__ uint64_t s_tile_uoff[kGroupTiles];
   __shared__ uint64_t s_base, s_words;
@@ -250,8 +252,6 @@ encode_kernel(EncodeArgs a) {
     g = s_ticket;
   }
   if (tid == 0) s_flags = 0u;
-#pragma unroll
-  for (int i = tid; i < kStageWords; i += kEncThreads) s_stage[i] = 0u;
   if (g >= a.n_blocks) return;                   // only with a counter set ahead
   const int k = K >= 0 ? K : a.rice_k;
   const int64_t t0 = (int64_t)g * kGroupTiles;
@@ -370,25 +370,28 @@ encode_kernel(EncodeArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = 0.0f;
   }
-  fwht128_x8(x, r);
+  // the staging window holds the tile transposes of the transform until the
+  // group layout is known (it is cleared after the next block barrier)
+  fwht128_t8(x, reinterpret_cast<float *>(s_stage) + tl * kTrTile, r);
 
   // ---- scale + dither (one rounding), range rule for the whole tile
   const uint64_t gt = a.tile_base + (uint64_t)t;
   bool bad = false;
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    float u[8];
+  {
+    float u[16];
     if (a.dither) {
-      dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + jj), u);
+      dither8<LAT>(a.keys, gt, (uint32_t)(2 * r), u);
+      dither8<LAT>(a.keys, gt, (uint32_t)(2 * r + 1), u + 8);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = 0.0f;
+      for (int i = 0; i < 16; ++i) u[i] = 0.0f;
     }
+    const uint64_t S2 = pk2(a.s_enc, a.s_enc);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float y = __fmaf_rn(x[8 * jj + i], a.s_enc, u[i]);
-      bad |= !(fabsf(y) <= kRangeLimit);
-      x[8 * jj + i] = y;
+      upk2(fma2(pk2(x[i], x[8 + i]), S2, pk2(u[i], u[8 + i])), x[i], x[8 + i]);
+      bad |= !(fabsf(x[i]) <= kRangeLimit);
+      bad |= !(fabsf(x[8 + i]) <= kRangeLimit);
     }
   }
   const uint32_t bal = __ballot_sync(0xffffffffu, valid && bad);
@@ -410,8 +413,12 @@ encode_kernel(EncodeArgs a) {
 
   // ---- nearest point, fold, unary lengths
   uint32_t sym[16];
-  quantize_fold8<LAT>(x, sym);
-  quantize_fold8<LAT>(x + 8, sym + 8);
+  if (LAT == 8) {
+    quantize_fold16_e8(x, sym);
+  } else {
+    quantize_fold8<LAT>(x, sym);
+    quantize_fold8<LAT>(x + 8, sym + 8);
+  }
   uint32_t ubits = 0;
   if (valid) {
 #pragma unroll
@@ -427,6 +434,10 @@ encode_kernel(EncodeArgs a) {
   const uint32_t u_in_tile = incl - ubits;
   if (r == 7) s_tile_u[tl] = incl;
   __syncthreads();
+  // the transposes are done: clear the staging window for the bit assembly
+#pragma unroll
+  for (int i = tid; i < kStageWords / 4; i += kEncThreads)
+    reinterpret_cast<uint4 *>(s_stage)[i] = make_uint4(0u, 0u, 0u, 0u);
 
   // ---- group layout (warp 0): tile offsets, group total, published at once
   const uint64_t R = (uint64_t)(K >= 0 ? tile_rbits<LAT>(K) : a.rbits);
