@@ -276,6 +276,10 @@ def run_ours(args, rank, world):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    st_timed = int(status.item())                # errors raised inside the timed steps
+    if st_timed:
+        raise RuntimeError(f"codec status after the timed steps: {hq.hq_status_string(st_timed)} "
+                           f"({st_timed})")
     ms = t_start.elapsed_time(t_end) / args.steps
     if world > 1:
         tt = torch.tensor([ms], device=dev)
@@ -307,6 +311,32 @@ def run_ours(args, rank, world):
             "traffic": traffic, "peak_kind": peak_kind,
             "frac_of_nominal_8TBps": round(op_report[dom]["achieved_GBps"] / 8000.0, 4)}
 
+    # ---- N > 1: the ranks' caches are shards of one tensor of world x n tiles;
+    # shard.code_rank codes this rank's group-aligned range (tile_base = its
+    # first tile, as in the timed steps) and the one exchange, an all-gather
+    # of word totals, places its stream in the global stream (untimed)
+    sharded = None
+    if world > 1:
+        from weights_hq_encode_gb300 import shard
+
+        def allgather_int(v):
+            got = [torch.zeros(1, dtype=torch.int64, device=dev) for _ in range(world)]
+            dist.all_gather(got, torch.tensor([v], dtype=torch.int64, device=dev))
+            return [int(t.item()) for t in got]
+
+        r3 = RATES[-1]
+        rc = shard.code_rank(world * n, world, rank,
+                             shard.device_encode_range(hq, params[r3], xt, x_first=base),
+                             allgather_int)
+        same = rc.begin == base and rc.total_words == total[r3] and rc.status == 0 and bool(
+            torch.equal(rc.stream[:total[r3]], streams[r3][:total[r3]]))
+        flags = allgather_int(1 if same else 0)
+        sharded = {"rate_bps": float(r3), "global_tiles": world * n,
+                   "global_stream_words": sum(rc.totals), "rank_word_bases":
+                   [shard.exclusive_word_base(rc.totals, q) for q in range(world)],
+                   "ranks_match_timed_stream": all(flags)}
+        del rc
+
     # ---- end to end through the C ABI with host buffers
     e2e = None if args.skip_e2e else run_e2e(args, hq, params, xt, n, ng, total, dev, world)
 
@@ -332,6 +362,7 @@ def run_ours(args, rank, world):
                           "tiles": n, "l2": "inputs (1 GiB) larger than L2 (129 MB); no flush",
                           "parallelism": f"{world} independent replicas (tile shards)"},
                "roofline": roof, "ops": op_report, "clocks": clk, "e2e": e2e,
+               "codec_status_after_timed_steps": st_timed, "sharded": sharded,
                "gpu_launches": len(order) * args.steps, "fused_scores": fused,
                "fused_attention": attn, "fused_gemm": gemm, "other_workloads": extra,
                "cpu_baseline": cpu, "source_hash": source_hash(),
@@ -560,6 +591,47 @@ def _time_codec(hq, p, xt, n, dev, reps=5):
     return res[0], res[1], tot * 32.0 / (n * 128)
 
 
+# Per-dimension mean squared error of a uniform point of the Voronoi cell of
+# each embedded lattice, G(Lambda) det(Lambda)^(2/n), in lattice units (the
+# HyperQuant summary, Method 2: lower normalized second moment, less
+# distortion at a fixed rate; G from Conway & Sloane's table of second
+# moments): Z 1/12; D4 G = 0.0766032, det 2; 2E8 G = 929/12960, det 2^8;
+# A2 (minimal distance 1) G = 5/(36 sqrt 3), det sqrt(3)/2, i.e. 5/72.
+CELL_MSE = {"Z": 1.0 / 12.0, "D4": 0.0766032 * 2 ** 0.5, "E8": 929.0 / 12960.0 * 4.0,
+            "A2": 5.0 / 72.0}
+
+
+def _distortion(hq, p, xt, n, dev, alpha):
+    """Measured distortion of the codec on xt: the whole input is coded and
+    decoded to fp32 by the library, and the squared error against the bf16
+    input is summed on the GPU (float64 accumulation, 32 Mi-element chunks).
+    Returns (per-dimension MSE in input units, the same x alpha^2 = lattice
+    units)."""
+    import torch
+    ng = hq.hq_num_groups(n)
+    offs = torch.zeros(ng + 1, dtype=torch.int64, device=dev)
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert hq.hq_encode(p, xt, n, None, 0, offs, ws, st) == 0
+    tot = int(offs[-1].item())
+    buf = torch.empty(tot + 1, dtype=torch.int32, device=dev)
+    st.zero_()                                   # the size query flags the zero capacity
+    assert hq.hq_encode(p, xt, n, buf, tot, offs, ws, st) == 0
+    out = torch.empty((n, 128), dtype=torch.float32, device=dev)
+    assert hq.hq_decode(p, buf, tot, offs, n, out, hq.HQ_OUT_F32, st) == 0
+    torch.cuda.synchronize()
+    if int(st.item()):
+        raise RuntimeError(f"status {hq.hq_status_string(int(st.item()))}")
+    xs = xt.view(torch.bfloat16)
+    acc = torch.zeros((), dtype=torch.float64, device=dev)
+    step = 1 << 18
+    for t0 in range(0, n, step):
+        d = out[t0:t0 + step] - xs[t0:t0 + step].float()
+        acc += (d.double() ** 2).sum()
+    mse = float(acc.item()) / (n * 128)
+    return mse, mse * float(alpha) ** 2
+
+
 def run_extra_workloads(hq, I, cal, dev):
     """The other stand-in workloads, timed beside the step: the four
     Llama-3.1-8B-shaped weight matrices (E8, no dither, 3/4/5 bps, one call
@@ -600,12 +672,28 @@ def run_extra_workloads(hq, I, cal, dev):
         for rate, c in cal["long_context"].get(name, {}).items():
             p = hq.make_params(lat, c["k"], c["alpha"], 1, L["dither_seed"], lsigns, 1 << 40)
             e, d, bps = _time_codec(hq, p, xt, n, dev)
+            mse_x, mse_l = _distortion(hq, p, xt, n, dev, c["alpha"])
             lc[f"{name}@{rate}"] = {"encode_ms": round(e, 4), "decode_ms": round(d, 4),
                                     "encode_GBps_bf16eq": round(2.0 * n * 128 / (e * 1e-3) / 1e9, 1),
                                     "decode_GBps_bf16eq": round(2.0 * n * 128 / (d * 1e-3) / 1e9, 1),
-                                    "realized_bps": round(bps, 4)}
+                                    "realized_bps": round(bps, 4),
+                                    "mse": round(mse_l, 6), "mse_pred": round(CELL_MSE[name], 6),
+                                    "mse_over_pred": round(mse_l / CELL_MSE[name], 5),
+                                    "mse_input_units": float(f"{mse_x:.6g}")}
+    order = {}
+    for rate in ("1.7", "2.0", "2.5", "3.0"):
+        got = [(lc[f"{nm}@{rate}"]["mse_input_units"], nm) for nm in ("E8", "D4", "A2", "Z")
+               if f"{nm}@{rate}" in lc]
+        order[rate] = {"by_distortion": [nm for _, nm in sorted(got)],
+                       "E8<D4<A2<Z": [nm for _, nm in sorted(got)] == ["E8", "D4", "A2", "Z"]}
     out["long_context"] = {"workload": "one layer's K and V, 8 heads x 131072 tokens (512 MiB bf16), "
-                                       "dither on", **lc}
+                                       "dither on",
+                           "mse_note": "mse = alpha^2 x per-dimension mean squared error of the fp32 "
+                                       "decode against the bf16 input (lattice units); mse_pred = "
+                                       "G(Lambda) det^(2/n) of the lattice's Voronoi cell; "
+                                       "mse_input_units = the distortion itself, compared across "
+                                       "lattices at each rate",
+                           **lc, "distortion_order": order}
     return out
 
 
@@ -669,6 +757,18 @@ def main():
     ap.add_argument("--skip-fused", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch this script under torchrun on this node
+        import socket
+        import subprocess
+        sk = socket.socket()
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+        sk.close()
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr=127.0.0.1",
+               f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -88,11 +88,11 @@ enum { HQ_OUT_BF16 = 0, HQ_OUT_F32 = 1 };
  *                      predecessor in the encoder's cross-block scan, after
  *                      which HQ_ERR_TIMEOUT is raised.
  *   flags              bit 0 (HQ_FLAG_WORKSPACE_READY): the caller has zeroed
- *                      the encode workspace itself; hq_encode skips its memset
- *                      and the encoder blocks take their groups from the
- *                      workspace's ticket counter (one atomic per block)
- *                      rather than from their launch index; the output is
- *                      the same.
+ *                      the encode workspace itself and hq_encode skips its
+ *                      memset; the output is the same.  (Encoder blocks
+ *                      always take their groups from the workspace's ticket
+ *                      counter, one atomic per block, so that the cross-block
+ *                      scan progresses whatever order blocks start in.)
  *   d_rot              NULL, or device [n_segments][128][128] fp32 row-major
  *                      per-layer dense rotations R (Method 3-4: a full
  *                      Haar-uniform QJL matrix instead of the +-1 diagonal):
@@ -302,7 +302,10 @@ int hq_decode_gemm(const hq_params *p, const uint32_t *d_w_stream, uint64_t w_wo
  *   n_tiles > HQ_NOALLOC_MAX_TILES returns HQ_ERR_INVALID, nothing launched.
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture.
+ *   first call before any stream capture.  The cached address belongs to the
+ *   device's current primary context: after cudaDeviceReset (or anything else
+ *   that destroys that context) the address is stale, so do not call this
+ *   entry point again in that process.
  *   All calls on a device share the one scratch array: calls that may overlap
  *   on the GPU (different streams without ordering between them) race and
  *   corrupt each other's scan; serialise them (one stream, or events).
@@ -315,6 +318,14 @@ int hq_encode_noalloc(const hq_params *p, const uint16_t *d_x, int64_t n_tiles,
  * (Salmon et al., SC'11) with key (seed lo, seed hi) and counter
  * (segment lo, segment hi, 0, 0x5349474E).  out[4] is host memory. */
 void hq_make_signs(uint64_t seed, uint64_t segment, uint32_t out[4]);
+
+/* Host: the sign mask of one layer of a KV cache, D XOR S_layer -- the random
+ * diagonal D of the transform (Method 1, drawn once per model from seed_d,
+ * segment 0) composed with the per-layer +-1 rotation S_layer (Method 4,
+ * drawn from seed_s with the layer as segment).  Both are diagonal and act
+ * before H, so they compose into one mask: out[i] = hq_make_signs(seed_d,
+ * 0)[i] ^ hq_make_signs(seed_s, layer)[i].  out[4] is host memory. */
+void hq_make_layer_signs(uint64_t seed_d, uint64_t seed_s, uint64_t layer, uint32_t out[4]);
 
 /* Host: a static, human-readable name for a status value or bit set. */
 const char *hq_status_string(int status);

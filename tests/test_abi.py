@@ -42,6 +42,9 @@ def test_library_exports_every_declared_symbol(hqlib):
 def test_host_entry_points(hqlib, oracle):
     for seed, seg in ((0, 0), (20, 0), (21, 31), (2**64 - 1, 2**40 + 3)):
         assert hqlib.hq_make_signs(seed, seg) == [int(v) for v in oracle.make_signs(seed, seg)]
+    for sd, ss, layer in ((20, 21, 0), (20, 21, 31), (1, 2**63 + 5, 7)):
+        want = oracle.make_signs(sd, 0) ^ oracle.make_signs(ss, layer)
+        assert hqlib.hq_make_layer_signs(sd, ss, layer) == [int(v) for v in want]
     assert hqlib.hq_num_groups(0) == 0
     assert hqlib.hq_num_groups(1) == 1 and hqlib.hq_num_groups(32) == 1
     assert hqlib.hq_num_groups(33) == 2
@@ -50,6 +53,15 @@ def test_host_entry_points(hqlib, oracle):
     assert hqlib.hq_decode_qk_workspace_bytes(16, 32) == 16 * 32 * 128 * 4
     assert hqlib.hq_status_string(8) == "corrupt stream"
     assert hqlib.hq_status_string(0) == "ok"
+
+
+def test_noalloc_limit_fits_the_built_in_scratch(hqlib):
+    # the encoder workspace of the largest call hq_encode_noalloc accepts must
+    # fit the ~1 MiB array compiled into the library (8 bytes of header plus 8
+    # per 32-tile block, rounded up to 256 bytes)
+    need = hqlib.hq_encode_workspace_bytes(hqlib.HQ_NOALLOC_MAX_TILES)
+    assert need <= ((8 + 8 * (hqlib.HQ_NOALLOC_MAX_TILES // 32)) + 255) // 256 * 256
+    assert need <= (1 << 20) + 256
 
 
 def test_params_layout(hqlib):

@@ -3,8 +3,9 @@
 Codes, bitstreams and group indices must be bit-identical; decoded fp32 must
 be within 1e-5 relative (per tile, l2) and is expected bit-identical; bf16
 output must be bit-identical.  Sizes span several blocks of 128 tiles and
-ragged tails; full-size workloads are checked on sampled groups, each
-re-encoded by the oracle from the same input tiles."""
+ragged tails; the full-size workloads (KV cache, weight matrices, the
+long-context sweep, the fused-scores keys) are compared whole: every stream
+word, every index entry and every bf16 decoded value."""
 import numpy as np
 import pytest
 import torch
@@ -226,9 +227,9 @@ def test_lookback_timeout_is_reported(hq, oracle):
 
 
 def test_prepared_workspace_codes_identically(hq, oracle):
-    """With HQ_FLAG_WORKSPACE_READY the blocks take their groups from the
-    (caller-zeroed) ticket counter instead of their launch index: the stream,
-    index and status are the same bit for bit."""
+    """With HQ_FLAG_WORKSPACE_READY the library skips its workspace memset and
+    the blocks take their groups from the caller-zeroed ticket counter: the
+    stream, index and status are the same bit for bit."""
     rng = np.random.default_rng(6)
     x = _rand_bits(rng, 777)
     c = Case(x, 8, 2, 2.0, 1, 12, oracle.make_signs(6, 0), 1 << 40)
@@ -269,26 +270,37 @@ def test_invalid_arguments(hq, oracle):
 
 
 # ---------------------------------------------------------------- full-size workloads
-def _sampled_groups(hq, oracle, x_dev, n, lattice, k, alpha, dither, seed, mask_of_tile,
-                    stream, offsets, groups, check_decode=True, out_dev=None):
-    """Re-encode sampled groups with the oracle and compare words (and decode)."""
-    offs = offsets.cpu().numpy().view(np.uint64)
-    for g in groups:
-        t0, t1 = 32 * g, min(32 * g + 32, n)
-        xb = x_dev[t0:t1].cpu().numpy().view(np.uint16)
-        P = oracle.make_params(lattice, k, alpha, dither, seed, mask_of_tile(t0), 1 << 40, t0)
-        ref = oracle.encode(P, xb)
-        w0, w1 = int(offs[g]), int(offs[g + 1])
-        assert w1 - w0 == ref["total_words"], g
-        assert (u32(stream[w0:w1]) == ref["stream"]).all(), g
-        if check_decode:
-            d = oracle.decode(P, ref["stream"], ref["offsets"], t1 - t0, out="bf16")
-            got = out_dev[t0:t1].cpu().view(torch.int16).numpy().view(np.uint16)
-            assert (got == d["out"]).all(), g
+def _whole(hq, oracle, xt, n, P, p, decode=True):
+    """Encode the whole workload on both sides and compare every word of the
+    stream, every index entry and the status; then decode the whole stream to
+    bf16 on both sides and compare every value.  Returns (stream, offsets,
+    total) of the GPU encode."""
+    xb = xt.cpu().numpy().view(np.uint16).reshape(-1, 128)
+    ref = oracle.encode(P, xb)
+    stream, offsets, status, total, _ = gpu_encode(hq, p, xt, n)
+    assert status == ref["status"] == 0
+    assert total == ref["total_words"]
+    assert (offsets.cpu().numpy().view(np.uint64) == ref["offsets"]).all()
+    s = u32(stream)
+    assert (s[:total] == ref["stream"][:total]).all()
+    assert (s[total:] == 0xFFFFFFFF).all()
+    del xb, s
+    if decode:
+        out, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_BF16)
+        assert st == 0
+        got = out.cpu().view(torch.int16).numpy().view(np.uint16)
+        del out
+        dref = oracle.decode(P, ref["stream"], ref["offsets"], n, out="bf16")
+        assert dref["status"] == 0
+        assert np.array_equal(got, dref["out"])
+    return stream, offsets, total
 
 
 @pytest.mark.parametrize("rate", ["2.0", "3.0"])
-def test_kv_cache_8b_full_size_sampled(hq, oracle, rate):
+def test_kv_cache_8b_whole(hq, oracle, rate):
+    """The Llama-3.1-8B-shaped KV cache (32 layers x K,V x 8 heads x 8192
+    tokens, per-layer sign rotation, dither, E8): the whole stream, index and
+    bf16 decode equal the oracle's; the realized rate is within 0.01 bps."""
     from weights_hq_encode_gb300 import inputs as I
     C = I.KV8B
     cal = calibration()["kv_cache_8b"]["E8"][rate]
@@ -299,81 +311,67 @@ def test_kv_cache_8b_full_size_sampled(hq, oracle, rate):
     tps = C["kv_heads"] * C["tokens"]
     signs = torch.from_numpy(seg.view(np.int32).copy()).cuda()
     p = hq.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seed"], signs, tps)
+    P = oracle.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seed"], seg, tps)
     xt = hq.as_tiles(x)
-    stream, offsets, status, total, _ = gpu_encode(hq, p, xt, n)
-    assert status == 0
+    del x
+    stream, offsets, total = _whole(hq, oracle, xt, n, P, p)
     bps = (total * 32 - 15.5 * hq.hq_num_groups(n)) / (n * 128)
     assert abs(bps - float(rate)) < 0.01, bps
-    out, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_BF16)
+    # fp32 decode of sampled groups is within 1e-5 (and in practice equal to) the oracle's
+    outf, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_F32)
     assert st == 0
     rng = np.random.default_rng(int(float(rate) * 10))
-    ng = hq.hq_num_groups(n)
-    groups = sorted(set([0, 1, ng - 1] + rng.integers(0, ng, 40).tolist()))
-    _sampled_groups(hq, oracle, xt, n, 8, cal["k"], cal["alpha"], 1, C["dither_seed"],
-                    lambda t0: seg[t0 // tps].reshape(1, 4), stream, offsets, groups,
-                    out_dev=out)
-    # fp32 decode of a sample is within 1e-5 of the oracle's
-    del out
-    outf, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_F32)
-    for g in groups[:6]:
+    for g in [0, hq.hq_num_groups(n) - 1] + rng.integers(0, hq.hq_num_groups(n), 6).tolist():
         t0 = 32 * g
         xb = xt[t0:t0 + 32].cpu().numpy().view(np.uint16)
-        P = oracle.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seed"],
-                               seg[t0 // tps].reshape(1, 4), 1 << 40, t0)
-        ref = oracle.encode(P, xb)
-        d = oracle.decode(P, ref["stream"], ref["offsets"], 32)
+        Pg = oracle.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seed"],
+                                seg[t0 // tps].reshape(1, 4), 1 << 40, t0)
+        ref = oracle.encode(Pg, xb)
+        d = oracle.decode(Pg, ref["stream"], ref["offsets"], xb.shape[0])
         assert np.all(_rel_l2_per_tile(outf[t0:t0 + 32].cpu().numpy(), d["out"]) <= 1e-5)
 
 
-def test_weights_8b_sampled(hq, oracle):
+@pytest.mark.parametrize("rate", ["3.0", "4.0", "5.0"])
+def test_weights_8b_whole(hq, oracle, rate):
+    """The four Llama-3.1-8B linear-weight shapes at 3, 4 and 5 bps (no
+    dither, one sign mask): whole streams, indexes and bf16 decodes."""
     from weights_hq_encode_gb300 import inputs as I
     C = I.WEIGHTS8B
     cal = calibration()["weights_8b"]["E8"]
     mask = oracle.make_signs(C["sign_seed"], 0).reshape(1, 4)
     signs = torch.from_numpy(mask.view(np.int32).copy()).cuda()
-    for rate in ("3.0", "4.0", "5.0"):
-        for i in range(len(C["shapes"])):
-            c = cal[rate][i]
-            w = I.weight_matrix(i, "cuda")
-            xt = hq.as_tiles(w)
-            n = xt.shape[0]
-            p = hq.make_params(8, c["k"], c["alpha"], 0, 0, signs, 1 << 40)
-            stream, offsets, status, total, _ = gpu_encode(hq, p, xt, n)
-            assert status == 0
-            bps = (total * 32 - 15.5 * hq.hq_num_groups(n)) / (n * 128)
-            assert abs(bps - float(rate)) < 0.01, (rate, i, bps)
-            out, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_BF16)
-            assert st == 0
-            rng = np.random.default_rng(i)
-            ng = hq.hq_num_groups(n)
-            groups = sorted(set([0, ng - 1] + rng.integers(0, ng, 6).tolist()))
-            _sampled_groups(hq, oracle, xt, n, 8, c["k"], c["alpha"], 0, 0, lambda t0: mask,
-                            stream, offsets, groups, out_dev=out)
-            del w, xt, stream, out
+    for i in range(len(C["shapes"])):
+        c = cal[rate][i]
+        xt = hq.as_tiles(I.weight_matrix(i, "cuda"))
+        n = xt.shape[0]
+        p = hq.make_params(8, c["k"], c["alpha"], 0, 0, signs, 1 << 40)
+        P = oracle.make_params(8, c["k"], c["alpha"], 0, 0, mask, 1 << 40)
+        stream, offsets, total = _whole(hq, oracle, xt, n, P, p)
+        bps = (total * 32 - 15.5 * hq.hq_num_groups(n)) / (n * 128)
+        assert abs(bps - float(rate)) < 0.01, (rate, i, bps)
+        del xt, stream, offsets
 
 
-def test_long_context_sweep_sampled(hq, oracle):
+@pytest.mark.parametrize("name,lat", [("Z", 1), ("A2", 2), ("D4", 4), ("E8", 8)])
+def test_long_context_sweep_whole(hq, oracle, name, lat):
+    """One layer's K and V of 131072 tokens, dither on, every rate of the
+    sweep (1.7, 2.0, 2.5, 3.0 bps): whole streams, indexes and bf16 decodes."""
     from weights_hq_encode_gb300 import inputs as I
     C = I.LONGCTX
     cal = calibration()["long_context"]
-    x = I.long_context_layer("cuda")
-    xt = hq.as_tiles(x)
+    xt = hq.as_tiles(I.long_context_layer("cuda"))
     n = xt.shape[0]
     mask = (oracle.make_signs(C["sign_seed"], 0) ^ oracle.make_signs(C["layer_sign_seed"], 0))
     mask = mask.reshape(1, 4)
     signs = torch.from_numpy(mask.view(np.int32).copy()).cuda()
-    for name, lat in (("Z", 1), ("A2", 2), ("D4", 4), ("E8", 8)):
-        for rate in ("1.7", "2.0", "2.5", "3.0"):
-            c = cal[name][rate]
-            p = hq.make_params(lat, c["k"], c["alpha"], 1, C["dither_seed"], signs, 1 << 40)
-            stream, offsets, status, total, _ = gpu_encode(hq, p, xt, n)
-            assert status == 0
-            bps = (total * 32 - 15.5 * hq.hq_num_groups(n)) / (n * 128)
-            assert abs(bps - float(rate)) < 0.01, (name, rate, bps)
-            ng = hq.hq_num_groups(n)
-            _sampled_groups(hq, oracle, xt, n, lat, c["k"], c["alpha"], 1, C["dither_seed"],
-                            lambda t0: mask, stream, offsets, [0, ng // 2, ng - 1],
-                            check_decode=False)
+    for rate in ("1.7", "2.0", "2.5", "3.0"):
+        c = cal[name][rate]
+        p = hq.make_params(lat, c["k"], c["alpha"], 1, C["dither_seed"], signs, 1 << 40)
+        P = oracle.make_params(lat, c["k"], c["alpha"], 1, C["dither_seed"], mask, 1 << 40)
+        stream, offsets, total = _whole(hq, oracle, xt, n, P, p)
+        bps = (total * 32 - 15.5 * hq.hq_num_groups(n)) / (n * 128)
+        assert abs(bps - float(rate)) < 0.01, (name, rate, bps)
+        del stream, offsets
 
 
 # ---------------------------------------------------------------- fused scores
@@ -430,6 +428,12 @@ def test_decode_qk_full_size_sampled(hq, oracle):
     K, q, p, stream, offsets, total, scores, mask, cal = _scores_case(
         hq, oracle, C["kv_heads"], C["tokens"], C["batch"], C["q_heads"], C["dither_seeds"][0])
     n = C["kv_heads"] * C["tokens"]
+    # the whole compressed K stream and index equal the oracle's
+    P = oracle.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seeds"][0], mask, n)
+    ref = oracle.encode(P, hq.as_tiles(K).cpu().numpy().view(np.uint16))
+    assert total == ref["total_words"]
+    assert (u32(stream[:total]) == ref["stream"]).all()
+    assert (offsets.cpu().numpy().view(np.uint64) == ref["offsets"]).all()
     rng = np.random.default_rng(9)
     ng = hq.hq_num_groups(n)
     qb = q.cpu().view(torch.int16).numpy().view(np.uint16)

@@ -1,8 +1,9 @@
-"""Multi-rank path on CPU (gloo, world size 2): each rank codes its
-group-aligned tile range with tile_base = its first tile; the per-rank
-streams, joined through one all-gather of word totals, equal the stream of one
-call over the whole tensor, bit for bit (the per-rank coder here is the CPU
-oracle; on GPUs each rank runs hq_encode on its own device)."""
+"""Multi-rank path on CPU (gloo, world size 2): shard.code_rank -- the rank
+function bench.py runs on GPUs -- codes each rank's group-aligned tile range
+with tile_base = its first tile; the per-rank streams, joined through one
+all-gather of word totals, equal the stream of one call over the whole
+tensor, bit for bit.  Only the device call is replaced: the CPU oracle codes
+the range here, hq_encode on the rank's GPU in bench.py."""
 import os
 import socket
 
@@ -32,19 +33,27 @@ def _rank_main(rank, world, port, result_path):
         from weights_hq_encode_gb300 import inputs as I, shard
         x = I.bf16_bits(I.tiny_kv()).reshape(-1, 128)
         x = np.concatenate([x, x[:77]])                     # 333 tiles: ragged last group
-        b, e = shard.shard_range(x.shape[0], world, rank)
-        P = O.make_params(8, 2, 1.7, 1, 7, O.make_signs(0, 0), 1 << 40, tile_base=b)
-        enc = O.encode(P, x[b:e], threads=1)
-        totals = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
-        dist.all_gather(totals, torch.tensor([enc["total_words"]], dtype=torch.int64))
-        totals = [int(t.item()) for t in totals]
-        base = shard.exclusive_word_base(totals, rank)
+        def encode_range(b, e):                            # the oracle stands in for hq_encode
+            P = O.make_params(8, 2, 1.7, 1, 7, O.make_signs(0, 0), 1 << 40, tile_base=b)
+            enc = O.encode(P, x[b:e], threads=1)
+            return enc["stream"], enc["offsets"].tolist(), enc["total_words"], enc["status"]
+
+        def allgather_int(v):                              # the one exchange
+            totals = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
+            dist.all_gather(totals, torch.tensor([v], dtype=torch.int64))
+            return [int(t.item()) for t in totals]
+
+        rc = shard.code_rank(x.shape[0], world, rank, encode_range, allgather_int)
+        assert rc.status == 0
         # gather streams and indices (test only: a deployment keeps them sharded)
         objs = [None] * world
-        dist.all_gather_object(objs, (base, enc["stream"].tolist(), enc["offsets"].tolist()))
+        dist.all_gather_object(objs, (rc.word_base, rc.stream.tolist(), rc.offsets,
+                                      rc.global_offsets()))
         if rank == 0:
-            stream = [w for _, s, _ in sorted(objs, key=lambda o: o[0]) for w in s]
-            offsets = shard.merge_offsets([o for _, _, o in objs])
+            stream = [w for _, s, _, _ in sorted(objs, key=lambda o: o[0]) for w in s]
+            offsets = shard.merge_offsets([o for _, _, o, _ in objs])
+            glob = [v for _, _, _, g in objs[:-1] for v in g[:-1]] + objs[-1][3]
+            assert glob == offsets
             np.savez(result_path, stream=np.array(stream, np.uint64), offsets=np.array(offsets, np.uint64))
     finally:
         dist.destroy_process_group()

@@ -145,7 +145,6 @@ int encode_impl(const hq_params *p, const uint16_t *d_x, int64_t n_tiles, uint32
   a.spins = p->lookback_spins ? p->lookback_spins : kDefaultSpins;
   a.payload_bits = d_bits;
   a.rot = p->d_rot;
-  a.use_ticket = (p->flags & HQ_FLAG_WORKSPACE_READY) ? 1 : 0;
   if (!(p->flags & HQ_FLAG_WORKSPACE_READY)) {
     if (cudaMemsetAsync(d_ws, 0, hq_encode_workspace_bytes(n_tiles), st) != cudaSuccess)
       return HQ_ERR_CUDA;
@@ -452,6 +451,13 @@ void hq_make_signs(uint64_t seed, uint64_t segment, uint32_t out[4]) {
   out[1] = c1;
   out[2] = c2;
   out[3] = c3;
+}
+
+void hq_make_layer_signs(uint64_t seed_d, uint64_t seed_s, uint64_t layer, uint32_t out[4]) {
+  uint32_t d[4], sl[4];
+  hq_make_signs(seed_d, 0, d);
+  hq_make_signs(seed_s, layer, sl);
+  for (int i = 0; i < 4; ++i) out[i] = d[i] ^ sl[i];
 }
 
 const char *hq_status_string(int status) {

@@ -240,17 +240,15 @@ encode_kernel(EncodeArgs a) {
 
   const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
   uint64_t *state = reinterpret_cast<uint64_t *>(a.ws) + 1;
-  // This block's group.  Blocks start in index order, so every predecessor
-  // of a waiting block has started and the look-back always progresses; with
-  // a caller-prepared workspace the group comes from its ticket counter
-  // instead (a counter set ahead leaves groups unprocessed, which the
-  // bounded waits turn into HQ_ERR_TIMEOUT).
-  uint32_t g = blockIdx.x;
-  if (a.use_ticket) {                            // uniform over the grid
-    if (tid == 0) s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
-    __syncthreads();
-    g = s_ticket;
-  }
+  // This block's group comes from the workspace's ticket counter, not from
+  // the launch index: a block holding ticket g knows that the blocks holding
+  // tickets 0 .. g-1 are already running, so its look-back always makes
+  // progress whatever order the hardware starts blocks in.  (A counter set
+  // ahead by the caller leaves groups unprocessed, which the bounded waits
+  // turn into HQ_ERR_TIMEOUT.)
+  if (tid == 0) s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
+  __syncthreads();
+  const uint32_t g = s_ticket;
   if (tid == 0) s_flags = 0u;
   if (g >= a.n_blocks) return;                   // only with a counter set ahead
   const int k = K >= 0 ? K : a.rice_k;

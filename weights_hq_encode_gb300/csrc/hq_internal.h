@@ -39,7 +39,6 @@ struct EncodeArgs {
   int dither;
   uint32_t spins;
   unsigned long long *payload_bits;   // non-null: add each group's Rice bits here
-  int use_ticket;           // groups from the workspace's ticket counter, not blockIdx
   const float *rot;         // nullptr, or [n_segments][128][128] row-major rotations
 };
 

@@ -11,15 +11,17 @@
 
 #include <cuda_runtime.h>
 
+#include "hq_device.cuh"
 #include "hq_internal.h"
 
 namespace {
 
-// 8-byte ticket header + 8 bytes of look-back state per index group (one
-// encoder block per group) for HQ_NOALLOC_MAX_TILES tiles, rounded up to 256
-// bytes.
+// 8-byte ticket header + 8 bytes of look-back state per encoder block (one
+// block per kGroupTiles tiles, the constant the encoder itself uses) for
+// HQ_NOALLOC_MAX_TILES tiles, rounded up to 256 bytes.
 constexpr size_t kNoallocScratchBytes =
-    ((8 + 8 * (size_t)(HQ_NOALLOC_MAX_TILES / HQ_GROUP_TILES)) + 255) / 256 * 256;
+    ((8 + 8 * (size_t)((HQ_NOALLOC_MAX_TILES + hq::kGroupTiles - 1) / hq::kGroupTiles)) + 255) /
+    256 * 256;
 
 static __device__ __align__(256) unsigned char g_encode_scratch[kNoallocScratchBytes];
 

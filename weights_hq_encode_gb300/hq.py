@@ -23,7 +23,8 @@ HQ_TILE, HQ_GROUP_TILES = 128, 32
 HQ_FLAG_WORKSPACE_READY = 1
 
 EXPORTED = ("hq_num_groups", "hq_encode_workspace_bytes", "hq_encode", "hq_decode",
-            "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs", "hq_status_string",
+            "hq_decode_qk_workspace_bytes", "hq_decode_qk", "hq_make_signs",
+            "hq_make_layer_signs", "hq_status_string",
             "hq_encode_noalloc", "hq_payload_bits", "hq_calibrate",
             "hq_decode_attention_workspace_bytes", "hq_decode_attention",
             "hq_decode_gemm_workspace_bytes", "hq_decode_gemm")
@@ -86,6 +87,8 @@ def _load():
     L.hq_decode_gemm.argtypes = [vp, vp, u64, vp, i64, i64, vp, ctypes.c_int, vp, vp, sz, vp, vp]
     L.hq_make_signs.restype = None
     L.hq_make_signs.argtypes = [u64, u64, vp]
+    L.hq_make_layer_signs.restype = None
+    L.hq_make_layer_signs.argtypes = [u64, u64, u64, vp]
     L.hq_status_string.restype = ctypes.c_char_p
     L.hq_status_string.argtypes = [ctypes.c_int]
     return L
@@ -231,6 +234,12 @@ def hq_make_signs(seed: int, segment: int):
     return [int(v) for v in out]
 
 
+def hq_make_layer_signs(seed_d: int, seed_s: int, layer: int):
+    out = (ctypes.c_uint32 * 4)()
+    _lib.hq_make_layer_signs(seed_d, seed_s, layer, out)
+    return [int(v) for v in out]
+
+
 def hq_status_string(status: int) -> str:
     return _lib.hq_status_string(int(status)).decode()
 
@@ -245,8 +254,7 @@ def signs_tensor(masks, device="cuda") -> torch.Tensor:
 
 def kv_layer_masks(seed_d: int, seed_s: int, layers: int):
     """Per-layer masks D XOR S_layer (Method 1 and 4: two sign diagonals)."""
-    d = hq_make_signs(seed_d, 0)
-    return [[d[i] ^ s for i, s in enumerate(hq_make_signs(seed_s, l))] for l in range(layers)]
+    return [hq_make_layer_signs(seed_d, seed_s, l) for l in range(layers)]
 
 
 def as_tiles(x: torch.Tensor) -> torch.Tensor:
