@@ -510,10 +510,11 @@ float oracle_decode_scale(float alpha) { return (float)(1.0 / ((double)alpha * s
  * the summary fixes neither; u = +0 without dither).  Range rule (reading of
  * "alpha is chosen so that codes fit"): if any y_i is NaN or |y_i| > 2^20 the
  * tile is coded as if x were 0 and ORA_ERR_RANGE is reported. */
-int oracle_tile_codes(const ora_params *P, const uint16_t *x, int64_t t,
-                      int32_t *v) {
+/* The lattice-domain values y of one tile (before the nearest point), with
+ * the range rule applied; returns the range flag. */
+static int tile_y(const ora_params *P, const uint16_t *x, int64_t t, float *y) {
   const uint32_t *m = tile_mask(P, t);
-  float z[TILE], u[TILE], y[TILE], xf[TILE];
+  float z[TILE], u[TILE], xf[TILE];
   for (int i = 0; i < TILE; ++i) xf[i] = bf16_to_float(x[i]);
   if (P->rot) oracle_rotate(tile_rot(P, t), xf, xf);
   for (int i = 0; i < TILE; ++i) z[i] = mask_bit(m, i) ? -xf[i] : xf[i];
@@ -528,6 +529,13 @@ int oracle_tile_codes(const ora_params *P, const uint16_t *x, int64_t t,
   }
   if (flag)
     for (int i = 0; i < TILE; ++i) y[i] = fmaf(0.0f, s, u[i]);
+  return flag;
+}
+
+int oracle_tile_codes(const ora_params *P, const uint16_t *x, int64_t t,
+                      int32_t *v) {
+  float y[TILE];
+  const int flag = tile_y(P, x, t, y);
   if (P->lattice == ORA_E8) {
     for (int b = 0; b < TILE; b += 8) oracle_nearest_e8(y + b, v + b);
   } else if (P->lattice == ORA_D4) {
@@ -883,6 +891,108 @@ int oracle_scores(const float *khat, int n_kv_heads, int64_t n_tokens, const uin
 }
 
 /* Exposed limits so that tests can read the format constants. */
+/* ------------------------------------------------------------------------ */
+/* Diagnostic, no counterpart in the method: how often the E8 coset choice   */
+/* by the fp32 linear identity (oracle_nearest_e8) differs from the plain    */
+/* rule -- both cosets' nearest points by Conway & Sloane's D_n decoder on   */
+/* a = y/2 and a - 1/2, then the two fp32 squared distances summed left to   */
+/* right, the odd coset only when strictly nearer.                            */
+/* ------------------------------------------------------------------------ */
+static void dn8_nearest(const float *b, float *f) {
+  float best = -1.0f;
+  int j = 0, par = 0;
+  for (int i = 0; i < 8; ++i) {
+    f[i] = rintf(b[i]);
+    par ^= ((int64_t)f[i]) & 1;
+    const float d = fabsf(b[i] - f[i]);
+    if (d > best) { best = d; j = i; }
+  }
+  if (par) f[j] += (b[j] >= f[j]) ? 1.0f : -1.0f;
+}
+
+void oracle_e8_plain(const float *y, int32_t *v) {
+  float a[8], a2[8], A[8], B[8];
+  for (int i = 0; i < 8; ++i) { a[i] = 0.5f * y[i]; a2[i] = a[i] - 0.5f; }
+  dn8_nearest(a, A);
+  dn8_nearest(a2, B);
+  float dA = 0.0f, dB = 0.0f;
+  for (int i = 0; i < 8; ++i) {
+    A[i] = 2.0f * A[i];
+    B[i] = 2.0f * B[i] + 1.0f;
+    const float da = y[i] - A[i], db = y[i] - B[i];
+    dA = dA + da * da;
+    dB = dB + db * db;
+  }
+  const float *w = (dB < dA) ? B : A;
+  for (int i = 0; i < 8; ++i) v[i] = (int32_t)w[i];
+}
+
+typedef struct {
+  const ora_params *P;
+  const uint16_t *x;
+  pthread_mutex_t mu;
+  int64_t vectors, differ, coset_differ;
+  double dist_sum, max_abs;   /* sum of exact (double) dist^2(plain) - dist^2(oracle) */
+} census_ctx;
+
+static void census_range(void *c, int64_t b, int64_t e) {
+  census_ctx *C = (census_ctx *)c;
+  int64_t nv = 0, nd = 0, nc = 0;
+  double ds = 0.0, mx = 0.0;
+  float y[TILE];
+  for (int64_t t = b; t < e; ++t) {
+    tile_y(C->P, C->x + t * TILE, t, y);
+    for (int q = 0; q < TILE; q += 8) {
+      int32_t vo[8], vp[8];
+      oracle_nearest_e8(y + q, vo);
+      oracle_e8_plain(y + q, vp);
+      ++nv;
+      if (memcmp(vo, vp, sizeof vo) != 0) {
+        ++nd;
+        if (((vo[0] ^ vp[0]) & 1) != 0) ++nc;
+        double d2o = 0.0, d2p = 0.0;
+        for (int i = 0; i < 8; ++i) {
+          const double eo = (double)y[q + i] - vo[i], ep = (double)y[q + i] - vp[i];
+          d2o += eo * eo;
+          d2p += ep * ep;
+        }
+        ds += d2p - d2o;
+        if (fabs(d2p - d2o) > mx) mx = fabs(d2p - d2o);
+      }
+    }
+  }
+  pthread_mutex_lock(&C->mu);
+  C->vectors += nv;
+  C->differ += nd;
+  C->coset_differ += nc;
+  C->dist_sum += ds;
+  if (mx > C->max_abs) C->max_abs = mx;
+  pthread_mutex_unlock(&C->mu);
+}
+
+/* out[0] = 8-vectors coded, out[1] = vectors whose codes differ between the
+ * two rules, out[2] = of those, vectors whose coset differs; dist[0] = sum
+ * over the differing vectors of the exact squared distance to the plain
+ * rule's point minus that to the oracle's, dist[1] = the largest |.| of one
+ * vector.  E8 only. */
+int oracle_e8_rule_census(const ora_params *P, const uint16_t *x, int64_t n_tiles, int64_t *out,
+                          double *dist, int nthreads) {
+  if (!params_ok(P) || P->lattice != ORA_E8 || n_tiles < 0) return -1;
+  census_ctx C;
+  memset(&C, 0, sizeof C);
+  C.P = P;
+  C.x = x;
+  pthread_mutex_init(&C.mu, NULL);
+  parallel_for(n_tiles, nthreads, census_range, &C);
+  pthread_mutex_destroy(&C.mu);
+  out[0] = C.vectors;
+  out[1] = C.differ;
+  out[2] = C.coset_differ;
+  dist[0] = C.dist_sum;
+  dist[1] = C.max_abs;
+  return 0;
+}
+
 int oracle_group_tiles(void) { return GROUP_TILES; }
 float oracle_range_limit(void) { return RANGE_LIMIT; }
 uint32_t oracle_symbol_limit(void) { return SYMBOL_LIMIT; }

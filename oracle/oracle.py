@@ -93,6 +93,9 @@ def lib():
             L.oracle_encode_scale.argtypes = [ctypes.c_float]
             L.oracle_decode_scale.restype = ctypes.c_float
             L.oracle_decode_scale.argtypes = [ctypes.c_float]
+            L.oracle_e8_rule_census.restype = ctypes.c_int
+            L.oracle_e8_rule_census.argtypes = [vp, vp, i64, vp, vp, ctypes.c_int]
+            L.oracle_e8_plain.argtypes = [vp, vp]
             L.oracle_group_tiles.restype = ctypes.c_int
             L.oracle_range_limit.restype = ctypes.c_float
             L.oracle_symbol_limit.restype = ctypes.c_uint32
@@ -289,3 +292,25 @@ def scores(khat: np.ndarray, n_kv_heads: int, n_tokens: int, q_bf16_bits: np.nda
     if rc != 0:
         raise ValueError("oracle_scores: invalid arguments")
     return out
+
+
+def e8_plain(y) -> np.ndarray:
+    """The plain E8 rule: both cosets by the D_n decoder, fp32 squared
+    distances summed left to right (diagnostic; the codec uses nearest_e8)."""
+    yy = np.ascontiguousarray(y, dtype=np.float32).reshape(8)
+    v = np.zeros(8, np.int32)
+    lib().oracle_e8_plain(_p(yy), _p(v))
+    return v
+
+
+def e8_rule_census(P: Params, x_bf16_bits: np.ndarray, threads: int | None = None) -> dict:
+    """Counts, over every 8-vector the oracle codes from these tiles, where
+    nearest_e8 (fp32 linear identity) and the plain rule disagree."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16).reshape(-1, 128)
+    out = np.zeros(3, np.int64)
+    dist = np.zeros(2, np.float64)
+    if lib().oracle_e8_rule_census(ctypes.byref(P), _p(x), x.shape[0], _p(out), _p(dist),
+                                   threads or default_threads()) != 0:
+        raise ValueError("oracle_e8_rule_census: invalid arguments")
+    return dict(vectors=int(out[0]), differ=int(out[1]), coset_differ=int(out[2]),
+                dist_sum=float(dist[0]), dist_max=float(dist[1]))

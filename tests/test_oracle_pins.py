@@ -165,6 +165,26 @@ def test_e8_nearest_point_brute_force(oracle):
     assert np.mean(np.abs(d_or - d_min) < 1e-12) > 0.999
 
 
+def test_plain_e8_rule_and_census(oracle):
+    """The plain E8 rule (both cosets by the D_n decoder, fp32 squared
+    distances) is a nearest point by brute force too, and where it and the
+    codec's linear identity disagree the census only finds exact-distance
+    near-ties (Method 2, Conway & Sloane's E8 decoder)."""
+    rng = np.random.default_rng(12)
+    y = np.concatenate([rng.standard_normal((2500, 8)) * sc for sc in (0.3, 1.0, 3.0, 30.0)])
+    y = y.astype(np.float32).astype(np.float64)
+    v = np.stack([oracle.e8_plain(r) for r in y])
+    assert _in_2e8(v).all()
+    assert np.all(((v - y) ** 2).sum(-1) <= _brute_e8_min(y) + 1e-4)
+    same = (v == _e8_codes(oracle, y)).all(-1)
+    assert same.mean() > 0.999
+    x = (rng.standard_normal((3000, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    P = oracle.make_params(8, 2, 2.3, 1, 8, oracle.make_signs(4, 0), 1 << 40)
+    c = oracle.e8_rule_census(P, x)
+    assert c["vectors"] == 3000 * 16
+    assert c["differ"] <= 3 and c["dist_max"] <= 1e-4
+
+
 def test_e8_ties_and_translation(oracle):
     # exact ties: equidistant from 0 and a minimal vector, or all-integer inputs
     ties = np.array([[1, 1, 0, 0, 0, 0, 0, 0], [0.5] * 8, [1] * 8, [-1, 1, -1, 1, 0, 0, 0, 0],

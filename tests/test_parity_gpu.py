@@ -331,6 +331,33 @@ def test_kv_cache_8b_whole(hq, oracle, rate):
         assert np.all(_rel_l2_per_tile(outf[t0:t0 + 32].cpu().numpy(), d["out"]) <= 1e-5)
 
 
+@pytest.mark.parametrize("rate", ["2.0", "3.0"])
+def test_kv_cache_8b_e8_rule_census(oracle, rate):
+    """On the KV-cache inputs, how often the codec's E8 coset test (an fp32
+    evaluation of the exact linear identity for the difference of the two
+    squared distances) and the plain rule (the two fp32 squared distances
+    summed left to right) pick different points: only at exact-distance
+    near-ties, and rarely.  The inputs are the GPU-drawn cache, read back."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weights_hq_encode_gb300 import inputs as I
+    from weights_hq_encode_gb300 import hq
+    C = I.KV8B
+    cal = calibration()["kv_cache_8b"]["E8"][rate]
+    x = I.kv_cache_8b("cuda")
+    xb = x.reshape(-1, 128).view(torch.int16).cpu().numpy().view(np.uint16)
+    del x
+    masks = hq.kv_layer_masks(C["sign_seed"], C["layer_sign_seed"], C["layers"])
+    seg = np.array([masks[l] for l in range(C["layers"]) for _ in (0, 1)], np.uint32)
+    P = oracle.make_params(8, cal["k"], cal["alpha"], 1, C["dither_seed"], seg,
+                           C["kv_heads"] * C["tokens"])
+    c = oracle.e8_rule_census(P, xb)
+    print(f"\nE8 rule census, KV cache at {rate} bps: {c}")
+    assert c["vectors"] == xb.shape[0] * 16
+    assert c["differ"] <= 1e-6 * c["vectors"]
+    assert c["dist_max"] <= 1e-3
+
+
 @pytest.mark.parametrize("rate", ["3.0", "4.0", "5.0"])
 def test_weights_8b_whole(hq, oracle, rate):
     """The four Llama-3.1-8B linear-weight shapes at 3, 4 and 5 bps (no

@@ -21,7 +21,9 @@ decode_kernel(DecodeArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
   // D_i * s_dec of the block's first segment, coordinates 16r + j and 16r + j + 8
-  // side by side (the pairs a lane holds after the transform)
+  // side by side (the pairs a lane holds after the transform); lane r's block
+  // c (j = 2c, 2c + 1) at 8c + r, so the 8 lanes of a tile read 128
+  // contiguous bytes
   __shared__ float4 s_scale[kTile / 4];
   __shared__ __align__(16) float s_tr[kGroupTiles * kTrTile];  // transposes of the transform
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
@@ -29,7 +31,8 @@ decode_kernel(DecodeArgs a) {
   const int64_t seg0 = div_by(g * kGroupTiles, a.tiles_per_segment, a.seg_shift);
   if (tid < kTile) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 5));
-    reinterpret_cast<float *>(s_scale)[16 * (tid >> 4) + 2 * (tid & 7) + ((tid >> 3) & 1)] =
+    reinterpret_cast<float *>(s_scale)[32 * ((tid & 7) >> 1) + 4 * (tid >> 4) + 2 * (tid & 1) +
+                                       ((tid >> 3) & 1)] =
         __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
   }
   constexpr int kRS = kTile + 4;                 // row stride of the rotation's operands
@@ -50,7 +53,7 @@ decode_kernel(DecodeArgs a) {
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const float4 sc = s_scale[4 * r + c];
+        const float4 sc = s_scale[8 * c + r];
         upk2(mul2(pk2(e[2 * c], e[2 * c + 8]), pk2(sc.x, sc.y)), e[2 * c], e[2 * c + 8]);
         upk2(mul2(pk2(e[2 * c + 1], e[2 * c + 9]), pk2(sc.z, sc.w)), e[2 * c + 1], e[2 * c + 9]);
       }

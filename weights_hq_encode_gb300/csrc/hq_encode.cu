@@ -235,7 +235,9 @@ encode_kernel(EncodeArgs a) {
   __shared__ uint64_t s_base, s_words;
   __shared__ uint32_t s_ticket, s_flags;
   __shared__ int s_ok;
-  __shared__ uint4 s_signx[kTile / 8];          // sign XOR words of the first segment
+  // sign XOR words of the first segment; lane r's two 16-byte blocks sit at
+  // r and 8 + r, so the 8 lanes of a tile read 128 contiguous bytes
+  __shared__ uint4 s_signx[kTile / 8];
 
 
   const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
@@ -273,7 +275,8 @@ encode_kernel(EncodeArgs a) {
   }
   if (tid < kTile / 2) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
-    reinterpret_cast<uint32_t *>(s_signx)[tid] =
+    // word tid = pair q = tid & 7 of lane r = tid >> 3
+    reinterpret_cast<uint32_t *>(s_signx)[32 * ((tid & 7) >> 2) + 4 * (tid >> 3) + (tid & 3)] =
         (((mword >> (2 * (tid & 15))) & 3u) * 0x40008000u) & 0x80008000u;
   }
   __syncthreads();
@@ -338,7 +341,7 @@ encode_kernel(EncodeArgs a) {
       z[4 * c + 2] = q.z;
       z[4 * c + 3] = q.w;
     }
-    const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
+    const uint4 s0 = s_signx[r], s1 = s_signx[8 + r];
     const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {                // bf16-pair sign bits 15 / 31 -> fp32 bit 31
@@ -348,7 +351,7 @@ encode_kernel(EncodeArgs a) {
   } else if (valid) {
     uint32_t sw[8];
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
-      const uint4 s0 = s_signx[2 * r], s1 = s_signx[2 * r + 1];
+      const uint4 s0 = s_signx[r], s1 = s_signx[8 + r];
       sw[0] = s0.x; sw[1] = s0.y; sw[2] = s0.z; sw[3] = s0.w;
       sw[4] = s1.x; sw[5] = s1.y; sw[6] = s1.z; sw[7] = s1.w;
     } else {
