@@ -214,14 +214,6 @@ __device__ __forceinline__ void fwht128_t8_smem(float x[16], float *tile, int r)
                  : "memory");
   __syncwarp();
 }
-// Coordinate 16r + 8v + c of the transformed tile (after fwht128_t8_smem).
-__device__ __forceinline__ float tr_coord(const float *tile, int r, int v, int c) {
-  float f;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f)
-               : "r"((uint32_t)__cvta_generic_to_shared(tile + 2 * r + v) + 4u * kTrRow * c)
-               : "memory");
-  return f;
-}
 // The whole transform back in registers: x[j], x[j + 8] = coordinates 16r + j, 16r + j + 8.
 __device__ __forceinline__ void fwht128_t8(float x[16], float *tile, int r) {
   fwht128_t8_smem(x, tile, r);
@@ -318,8 +310,9 @@ __device__ __forceinline__ float mulsign(float a, float e) {
 // a grid point u0 of a box that tiles space by the lattice, minus Q(u0).
 // The boxes are centred, so Q(u0) needs the general rounding on one
 // coordinate per vector only; the rest of the nearest-point rule is the same
-// as nearest_e8 / nearest_d4 (largest-error / smallest-error coordinate,
-// first index among equals, the odd E8 coset only when strictly nearer).
+// as in quantize_fold16_e8 / nearest_d4 (largest-error / smallest-error
+// coordinate, first index among equals, the odd E8 coset only when strictly
+// nearer).
 template <int LAT, class Keys>
 __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t j, float u[8]) {
   const uint4 w4 = dither_words(key, tile, j);
@@ -404,68 +397,14 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
 }
 
 // ---------------------------------------------------------------- fold / strip
-// Symbols of one 8-coordinate group (Method 3).  E8: p = coset, w = (v - p)/2,
-// r = parity(w0..w6), t = (w7 - r)/2; s_i = 2Z(w_i) + p, s_7 = 4Z(t) + 2r + p.
-// D4 (two vectors): r = parity(v0+v1+v2), t = (v3 - r)/2, s_3 = 2Z(t) + r.
+// Nearest point and symbols of one 8-coordinate group (Method 2 and 3) for
+// D4, A2 and Z (E8: quantize_fold16_e8).  D4 (two vectors):
+// r = parity(v0+v1+v2), t = (v3 - r)/2, s_3 = 2Z(t) + r; A2 (four pairs):
+// s_0 = Z(n), s_1 = 2Z((m - p)/2) + p with p = n mod 2; Z: s = Z(v).
 template <int LAT>
 __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) {
-  if (LAT == 8) {
-    // nearest point of 2E8 (nearest_e8 rule), kept as floats v_i = F_i + c_i
-    float F[8], e[8];
-    uint32_t par = 0, sx = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float T = __fadd_rn(y[i], kMagic2);
-      F[i] = __fsub_rn(T, kMagic2);
-      e[i] = __fsub_rn(y[i], F[i]);
-      par ^= __float_as_uint(T);
-      sx ^= __float_as_uint(e[i]);
-    }
-    const uint32_t pA = par & 1u, pB = pA ^ (sx >> 31);
-    float S = fabsf(e[0]), mx = fabsf(e[0]), mn = fabsf(e[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) {
-      const float ai = fabsf(e[i]);
-      S = __fadd_rn(S, ai);
-      mx = fmaxf(mx, ai);
-      mn = fminf(mn, ai);
-    }
-    float D = __fmaf_rn(-2.0f, S, pA ? 4.0f : 8.0f);
-    if (pB) D = __fmaf_rn(4.0f, mn, D);
-    if (pA) D = __fmaf_rn(4.0f, mx, D);
-    const bool odd = D < 0.0f;
-    const float m = odd ? mn : mx;
-    bool open = odd ? (pB != 0u) : (pA != 0u);
-    // even coset: c = 0, the fixed coordinate +2 sign(e); odd: c = sign(e),
-    // the fixed coordinate -sign(e) (an error of -0 counts as negative)
-    const float wb = odd ? 1.0f : 0.0f, wh = odd ? -1.0f : 2.0f;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const bool hit = open && fabsf(e[i]) == m;
-      open = open && !hit;
-      const float c = __uint_as_float(__float_as_uint(hit ? wh : wb) ^
-                                      (__float_as_uint(e[i]) & 0x80000000u));
-      v[i] = __fadd_rn(F[i], c);
-    }
-    // fold (p = coset): s_i = 2Z(w_i) + p with w_i = (v_i - p)/2 and
-    // 2Z(w) = |4w + 1| - 1, i.e. s_i = |2 v_i + 1 - 2p| - 1 + p (exact in fp32);
-    // r = parity of sum_{i<7} w_i, s_7 = |2 v_7 - 2p - 4r + 2| - 2 + 2r + p.
-    const float p = odd ? 1.0f : 0.0f;
-    const float c1 = odd ? -1.0f : 1.0f;             // 1 - 2p
-    const float cs = odd ? kMagic1 : kMagic1 - 1.0f; // p - 1 + magic
-    float sum7 = v[0];
-#pragma unroll
-    for (int i = 1; i < 7; ++i) sum7 = __fadd_rn(sum7, v[i]);
-    const float half = __fmaf_rn(sum7, 0.5f, odd ? -3.5f : 0.0f);     // (sum7 - 7p) / 2
-    const uint32_t r = __float_as_uint(__fadd_rn(half, kMagic1)) & 1u;
-#pragma unroll
-    for (int i = 0; i < 7; ++i)
-      s[i] = __float_as_uint(__fadd_rn(fabsf(__fmaf_rn(2.0f, v[i], c1)), cs)) - 0x4B400000u;
-    const float rf = r ? 1.0f : 0.0f;
-    const float a7 = fabsf(__fmaf_rn(2.0f, v[7], __fmaf_rn(-4.0f, rf, 2.0f - 2.0f * p)));
-    s[7] = __float_as_uint(__fadd_rn(a7, __fmaf_rn(2.0f, rf, p - 2.0f + kMagic1))) - 0x4B400000u;
-  } else if (LAT == 4) {
+  static_assert(LAT != 8, "E8 codes both 8-vectors of a lane at once: quantize_fold16_e8");
+  if (LAT == 4) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       int32_t v[4];
@@ -493,10 +432,21 @@ __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) 
   }
 }
 
-// The E8 rule of quantize_fold8 for the lane's two 8-vectors at once
-// (y[i] and y[8 + i] are coordinate i of each): the roundings, errors, lattice
-// point and fold run on pairs (one vector per half), the per-vector decision
-// in scalar code; every value is the one quantize_fold8 computes.
+// Nearest point of 2E8 and the Rice symbols of the lane's two 8-vectors
+// (Method 2 and 3; y[i] and y[8 + i] are coordinate i of each).  Per vector:
+// F_i = y_i rounded to the nearest even integer (magic-number rounding),
+// e_i = y_i - F_i (exact).  The even coset's nearest point is F, with the
+// coordinate of largest |e_i| moved by 2 sign(e_i) when sum F_i / 2 is odd;
+// the odd coset's is F + sign(e), with the coordinate of smallest |e_i| moved
+// back (-sign) when its parity needs it (an error of -0 counts as negative,
+// the first index among equal |e_i| moves).  The odd coset wins only when
+// the exact difference of the two squared distances, (8 - 4pA) - 2 sum|e| +
+// 4pB min|e| + 4pA max|e|, evaluated in fp32 in that order, is negative.
+// Fold (p = coset): s_i = 2Z(w_i) + p with w_i = (v_i - p)/2, i.e.
+// |2 v_i + 1 - 2p| - 1 + p (exact in fp32), for i < 7; r = parity of
+// w_0 + .. + w_6, s_7 = 4Z((w_7 - r)/2) + 2r + p.  The roundings, errors,
+// lattice point and fold run on fp32 pairs (one vector per half); the
+// per-vector decision in scalar code.
 __device__ __forceinline__ void quantize_fold16_e8(const float y[16], uint32_t s[16]) {
   float F[16], e[16];
   uint32_t par[2] = {0u, 0u}, sx[2] = {0u, 0u};
@@ -547,7 +497,7 @@ __device__ __forceinline__ void quantize_fold16_e8(const float y[16], uint32_t s
   float v[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) upk2(add2(pk2(F[i], F[8 + i]), pk2(c[i], c[8 + i])), v[i], v[8 + i]);
-  // fold, as in quantize_fold8
+  // fold
   uint64_t sum7 = pk2(v[0], v[8]);
 #pragma unroll
   for (int i = 1; i < 7; ++i) sum7 = add2(sum7, pk2(v[i], v[8 + i]));

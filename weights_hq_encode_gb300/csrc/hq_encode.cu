@@ -414,7 +414,7 @@ encode_kernel(EncodeArgs a) {
 
   // ---- nearest point, fold, unary lengths
   uint32_t sym[16];
-  if (LAT == 8) {
+  if constexpr (LAT == 8) {
     quantize_fold16_e8(x, sym);
   } else {
     quantize_fold8<LAT>(x, sym);
