@@ -480,3 +480,33 @@ def test_decode_qk_full_size_sampled(hq, oracle):
             got = scores[:, h * G:(h + 1) * G, tok].cpu().numpy()
             bound = 1e-4 * np.linalg.norm(rows, axis=-1) * np.linalg.norm(khat[j])
             assert np.all(np.abs(got - sref) <= bound)
+
+
+def test_decode_qk_corrupt_group_scores_zero(hq, oracle):
+    """A corrupt group of the compressed K (its index entry points past the
+    next group) is flagged and its tokens score 0 for every query row, as if
+    its keys decoded to zeros; every other token's score is unchanged."""
+    n_kv, T, B, Hq = 2, 200, 3, 8
+    K, q, p, stream, offsets, total, scores, mask, cal = _scores_case(hq, oracle, n_kv, T, B, Hq,
+                                                                      600)
+    good = scores.clone()
+    bad_off = offsets.clone()
+    bad_off[4] = bad_off[5] + 1                       # group 3 now ends past group 4's start
+    sc = torch.full_like(scores, 7.0)
+    ws = torch.empty(hq.hq_decode_qk_workspace_bytes(B, Hq), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hq.hq_decode_qk(p, stream, total, bad_off, n_kv, T, q.view(torch.int16), B, Hq, sc,
+                           ws, st) == hq.HQ_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) & hq.HQ_ERR_CORRUPT
+    tiles = np.arange(n_kv * T)
+    g = tiles // 32
+    hit = (g == 3) | (g == 4)                          # the groups whose bounds changed
+    G = Hq // n_kv
+    got, ref = sc.cpu().numpy(), good.cpu().numpy()
+    for h in range(n_kv):
+        tok = np.arange(T)
+        hh = hit[h * T + tok]
+        rows = slice(h * G, (h + 1) * G)
+        assert (got[:, rows][:, :, hh] == 0).all()
+        assert (got[:, rows][:, :, ~hh] == ref[:, rows][:, :, ~hh]).all()

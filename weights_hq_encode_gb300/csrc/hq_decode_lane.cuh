@@ -135,9 +135,9 @@ __device__ __forceinline__ Quot8<P> unary8_general(const uint32_t *W, P pos, P n
 // straight from global memory (each is read by the scan first, so the parse
 // hits L1).  Bit positions within the group have type P: 32-bit for groups
 // below 2^31 bits (every group of a sane stream), 64-bit otherwise.  The
-// return value is block-uniform: false when the group is corrupt (e is then
-// all zeros).
-template <int LAT, int K, class P, class Bar>
+// return value is false when the group is corrupt (e is then all zeros):
+// uniform over the decoding threads, or, with DEFER, this lane's own verdict.
+template <int LAT, int K, class P, class Bar, bool DEFER>
 __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, int nt,
                                               const uint32_t *W, P nwords, bool bad,
                                               float e[16], P *s_start,
@@ -295,17 +295,32 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
     }
     if (slow && posj != stop) lbad = true;       // bit after the last code
   }
-  const int any_bad = Bar::sync_or((bad || lbad) ? 1 : 0);
-  if (any_bad || !valid) {
+  if constexpr (DEFER) {
+    // the caller combines the lanes' verdicts at its own next barrier
+    const bool mine = bad || lbad;
+    if (mine || !valid) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) e[i] = 0.0f;
+      for (int i = 0; i < 16; ++i) e[i] = 0.0f;
+    }
+    return !mine;
+  } else {
+    const int any_bad = Bar::sync_or((bad || lbad) ? 1 : 0);
+    if (any_bad || !valid) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) e[i] = 0.0f;
+    }
+    return !any_bad;
   }
-  return !any_bad;
 }
 
 // Dispatch on the group's size: 32-bit bit positions unless the group holds
-// 2^31 bits or more.
-template <int LAT, int K, class Bar = BlockBar>
+// 2^31 bits or more.  Without DEFER the return value is the group's verdict
+// (uniform over the decoding threads) and a corrupt group yields zeros in
+// every lane; with DEFER each lane returns its own verdict and zeroes only
+// its own values, and the caller must OR the verdicts over the group (at a
+// barrier it takes anyway) and treat the whole group as zeros if any lane
+// failed.
+template <int LAT, int K, class Bar = BlockBar, bool DEFER = false>
 __device__ __forceinline__ bool decode_lane(const DecodeArgs &a, int64_t g, float e[16],
                                             uint64_t *s_start64,
                                             uint32_t (*s_warp)[kDecThreads / 32]) {
@@ -316,9 +331,10 @@ __device__ __forceinline__ bool decode_lane(const DecodeArgs &a, int64_t g, floa
   const uint64_t nwords = bad ? 0 : end - base;
   const uint32_t *W = a.stream + (bad ? 0 : base);
   if (nwords < (1ull << 26))
-    return decode_lane_p<LAT, K, uint32_t, Bar>(a, g, nt, W, (uint32_t)nwords, bad, e,
-                                           reinterpret_cast<uint32_t *>(s_start64), s_warp);
-  return decode_lane_p<LAT, K, uint64_t, Bar>(a, g, nt, W, nwords, bad, e, s_start64, s_warp);
+    return decode_lane_p<LAT, K, uint32_t, Bar, DEFER>(a, g, nt, W, (uint32_t)nwords, bad, e,
+                                                  reinterpret_cast<uint32_t *>(s_start64), s_warp);
+  return decode_lane_p<LAT, K, uint64_t, Bar, DEFER>(a, g, nt, W, nwords, bad, e, s_start64,
+                                                     s_warp);
 }
 
 }  // namespace hq

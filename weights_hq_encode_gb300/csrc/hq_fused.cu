@@ -133,10 +133,8 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
   for (int64_t g = gb + team; g < ge + kQkTeams; g += kQkTeams) {
     const bool has = g < ge;
     float e[16];
-    if (has) {
-      const bool ok = decode_lane<LAT, K, TeamBar>(a.dec, g, e, s_start[team], s_warp[team]);
-      if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-    }
+    bool lane_ok = true;                         // this lane's decoding verdict
+    if (has) lane_ok = decode_lane<LAT, K, TeamBar, true>(a.dec, g, e, s_start[team], s_warp[team]);
     if (committed > 0 && ok_wait) {              // the previous group: wait, then its scores
       // warp-uniform for the tensor-memory loads; team-uniform at the next barrier
       ok_wait = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22));
@@ -178,7 +176,23 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
     }
     fence_async_smem();
     tc_fence_before();
-    ok_wait = TeamBar::sync_and(ok_wait) != 0;
+    // one barrier for the group's decoding verdicts and the previous wait;
+    // only when something failed, two more sort out which (rare)
+    if (TeamBar::sync_or(!(lane_ok && ok_wait)) != 0) {
+      const bool corrupt = TeamBar::sync_or(!lane_ok) != 0;
+      ok_wait = TeamBar::sync_and(ok_wait) != 0;
+      if (corrupt) {                             // the group decodes to zeros
+        if (tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          unsigned char *dst = bdst + (8 * c + r) * kQkBKStride;
+          *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4 *>(dst + 32 * kQkBKStride) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        fence_async_smem();
+        TeamBar::sync();
+      }
+    }
     if (!ok_wait) continue;
     ++committed;
     if (tid == 0) {
@@ -385,9 +399,8 @@ __global__ void __launch_bounds__(kPvThreads, 1) pv_kernel(AttnArgs a) {
   for (int k = 0; k < 8; ++k) lsum[k] = 0.0f;
   for (int64_t g = gb + team; g < ge; g += kPvTeams) {   // team-uniform bounds
     float e[16];
-    const bool ok = decode_lane<LAT, K, TeamBar>(a.v, g, e, s_start[team], s_warp[team]);
+    const bool lane_ok = decode_lane<LAT, K, TeamBar, true>(a.v, g, e, s_start[team], s_warp[team]);
     pv_load_z(a, g, h, row0, G, rows, tile_lo, tile_hi, tid, pn);
-    if (!ok && tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_CORRUPT);
     // the MMAs of the team's previous group must be done with the operands
     if (committed > 0 && ok_wait) ok_wait = mbar_wait(bar, (uint32_t)(committed - 1) & 1u, kPvWaitLimit);
 #pragma unroll
@@ -409,7 +422,23 @@ __global__ void __launch_bounds__(kPvThreads, 1) pv_kernel(AttnArgs a) {
       bp[(k + 8) * kPvGStride / 4] = lo;
     }
     fence_async_smem();
-    ok_wait = TeamBar::sync_and(ok_wait) != 0;
+    // one barrier for the group's decoding verdicts and the previous wait;
+    // only when something failed, two more sort out which (rare)
+    if (TeamBar::sync_or(!(lane_ok && ok_wait)) != 0) {
+      const bool corrupt = TeamBar::sync_or(!lane_ok) != 0;
+      ok_wait = TeamBar::sync_and(ok_wait) != 0;
+      if (corrupt) {                             // the group's values decode to zeros
+        if (tid == 0) atomicOr(a.v.status, (uint32_t)HQ_ERR_CORRUPT);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int off = 128 * (c >> 3) + ((16 * r + 16 * c) & 0x70);
+          *reinterpret_cast<float *>(ebase + off) = 0.0f;
+          *reinterpret_cast<float *>(ebase + kPvOpBytes + off) = 0.0f;
+        }
+        fence_async_smem();
+        TeamBar::sync();
+      }
+    }
     if (!ok_wait) continue;
     const bool first = committed == 0;
     ++committed;

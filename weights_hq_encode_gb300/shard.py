@@ -83,14 +83,15 @@ def device_encode_range(hq, params, x_tiles, x_first: int = 0):
     then the encode) over global tiles [b, e), held by `x_tiles` (a CUDA int16
     view [n, 128] of bf16 data whose row 0 is global tile `x_first`), with
     `params` copied and its tile_base set to b."""
-    import copy
-
     import torch
 
     def run(b, e):
         n = e - b
         dev = x_tiles.device
-        p = copy.copy(params)
+        p = type(params).from_buffer_copy(params)     # a copy of the C struct's bytes
+        for keep in ("_signs", "_rot"):                # the device arrays it points to
+            if hasattr(params, keep):
+                setattr(p, keep, getattr(params, keep))
         p.tile_base = b
         if b < x_first or e - x_first > x_tiles.shape[0]:
             raise ValueError("the rank's tile range is not held by x_tiles")
