@@ -310,6 +310,19 @@ def run_ours(args, rank, world):
             "peak": peak, "unit": "GB/s", "frac": op_report[dom]["roofline_frac"],
             "traffic": traffic, "peak_kind": peak_kind,
             "frac_of_nominal_8TBps": round(op_report[dom]["achieved_GBps"] / 8000.0, 4)}
+    # The pipe that actually binds the codec kernels: the ALU pipe (integer,
+    # logic, compare and select work; two cycles per warp instruction).  Its
+    # instruction count per launch comes from the same ncu record as the
+    # traffic; the peak is 152 SMs x 4 sub-partitions x 16 lanes x the SM clock.
+    alu = (tr or {}).get("alu_warp_instructions", {}).get(dom) if traffic is not None else None
+    if alu is not None:
+        mhz = (clk or {}).get("sm_mhz") or 2070.0
+        alu_peak = 152 * 4 * 0.5 * mhz * 1e6 / 1e12          # warp instructions per ps -> T/s
+        alu_ach = alu / (op_report[dom]["ms"] * 1e-3) / 1e12
+        roof["alu_pipe"] = {"bound": "alu", "achieved": round(alu_ach, 4), "peak": round(alu_peak, 4),
+                            "unit": "T warp-instructions/s", "frac": round(alu_ach / alu_peak, 4),
+                            "instructions_per_launch": alu,
+                            "peak_kind": "derived: 152 SMs x 4 sub-partitions x 16 ALU lanes x SM clock"}
 
     # ---- N > 1: the ranks' caches are shards of one tensor of world x n tiles;
     # shard.code_rank codes this rank's group-aligned range (tile_base = its
