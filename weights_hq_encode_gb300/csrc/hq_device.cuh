@@ -284,15 +284,30 @@ __device__ __forceinline__ int32_t nearest_z(float y) {
 // exact ties go to the coset with m, n even.
 constexpr float kA2C = 0x1.279a74p-1f;           // fl32(1/sqrt 3)
 constexpr float kA2H = 0x1.bb67aep-1f;           // fl32(sqrt(3)/2)
-__device__ __forceinline__ float a2_px(int32_t m) { return __fmul_rn(0.5f, __int2float_rn(m)); }
-__device__ __forceinline__ float a2_py(int32_t n) { return __fmul_rn(kA2H, __int2float_rn(n)); }
+// int32 -> float for |n| < 2^22 (exact) by the magic number, on the FMA pipe
+__device__ __forceinline__ float small_int_to_float(int32_t n) {
+  return __fsub_rn(__int_as_float(0x4B400000 + n), kMagic1);
+}
+__device__ __forceinline__ float a2_px(int32_t m) { return __fmul_rn(0.5f, small_int_to_float(m)); }
+__device__ __forceinline__ float a2_py(int32_t n) { return __fmul_rn(kA2H, small_int_to_float(n)); }
 __device__ __forceinline__ void nearest_a2(float x, float y, int32_t &m, int32_t &n) {
   const float yc = __fmul_rn(y, kA2C);
-  const int32_t me = 2 * __float2int_rn(x), ne = 2 * __float2int_rn(yc);
-  const int32_t mo = 2 * __float2int_rn(__fsub_rn(x, 0.5f)) + 1;
-  const int32_t no = 2 * __float2int_rn(__fsub_rn(yc, 0.5f)) + 1;
-  const float dxe = __fsub_rn(x, a2_px(me)), dye = __fsub_rn(y, a2_py(ne));
-  const float dxo = __fsub_rn(x, a2_px(mo)), dyo = __fsub_rn(y, a2_py(no));
+  // rint(x), rint(yc), rint(x - 1/2), rint(yc - 1/2) by the magic number
+  // (round half to even, exact below 2^22; |x|, |yc| stay below 2^21)
+  const float Tx = __fadd_rn(x, kMagic1), Ty = __fadd_rn(yc, kMagic1);
+  const float Txo = __fadd_rn(__fsub_rn(x, 0.5f), kMagic1);
+  const float Tyo = __fadd_rn(__fsub_rn(yc, 0.5f), kMagic1);
+  const float fx = __fsub_rn(Tx, kMagic1), fy = __fsub_rn(Ty, kMagic1);
+  const float fxo = __fsub_rn(Txo, kMagic1), fyo = __fsub_rn(Tyo, kMagic1);
+  const int32_t me = 2 * (int32_t)(fbits(Tx) - fbits(kMagic1));
+  const int32_t ne = 2 * (int32_t)(fbits(Ty) - fbits(kMagic1));
+  const int32_t mo = 2 * (int32_t)(fbits(Txo) - fbits(kMagic1)) + 1;
+  const int32_t no = 2 * (int32_t)(fbits(Tyo) - fbits(kMagic1)) + 1;
+  // the points (m / 2, fl(h n)): m / 2 = rint (even coset) or rint + 1/2
+  // (odd coset), n = 2 rint or 2 rint + 1, all exact
+  const float dxe = __fsub_rn(x, fx), dye = __fsub_rn(y, __fmul_rn(kA2H, __fadd_rn(fy, fy)));
+  const float dxo = __fsub_rn(x, __fadd_rn(fxo, 0.5f));
+  const float dyo = __fsub_rn(y, __fmul_rn(kA2H, __fmaf_rn(2.0f, fyo, 1.0f)));
   const float de = __fmaf_rn(dxe, dxe, __fmul_rn(dye, dye));
   const float dd = __fmaf_rn(dxo, dxo, __fmul_rn(dyo, dyo));
   const bool odd = dd < de;
