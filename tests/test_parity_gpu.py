@@ -401,6 +401,28 @@ def test_long_context_sweep_whole(hq, oracle, name, lat):
         del stream, offsets
 
 
+@pytest.mark.parametrize("name,lat,rate", [("E8", 8, "3.0"), ("D4", 4, "2.0")])
+def test_long_context_dense_rotation_whole(hq, oracle, name, lat, rate):
+    """The per-layer Haar (QJL) rotation on a whole workload: the long-context
+    layer with one Haar matrix for its K half and one for its V half (segments
+    of 1 048 576 tiles), dither on; every stream word, index entry and bf16
+    decoded value equals the oracle's fixed-order fp32 chains."""
+    from weights_hq_encode_gb300 import inputs as I
+    C = I.LONGCTX
+    cal = calibration()["long_context"][name][rate]
+    xt = hq.as_tiles(I.long_context_layer("cuda"))
+    n = xt.shape[0]
+    mask = (oracle.make_signs(C["sign_seed"], 0) ^ oracle.make_signs(C["layer_sign_seed"], 0))
+    masks = np.stack([mask, mask])
+    tps = n // 2
+    rot = I.haar_rotations(2, seed=321)
+    signs = torch.from_numpy(masks.view(np.int32).copy()).cuda()
+    p = hq.make_params(lat, cal["k"], cal["alpha"], 1, C["dither_seed"], signs, tps,
+                       rot=torch.from_numpy(rot.copy()).cuda())
+    P = oracle.make_params(lat, cal["k"], cal["alpha"], 1, C["dither_seed"], masks, tps, rot=rot)
+    _whole(hq, oracle, xt, n, P, p)
+
+
 # ---------------------------------------------------------------- fused scores
 def _scores_case(hq, oracle, n_kv, T, B, Hq, seed_tok):
     from weights_hq_encode_gb300 import inputs as I
