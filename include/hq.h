@@ -202,9 +202,10 @@ size_t hq_decode_qk_workspace_bytes(int B, int Hq);
 /* Attention scores from compressed K (closing section, fused decode + MMA):
  *   scores[b][hq][t] = sum_d q[b][hq][d] * Khat[h][t][d],  h = hq / (Hq / n_kv_heads),
  * with Khat the decode of K tile h * n_tokens + t; K itself is never written.
- * The products run on the tensor cores: both operands are split into two
- * tf32 parts (|x - hi - lo| <= 2^-22 |x|) and the partial products summed in
- * an fp32 accumulator, an fp32-level result.
+ * The products run on the tensor cores: each query row and each key is
+ * scaled by a power of two (exact) to below 1 in magnitude and split into
+ * two fp16 parts (|x - hi - lo| <= 2^-22 |x| + 2^-25), the partial products
+ * summed in an fp32 accumulator and the scales undone, an fp32-level result.
  *   d_q        [B][Hq][128] bf16, device.
  *   d_scores   [B][Hq][n_tokens] fp32, device.
  *   d_ws       >= hq_decode_qk_workspace_bytes(B, Hq) bytes, device.
@@ -236,8 +237,9 @@ size_t hq_decode_attention_workspace_bytes(int n_kv_heads, int64_t n_tokens, int
  * value side is accumulated in the lattice domain and transformed once per
  * query row; the softmax is formed per chunk of tokens (maximum and sum) and
  * the chunks are combined in a fixed order, so the result is deterministic.
- * Both contractions run on the tensor cores with split tf32 operands and
- * fp32 accumulators (as for hq_decode_qk).
+ * Both contractions run on the tensor cores with fp32 accumulators: the
+ * scores as in hq_decode_qk, the value sums with operands split into two tf32
+ * parts (|x - hi - lo| <= 2^-22 |x|).
  *   d_q        [B][Hq][128] bf16, device.
  *   d_out      [B][Hq][128] fp32, device, 16-byte aligned.
  *   d_probs    optional [B][Hq][n_tokens] fp32 output of p (NULL: p is not

@@ -6,10 +6,19 @@ The K and V streams are written by the CPU oracle and copied to the GPU, so
 every expected value comes from the oracle alone.
 
 Tolerance, derived to first order in u = 2^-24 from the fp32 steps of the
-CUDA path.  A score is a 128-term fp32 dot of the rotated query (7 rounded
-transform stages and one scaling) with e, so |dz_t| <= (128 + 8) u zeta,
-zeta = scale |q| max_t |Khat_t| (the transform is orthogonal, so
-|q'| |e_t| = |q| |Khat_t|).  Softmax turns that into a relative error of
+CUDA path.  A score is the rotated query (7 rounded transform stages and one
+scaling: 8 u) dotted with e on the tensor cores: the query row and the
+token are each scaled by a power of two to below 1 (exact) and split into
+two fp16 parts (per value |x - x_1 - x_2| <= 2^-22 |x| + 2^-25, the second
+term from fp16's subnormal spacing), and the three kept partial products
+q_1 e_1 + q_1 e_2 + q_2 e_1 miss the exact dot of the scaled vectors x, y
+by at most 3 * 2^-22 sum|x_i y_i| + 2^-25 (sum|x_i| + sum|y_i|) <= 35 u |x| |y|
+(the largest scaled value is at least 1/2 and sum|x_i| <= sqrt(128) |x|),
+i.e. 35 u |q'| |e_t| once the scales are undone; they
+are accumulated in fp32 over 24 MMA steps, at most 2 u each even if the
+accumulation truncates (48 u).  So |dz_t| <= (8 + 35 + 48) u zeta <
+136 u zeta, zeta = scale |q| max_t |Khat_t| (the transform is orthogonal,
+so |q'| |e_t| = |q| |Khat_t|).  Softmax turns that into a relative error of
 p_t of at most 2 max|dz| plus a few u for exp and the division.  The value
 side sums p_t e_t over at most 256 tokens per chunk on the tensor cores:
 both operands split into two tf32 parts (|x - hi - lo| <= 2^-22 |x| = 4 u |x|,

@@ -504,6 +504,36 @@ def test_decode_qk_full_size_sampled(hq, oracle):
             assert np.all(np.abs(got - sref) <= bound)
 
 
+def test_decode_qk_query_rows_of_very_different_magnitude(hq, oracle):
+    """Query rows scaled by powers of two from 2^-100 to 2^100 (exact in
+    bf16): every row's scores stay within the relative bound of its own norm,
+    so the tensor-core operands keep each row's precision at any scale (a
+    16-bit operand format without per-row scaling would overflow or lose the
+    small rows)."""
+    n_kv, T, B, Hq = 2, 200, 5, 8
+    K, q, p, stream, offsets, total, scores, mask, cal = _scores_case(hq, oracle, n_kv, T, B, Hq,
+                                                                      700)
+    f = torch.exp2(torch.tensor([-100.0, -20.0, 0.0, 20.0, 100.0], device="cuda"))[:, None, None]
+    qs = (q.float() * f).to(torch.bfloat16)
+    assert torch.equal(qs.float(), q.float() * f)
+    sc = torch.full((B, Hq, T), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(hq.hq_decode_qk_workspace_bytes(B, Hq), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hq.hq_decode_qk(p, stream, total, offsets, n_kv, T, qs.view(torch.int16), B, Hq, sc,
+                           ws, st) == hq.HQ_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    P = oracle.make_params(8, cal["k"], cal["alpha"], 1, 700, mask, n_kv * T)
+    ref = oracle.encode(P, K.reshape(-1, 128).cpu().view(torch.int16).numpy().view(np.uint16))
+    khat = oracle.decode(P, ref["stream"], ref["offsets"], n_kv * T)["out"]
+    qb = qs.cpu().view(torch.int16).numpy().view(np.uint16)
+    sref = oracle.scores(khat, n_kv, T, qb, B, Hq)
+    qn = np.linalg.norm((qb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=-1)
+    kn = np.linalg.norm(khat.reshape(n_kv, T, 128).astype(np.float64), axis=-1)
+    bound = 1e-4 * qn[:, :, None] * np.repeat(kn, Hq // n_kv, axis=0)[None]
+    assert np.all(np.abs(sc.cpu().numpy().astype(np.float64) - sref) <= bound)
+
+
 def test_decode_qk_corrupt_group_scores_zero(hq, oracle):
     """A corrupt group of the compressed K (its index entry points past the
     next group) is flagged and its tokens score 0 for every query row, as if

@@ -37,45 +37,91 @@ __global__ void rotate_queries_kernel(QkArgs a) {
 }
 
 // Scores of one KV head over a chunk of its token groups for one tile of
-// up to 64 query rows, on the tensor cores (tcgen05, kind::tf32, fp32
-// accumulator in tensor memory).  The fp32-level product of the split
-// operands is laid along K: with q' = q_hi + q_lo and e = e_hi + e_lo (each
-// part tf32), A = [q_hi | q_lo | q_hi] and B = [e_hi | e_hi | e_lo] over
-// K = 3 x 128, so one accumulator lane per query row receives
-// q_hi e_hi + q_lo e_hi + q_hi e_lo (the dropped q_lo e_lo is below 2^-22 of
-// each product).  M = 128 with rows 64..127 of A aliasing the next K-core
-// (their results are never read), N = 32 tokens of a group.
+// up to 64 query rows, on the tensor cores (tcgen05, kind::f16 with fp16
+// operands, fp32 accumulator in tensor memory).  Each query row and each
+// token's e is scaled by a power of two to below 1 in magnitude, then split
+// into two fp16 parts, x = x_1 + x_2 (|x - x_1 - x_2| <= 2^-22 |x| + 2^-25),
+// and the fp32-level product is laid along K: A = [q_1 | q_1 | q_2] and
+// B = [e_1 | e_2 | e_1] over K = 3 x 128, so one accumulator lane per query
+// row receives q_1 e_1 + q_1 e_2 + q_2 e_1 (the dropped q_2 e_2 is below
+// 2^-22 of the product); the epilogue multiplies by the two inverse scales
+// (exact).  M = 128 with rows 64..127 of A aliasing the next K-core (their
+// results are never read), N = 32 tokens of a group.
 //
 // The block holds the split query rows once and runs four independent teams
 // of 256 threads (named barriers), each decoding every fourth group of the
 // chunk into its own B and accumulator columns: a team decodes its next group
 // while the MMAs of its previous one run, then writes that group's scores
-// from tensor memory.  Dimensions are permuted consistently in A and B
-// (16-byte block 4 r + c of d goes to K-core 8 c + r) so that the eight lanes
-// of a tile store e to distinct banks.
+// from tensor memory.  With 16-bit operands (99 KB) and 32 registers per
+// thread two blocks fit on an SM, 64 warps of decoding.  Dimensions are
+// permuted consistently in A and B (16-byte block 2 r + c of d, dimensions
+// 16 r + 8 c .. +7, goes to K-core 8 c + r) so that the eight lanes of a
+// tile store e to distinct banks.
 constexpr int kQkRows = 64;                      // query rows per block
 constexpr int kQkTeams = 4;
 constexpr int kQkThreads = kQkTeams * kDecThreads;
+constexpr int kQkBlocksPerSm = 2;
 constexpr int kQkChunkMin = kQkTeams, kQkChunkMax = 32;   // groups of 32 tokens per block
+constexpr int kQkCores = kTile / 8;              // K-cores of one fp16 part (8 dimensions each)
 constexpr int kQkAKStride = 1024;                // bytes between K-cores of A (8 row groups)
 constexpr int kQkAGStride = 128;                 // bytes between 8-row groups of A
 constexpr int kQkBKStride = 528;                 // bytes between K-cores of B (4 token groups + 16)
 constexpr int kQkBGStride = 128;                 // bytes between 8-token groups of B
-constexpr int kQkABytes = 64 * kQkAKStride + 1024;   // [q_hi | q_lo] + the aliased rows' reach
-constexpr int kQkBBytes = 64 * kQkBKStride;          // [e_hi | e_lo] of one team
+constexpr int kQkABytes = 2 * kQkCores * kQkAKStride + 1024;   // [q_1 | q_2] + the aliased rows' reach
+constexpr int kQkBBytes = 2 * kQkCores * kQkBKStride;          // [e_1 | e_2] of one team
 constexpr int kQkSmemBytes = kQkABytes + kQkTeams * kQkBBytes;
-constexpr uint32_t kQkIdesc = umma_idesc_tf32(128, 32);
+constexpr uint32_t kQkIdesc = umma_idesc_f16(128, 32);
 constexpr uint32_t kQkTmemCols = 32 * kQkTeams;
+static_assert(kQkRows * kQkCores == kQkThreads, "one (row, 8-dimension block) of A per thread");
 
-// K-core of the 16-byte block db (0..31) of the 128 dimensions.
-__device__ __forceinline__ int qk_kcore(int db) { return 8 * (db & 3) + (db >> 2); }
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// The lane's 16 values of e (one token, dimensions 16 r .. 16 r + 15), scaled
+// by `sc` and split into fp16 parts: block c (dimensions 16 r + 8 c .. +7) of
+// e_1 at K-core 8 c + r (`dst` = K-core r of the token's row), e_2 a part
+// further on.
+__device__ __forceinline__ void qk_store_b(uint32_t dst, const float e[16], float sc) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      upk2(mul2(pk2(e[8 * c + 2 * i], e[8 * c + 2 * i + 1]), pk2(sc, sc)), x[2 * i], x[2 * i + 1]);
+    uint4 hi, lo;
+    split_f16x2(x[0], x[1], hi.x, lo.x);
+    split_f16x2(x[2], x[3], hi.y, lo.y);
+    split_f16x2(x[4], x[5], hi.z, lo.z);
+    split_f16x2(x[6], x[7], hi.w, lo.w);
+    st_shared16(dst + 8 * c * kQkBKStride, hi);
+    st_shared16(dst + (8 * c + kQkCores) * kQkBKStride, lo);
+  }
+}
+
+// A token's e into B: the largest |e| over the token's 8 lanes sets its
+// power-of-two scale; lane 0 of the tile keeps the inverse for the epilogue.
+// All 32 lanes of the warp must call it.
+__device__ __forceinline__ void qk_put_e(const float e[16], uint32_t dst, float *tinv, int tl, int r) {
+  float m = fabsf(e[0]);
+#pragma unroll
+  for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(e[i]));
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  if (r == 0) tinv[tl] = inv_scale_of(m);
+  qk_store_b(dst, e, scale_of(m));
+}
 
 template <int LAT, int K>
-__global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chunk_groups) {
+__global__ void __launch_bounds__(kQkThreads, kQkBlocksPerSm) scores_kernel(QkArgs a, int chunk_groups) {
   __shared__ uint64_t s_start[kQkTeams][kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[kQkTeams][2][kDecThreads / 32];
   __shared__ __align__(8) uint64_t s_bar[kQkTeams];
   __shared__ uint32_t s_taddr;
+  __shared__ uint32_t s_qmax[kQkRows];           // largest |q'| of each row (float bits)
+  __shared__ __align__(16) float s_tinv[kQkTeams][2][kGroupTiles];   // 1 / token scale, two groups
   extern __shared__ __align__(128) unsigned char s_ops[];   // A | B of team 0 | ... | B of team 3
   const int team = threadIdx.x / kDecThreads, tid = TeamBar::tid();
   const int tl = tid >> 3, r = tid & 7, warp = tid >> 5;
@@ -89,24 +135,35 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
   if (gb >= ge) return;                          // uniform: nothing of head h here
   if (threadIdx.x < 32) tmem_alloc(&s_taddr, kQkTmemCols);
   if (tid == 32) mbar_init(&s_bar[team], 1);
-  // A: the block's rotated query rows split into tf32 parts (rows past the
-  // end are zeros)
-  for (int u = threadIdx.x; u < kQkRows * 32; u += kQkThreads) {
-    const int q = u & (kQkRows - 1), db = u >> 6, row = row0 + q;   // 8 rows per 128-byte phase
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (threadIdx.x < kQkRows) s_qmax[threadIdx.x] = 0u;
+  // A: the block's rotated query rows, each scaled by a power of two to below
+  // 1 and split into fp16 parts (rows past the end are zeros); thread =
+  // (8-dimension block db, row q), 8 rows per 128-byte phase
+  {
+    const int q = threadIdx.x & (kQkRows - 1), db = threadIdx.x >> 6, row = row0 + q;
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
     if (row < rows) {
       const int b = row / G, gq = row - b * G;
-      v = __ldg(reinterpret_cast<const float4 *>(
-                    a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile) + db);
+      const float4 *src = reinterpret_cast<const float4 *>(
+                              a.qrot + ((int64_t)b * a.Hq + (int64_t)h * G + gq) * kTile) + 2 * db;
+      v0 = __ldg(src);
+      v1 = __ldg(src + 1);
     }
-    float4 hi, lo;
-    split_tf32(v.x, hi.x, lo.x);
-    split_tf32(v.y, hi.y, lo.y);
-    split_tf32(v.z, hi.z, lo.z);
-    split_tf32(v.w, hi.w, lo.w);
-    unsigned char *dst = s_ops + (q >> 3) * kQkAGStride + qk_kcore(db) * kQkAKStride + (q & 7) * 16;
-    *reinterpret_cast<float4 *>(dst) = hi;
-    *reinterpret_cast<float4 *>(dst + 32 * kQkAKStride) = lo;
+    const float m = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                          fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+    __syncthreads();                             // s_qmax cleared
+    atomicMax(&s_qmax[q], __float_as_uint(m));   // nonnegative floats order as integers
+    __syncthreads();
+    const float sc = scale_of(__uint_as_float(s_qmax[q]));
+    uint4 hi, lo;
+    split_f16x2(__fmul_rn(v0.x, sc), __fmul_rn(v0.y, sc), hi.x, lo.x);
+    split_f16x2(__fmul_rn(v0.z, sc), __fmul_rn(v0.w, sc), hi.y, lo.y);
+    split_f16x2(__fmul_rn(v1.x, sc), __fmul_rn(v1.y, sc), hi.z, lo.z);
+    split_f16x2(__fmul_rn(v1.z, sc), __fmul_rn(v1.w, sc), hi.w, lo.w);
+    const int core = 8 * (db & 1) + (db >> 1);
+    unsigned char *dst = s_ops + (q >> 3) * kQkAGStride + core * kQkAKStride + (q & 7) * 16;
+    *reinterpret_cast<uint4 *>(dst) = hi;
+    *reinterpret_cast<uint4 *>(dst + kQkCores * kQkAKStride) = lo;
   }
   fence_async_smem();
   tc_fence_before();
@@ -114,13 +171,13 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
   tc_fence_after();
   const uint32_t dcol = s_taddr + (uint32_t)(32 * team);
   const uint32_t a_op = smem_addr(s_ops), b_op = a_op + kQkABytes + team * kQkBBytes;
-  unsigned char *const bdst =
-      s_ops + kQkABytes + team * kQkBBytes + (tl >> 3) * kQkBGStride + (tl & 7) * 16;
+  const uint32_t bdst = b_op + (tl >> 3) * kQkBGStride + (tl & 7) * 16 + r * kQkBKStride;
   uint64_t *const bar = &s_bar[team];
   // epilogue geometry: team warps 0, 1, 4, 5 read lanes (query rows)
   // 32 (w % 4) + lane, tokens 16 (w / 4) .. +15 of the group
   const bool reader = (warp & 2) == 0;
   const int q_row = 32 * (warp & 1) + (tid & 31), row = row0 + q_row, tcol = 16 * (warp >> 2);
+  const float qinv = inv_scale_of(__uint_as_float(s_qmax[q_row]));
   float *srow = nullptr;
   if (reader && row < rows) {
     const int b = row / G, gq = row - b * G;
@@ -138,42 +195,42 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
     if (committed > 0 && ok_wait) {              // the previous group: wait, then its scores
       // warp-uniform for the tensor-memory loads; team-uniform at the next barrier
       ok_wait = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(committed - 1) & 1u, 1u << 22));
-      if (ok_wait && reader) {
+      if (ok_wait && has) qk_put_e(e, bdst, s_tinv[team][committed & 1], tl, r);   // B is free again
+      if (ok_wait && reader) {                   // two loads of 8 columns (32 registers)
         tc_fence_after();
-        float v[16];
-        tmem_ld16(dcol + ((uint32_t)(32 * (warp & 1)) << 16) + (uint32_t)tcol, v);
-        const int64_t t0 = (g - kQkTeams) * kGroupTiles + tcol;
-        if (srow != nullptr) {
-          if (t0 >= tile_lo && t0 + 16 <= tile_hi) {
-            float4 *dst = reinterpret_cast<float4 *>(srow + t0);
-            if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        const float *tinv = s_tinv[team][(committed - 1) & 1] + tcol;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[8];
+          tmem_ld8(dcol + ((uint32_t)(32 * (warp & 1)) << 16) + (uint32_t)(tcol + 8 * hh), v);
+          const float4 i0 = *reinterpret_cast<const float4 *>(tinv + 8 * hh);
+          const float4 i1 = *reinterpret_cast<const float4 *>(tinv + 8 * hh + 4);
+          const float ti[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], qinv), ti[j]);
+          const int64_t t0 = (g - kQkTeams) * kGroupTiles + tcol + 8 * hh;
+          if (srow != nullptr) {
+            if (t0 >= tile_lo && t0 + 8 <= tile_hi) {
+              float4 *dst = reinterpret_cast<float4 *>(srow + t0);
+              if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) srow[t0 + j] = v[j];
+              }
             } else {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) srow[t0 + j] = v[j];
+              for (int j = 0; j < 8; ++j)
+                if (t0 + j >= tile_lo && t0 + j < tile_hi) srow[t0 + j] = v[j];
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (t0 + j >= tile_lo && t0 + j < tile_hi) srow[t0 + j] = v[j];
           }
         }
       }
+    } else if (has) {                            // first group of the team (or after a timeout)
+      qk_put_e(e, bdst, s_tinv[team][committed & 1], tl, r);
     }
     if (!has) continue;
-    // B: this lane's 16 values split into tf32 parts, four 16-byte blocks each
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float4 hi, lo;
-      split_tf32(e[4 * c], hi.x, lo.x);
-      split_tf32(e[4 * c + 1], hi.y, lo.y);
-      split_tf32(e[4 * c + 2], hi.z, lo.z);
-      split_tf32(e[4 * c + 3], hi.w, lo.w);
-      unsigned char *dst = bdst + (8 * c + r) * kQkBKStride;
-      *reinterpret_cast<float4 *>(dst) = hi;
-      *reinterpret_cast<float4 *>(dst + 32 * kQkBKStride) = lo;
-    }
     fence_async_smem();
     tc_fence_before();
     // one barrier for the group's decoding verdicts and the previous wait;
@@ -183,12 +240,8 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
       ok_wait = TeamBar::sync_and(ok_wait) != 0;
       if (corrupt) {                             // the group decodes to zeros
         if (tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          unsigned char *dst = bdst + (8 * c + r) * kQkBKStride;
-          *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4 *>(dst + 32 * kQkBKStride) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        const float zeros[16] = {};
+        qk_store_b(bdst, zeros, 1.0f);
         fence_async_smem();
         TeamBar::sync();
       }
@@ -199,10 +252,10 @@ __global__ void __launch_bounds__(kQkThreads, 1) scores_kernel(QkArgs a, int chu
       tc_fence_after();
 #pragma unroll
       for (int part = 0; part < 3; ++part) {
-        const int ka = part == 1 ? 32 : 0, kb = part == 2 ? 32 : 0;
+        const int ka = part == 2 ? kQkCores : 0, kb = part == 1 ? kQkCores : 0;
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-          umma_tf32(dcol, umma_desc(a_op + (ka + 2 * ks) * kQkAKStride, kQkAKStride, kQkAGStride),
+        for (int ks = 0; ks < kQkCores / 2; ++ks)
+          umma_f16(dcol, umma_desc(a_op + (ka + 2 * ks) * kQkAKStride, kQkAKStride, kQkAGStride),
                     umma_desc(b_op + (kb + 2 * ks) * kQkBKStride, kQkBKStride, kQkBGStride), kQkIdesc,
                     (part > 0 || ks > 0) ? 1u : 0u);
       }

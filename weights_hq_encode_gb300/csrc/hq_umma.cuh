@@ -1,15 +1,16 @@
 // hq_umma.cuh -- fifth-generation tensor-core helpers (tcgen05, sm_103a):
-// tensor-memory allocation, shared-memory matrix descriptors, the tf32 MMA
-// with an fp32 accumulator in tensor memory, completion through an mbarrier,
-// and the 32-lane tensor-memory loads of the epilogue.
+// tensor-memory allocation, shared-memory matrix descriptors, the tf32 and
+// bf16 MMAs with an fp32 accumulator in tensor memory, completion through an
+// mbarrier, and the 32-lane tensor-memory loads of the epilogue.
 //
 // Operands sit in shared memory as "core matrices" of 8 rows x 16 bytes
-// (8 x 4 tf32 values, row-major inside the core), K-major, no swizzle: the
-// element (row, k) of an operand lives at
-//   (row / 8) * SBO + (k / 4) * LBO + (row % 8) * 16 + (k % 4) * 4
+// (8 x 4 tf32 or 8 x 8 bf16 values, row-major inside the core), K-major, no
+// swizzle: with E values per 16 bytes, the element (row, k) of an operand
+// lives at
+//   (row / 8) * SBO + (k / E) * LBO + (row % 8) * 16 + (k % E) * (16 / E)
 // bytes from its base, so LBO is the distance between cores adjacent along K
-// and SBO the distance between 8-row groups.  An MMA of K = 8 reads two
-// cores along K; the next K step starts 2 * LBO further on.
+// and SBO the distance between 8-row groups.  An MMA reads two cores along K
+// (K = 8 for tf32, 16 for bf16); the next K step starts 2 * LBO further on.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -33,6 +34,12 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint3
 constexpr uint32_t umma_idesc_tf32(int m, int n) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B (bits 7-9, 10-12 =
+// 0), fp32 accumulator, both K-major.
+constexpr uint32_t umma_idesc_f16(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // One warp allocates `ncols` (a power of two >= 32) tensor-memory columns
@@ -97,6 +104,16 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// The same with 16-bit operands (kind::f16, K = 16 per instruction).
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives on the mbarrier once every MMA this thread issued has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -120,6 +137,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 8 consecutive fp32 columns of this thread's tensor-memory lane (the same
+// lane rule as tmem_ld16).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 // x = hi + lo with hi = x rounded to tf32 (nearest, ties away) and lo the
 // rest, itself rounded to tf32: |x - hi - lo| <= 2^-22 |x|, so the four
 // products of two split operands carry an fp32-level error.
@@ -129,6 +159,33 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
   hi = __uint_as_float(h);
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(__fsub_rn(x, hi)));
   lo = __uint_as_float(l);
+}
+
+// (x0, x1) = hi + lo as fp16 pairs (x0 in the low half of each word) for
+// |x| < 1: hi = x rounded to fp16 (nearest even), lo = x - hi (exact in
+// fp32) rounded the same way, so |x - hi - lo| <= 2^-22 |x| + 2^-25 (the
+// second term from fp16's subnormal spacing 2^-24).
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(x1), "f"(x0));
+  float h0, h1;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(h0), "=f"(h1)
+      : "r"(hi));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(__fsub_rn(x1, h1)), "f"(__fsub_rn(x0, h0)));
+}
+
+// Power-of-two scale for values of largest magnitude m: scale_of(m) * m lies
+// in [1/2, 1) for 2^-126 <= m < 2^126 (below 1 for smaller m, below 4 for
+// any finite m), inv_scale_of(m) = 1 / scale_of(m); multiplying by either
+// changes no bit of a value that stays in the normal range.
+__device__ __forceinline__ uint32_t exp_field_of(float m) {
+  return min((__float_as_uint(m) >> 23) & 0xFFu, 252u);
+}
+__device__ __forceinline__ float scale_of(float m) {
+  return __uint_as_float((253u - exp_field_of(m)) << 23);
+}
+__device__ __forceinline__ float inv_scale_of(float m) {
+  return __uint_as_float((exp_field_of(m) + 1u) << 23);
 }
 
 }  // namespace hq
