@@ -423,6 +423,45 @@ def test_long_context_dense_rotation_whole(hq, oracle, name, lat, rate):
     _whole(hq, oracle, xt, n, P, p)
 
 
+def test_indices_past_two_to_the_31_elements(hq, oracle):
+    """A ragged input of 2^24 + 37 tiles (2^31 + 4736 elements, 4 GiB of bf16):
+    the groups at the start, on both sides of element 2^31 and at the
+    ragged end, and a few drawn at random, are coded and decoded exactly as
+    the oracle codes each of them alone (64-bit tile, element and stream
+    positions); the index is non-decreasing and ends at the stream's length."""
+    n = (1 << 24) + 37
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    xt = torch.empty(n, 128, dtype=torch.bfloat16, device="cuda")
+    for a in range(0, n, 1 << 22):
+        b = min(n, a + (1 << 22))
+        xt[a:b] = torch.randn(b - a, 128, generator=gen, device="cuda").to(torch.bfloat16)
+    cal = calibration()["kv_cache_8b"]["E8"]["3.0"]
+    seed = 77
+    mask = oracle.make_signs(5, 0).reshape(1, 4)
+    signs = torch.from_numpy(mask.view(np.int32).copy()).cuda()
+    p = hq.make_params(8, cal["k"], cal["alpha"], 1, seed, signs, n)
+    stream, offsets, status, total, _ = gpu_encode(hq, p, xt, n)
+    assert status == 0
+    off = offsets.cpu().numpy().view(np.uint64)
+    assert off[0] == 0 and off[-1] == total and (np.diff(off.astype(np.int64)) >= 0).all()
+    out, st = gpu_decode(hq, p, stream, total, offsets, n, hq.HQ_OUT_BF16)
+    assert st == 0
+    ng = hq.hq_num_groups(n)
+    edge = (1 << 24) // 32                           # the group that starts at element 2^31
+    rng = np.random.default_rng(3)
+    for g in sorted({0, edge - 1, edge, ng - 1} | set(rng.integers(0, ng, 4).tolist())):
+        t0, t1 = 32 * g, min(n, 32 * g + 32)
+        xb = xt[t0:t1].cpu().view(torch.int16).numpy().view(np.uint16)
+        P = oracle.make_params(8, cal["k"], cal["alpha"], 1, seed, mask, 1 << 40, t0)
+        ref = oracle.encode(P, xb)
+        assert ref["status"] == 0
+        words = u32(stream[int(off[g]):int(off[g + 1])])
+        assert words.size == ref["total_words"] and (words == ref["stream"][:words.size]).all()
+        dref = oracle.decode(P, ref["stream"], ref["offsets"], t1 - t0, out="bf16")
+        got = out[t0:t1].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, dref["out"])
+
+
 # ---------------------------------------------------------------- fused scores
 def _scores_case(hq, oracle, n_kv, T, B, Hq, seed_tok):
     from weights_hq_encode_gb300 import inputs as I
