@@ -621,7 +621,6 @@ __device__ __forceinline__ void point8(const int32_t v[8], float fv[8]) {
   }
 }
 
-// Remainder bits written per tile.
 // Remainder bits written per 8 coordinates and per tile.
 template <int LAT>
 __device__ __host__ __forceinline__ constexpr int rbits8(int k) {
