@@ -58,20 +58,23 @@ template <class Keys>
 __device__ __forceinline__ uint4 dither_words(const Keys &key, uint64_t tile, uint32_t j) {
   return philox10(make_uint4((uint32_t)tile, (uint32_t)(tile >> 32), j, kDitherTag), key);
 }
-// 1 + b 2^-16 for the 16-bit value b in the low / high half of w (exact).
-__device__ __forceinline__ float grid_lo(uint32_t w) {
-  return __uint_as_float(((w << 7) & 0x007FFF80u) | 0x3F800000u);
+// The 16-bit value b in the low / high half of w as an exact float: the two
+// bytes moved under the exponent of 2^23 (one byte permute), then 2^23
+// subtracted.
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610)), 8388608.0f);
 }
-__device__ __forceinline__ float grid_hi(uint32_t w) {
-  return __uint_as_float(((w >> 9) & 0x007FFF80u) | 0x3F800000u);
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632)), 8388608.0f);
 }
-// With f = 1 + b 2^-16 these give the grid midpoints exactly:
-//   -1   + (b + 1/2) 2^-15 = 2f + (-3 + 2^-16)
-//   -2   + (b + 1/2) 2^-14 = 4f + (-6 + 2^-15)
-//   -1/2 + (b + 1/2) 2^-16 =  f + (-3/2 + 2^-17)
-constexpr float kGrid15 = -3.0f + 0x1p-16f;
-constexpr float kGrid14 = -6.0f + 0x1p-15f;
-constexpr float kGrid16 = -1.5f + 0x1p-17f;
+// With b as above these give the grid midpoints exactly (at most 17
+// significant bits), in one fused multiply-add:
+//   -1   + (b + 1/2) 2^-15 = b 2^-15 + (-1 + 2^-16)
+//   -2   + (b + 1/2) 2^-14 = b 2^-14 + (-2 + 2^-15)
+//   -1/2 + (b + 1/2) 2^-16 = b 2^-16 + (-1/2 + 2^-17)
+constexpr float kGrid15 = -1.0f + 0x1p-16f;
+constexpr float kGrid14 = -2.0f + 0x1p-15f;
+constexpr float kGrid16 = -0.5f + 0x1p-17f;
 
 // ---------------------------------------------------------------- FWHT-128
 // Unnormalised Walsh-Hadamard transform, natural (Sylvester) order, stages
@@ -336,11 +339,11 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
     float e[8];
 #pragma unroll
     for (int m = 0; m < 3; ++m) {
-      e[2 * m] = __fmaf_rn(grid_lo(w[m]), 2.0f, kGrid15);
-      e[2 * m + 1] = __fmaf_rn(grid_hi(w[m]), 2.0f, kGrid15);
+      e[2 * m] = __fmaf_rn(half_lo(w[m]), 0x1p-15f, kGrid15);
+      e[2 * m + 1] = __fmaf_rn(half_hi(w[m]), 0x1p-15f, kGrid15);
     }
-    e[6] = __fmaf_rn(grid_lo(w[3]), 2.0f, kGrid15);
-    const float u07 = __fmaf_rn(grid_hi(w[3]), 4.0f, kGrid14);   // in (-2, 2)
+    e[6] = __fmaf_rn(half_lo(w[3]), 0x1p-15f, kGrid15);
+    const float u07 = __fmaf_rn(half_hi(w[3]), 0x1p-14f, kGrid14);   // in (-2, 2)
     // coordinates 0..6 lie in (-1, 1): nearest even integer 0, error = u0
     const float T7 = __fadd_rn(u07, kMagic2);
     const float F7 = __fsub_rn(T7, kMagic2);
@@ -375,10 +378,10 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float e[4];
-      e[0] = __fadd_rn(grid_lo(w[2 * h]), kGrid16);
-      e[1] = __fadd_rn(grid_hi(w[2 * h]), kGrid16);
-      e[2] = __fadd_rn(grid_lo(w[2 * h + 1]), kGrid16);
-      const float u03 = __fmaf_rn(grid_hi(w[2 * h + 1]), 2.0f, kGrid15);   // in (-1, 1)
+      e[0] = __fmaf_rn(half_lo(w[2 * h]), 0x1p-16f, kGrid16);
+      e[1] = __fmaf_rn(half_hi(w[2 * h]), 0x1p-16f, kGrid16);
+      e[2] = __fmaf_rn(half_lo(w[2 * h + 1]), 0x1p-16f, kGrid16);
+      const float u03 = __fmaf_rn(half_hi(w[2 * h + 1]), 0x1p-15f, kGrid15);   // in (-1, 1)
       const float T3 = __fadd_rn(u03, kMagic1);
       e[3] = __fsub_rn(u03, __fsub_rn(T3, kMagic1));
       bool open = (__float_as_uint(T3) & 1u) != 0u;   // odd sum: move the worst coordinate
@@ -395,8 +398,8 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
     // the box [-1/2, 1/2) x [-h, h), two cells of A2; u = u0 - point(Q(u0))
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const float x0 = __fadd_rn(grid_lo(w[m]), kGrid16);
-      const float y0 = __fmul_rn(kA2H, __fmaf_rn(grid_hi(w[m]), 2.0f, kGrid15));
+      const float x0 = __fmaf_rn(half_lo(w[m]), 0x1p-16f, kGrid16);
+      const float y0 = __fmul_rn(kA2H, __fmaf_rn(half_hi(w[m]), 0x1p-15f, kGrid15));
       int32_t qm, qn;
       nearest_a2(x0, y0, qm, qn);
       u[2 * m] = __fsub_rn(x0, a2_px(qm));
@@ -405,8 +408,8 @@ __device__ __forceinline__ void dither8(const Keys &key, uint64_t tile, uint32_t
   } else {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      u[2 * m] = __fadd_rn(grid_lo(w[m]), kGrid16);
-      u[2 * m + 1] = __fadd_rn(grid_hi(w[m]), kGrid16);
+      u[2 * m] = __fmaf_rn(half_lo(w[m]), 0x1p-16f, kGrid16);
+      u[2 * m + 1] = __fmaf_rn(half_hi(w[m]), 0x1p-16f, kGrid16);
     }
   }
 }
