@@ -467,21 +467,30 @@ __device__ __forceinline__ void quantize_fold8(const float y[8], uint32_t s[8]) 
 // per-vector decision in scalar code.
 __device__ __forceinline__ void quantize_fold16_e8(const float y[16], uint32_t s[16]) {
   float F[16], e[16];
-  uint32_t par[2] = {0u, 0u}, sx[2] = {0u, 0u};
   const uint64_t M2 = pk2(kMagic2, kMagic2);
+  uint64_t SF = 0, PE = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint64_t Y = pk2(y[i], y[8 + i]);
-    const uint64_t T = add2(Y, M2);
-    const uint64_t FF = sub2(T, M2);
-    upk2(sub2(Y, FF), e[i], e[8 + i]);
+    const uint64_t FF = sub2(add2(Y, M2), M2);
+    const uint64_t E = sub2(Y, FF);
+    upk2(E, e[i], e[8 + i]);
     upk2(FF, F[i], F[8 + i]);
-    float t0, t1;
-    upk2(T, t0, t1);
-    par[0] ^= __float_as_uint(t0);
-    par[1] ^= __float_as_uint(t1);
-    sx[0] ^= __float_as_uint(e[i]);
-    sx[1] ^= __float_as_uint(e[8 + i]);
+    SF = i == 0 ? FF : add2(SF, FF);             // sum F (exact: even integers, |F| <= 2^20 + 2)
+    PE = i == 0 ? E : mul2(PE, E);               // its sign = the XOR of the errors' signs
+  }
+  // parity of sum F / 2 from the magic-number rounding of the exact half sum;
+  // the sign parity of the errors from their product (the sign of a product
+  // is the XOR of the factors' signs, zeros included, whatever the rounding)
+  uint32_t par[2], sx[2];
+  {
+    float h0, h1, p0, p1;
+    upk2(fma2(SF, pk2(0.5f, 0.5f), pk2(kMagic1, kMagic1)), h0, h1);
+    upk2(PE, p0, p1);
+    par[0] = __float_as_uint(h0);
+    par[1] = __float_as_uint(h1);
+    sx[0] = __float_as_uint(p0);
+    sx[1] = __float_as_uint(p1);
   }
   float c[16];
   bool odd[2];

@@ -389,10 +389,16 @@ encode_kernel(EncodeArgs a) {
     }
     const uint64_t S2 = pk2(a.s_enc, a.s_enc);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      upk2(fma2(pk2(x[i], x[8 + i]), S2, pk2(u[i], u[8 + i])), x[i], x[8 + i]);
-      bad |= !(fabsf(x[i]) <= kRangeLimit);
-      bad |= !(fabsf(x[8 + i]) <= kRangeLimit);
+    for (int i = 0; i < 8; ++i) upk2(fma2(pk2(x[i], x[8 + i]), S2, pk2(u[i], u[8 + i])), x[i], x[8 + i]);
+    // range rule: a sum of magnitudes rounds to at least its largest term, so
+    // a sum within the limit clears all 16 values (NaN and overflow fail it
+    // and take the value-by-value test)
+    float sa[4] = {fabsf(x[0]), fabsf(x[1]), fabsf(x[2]), fabsf(x[3])};
+#pragma unroll
+    for (int i = 4; i < 16; ++i) sa[i & 3] = __fadd_rn(sa[i & 3], fabsf(x[i]));
+    if (!(__fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])) <= kRangeLimit)) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bad |= !(fabsf(x[i]) <= kRangeLimit);
     }
   }
   const uint32_t bal = __ballot_sync(0xffffffffu, valid && bad);
