@@ -510,17 +510,23 @@ float oracle_decode_scale(float alpha) { return (float)(1.0 / ((double)alpha * s
  * the summary fixes neither; u = +0 without dither).  Range rule (reading of
  * "alpha is chosen so that codes fit"): if any y_i is NaN or |y_i| > 2^20 the
  * tile is coded as if x were 0 and ORA_ERR_RANGE is reported. */
-/* The lattice-domain values y of one tile (before the nearest point), with
- * the range rule applied; returns the range flag. */
-static int tile_y(const ora_params *P, const uint16_t *x, int64_t t, float *y) {
+/* z = H D (R) x and the dither u of one tile (u = +0 without dither). */
+static void tile_zu(const ora_params *P, const uint16_t *x, int64_t t, float *z, float *u) {
   const uint32_t *m = tile_mask(P, t);
-  float z[TILE], u[TILE], xf[TILE];
+  float xf[TILE];
   for (int i = 0; i < TILE; ++i) xf[i] = bf16_to_float(x[i]);
   if (P->rot) oracle_rotate(tile_rot(P, t), xf, xf);
   for (int i = 0; i < TILE; ++i) z[i] = mask_bit(m, i) ? -xf[i] : xf[i];
   oracle_fwht128(z);
   if (P->dither) oracle_dither(P->lattice, P->dither_seed, P->tile_base + (uint64_t)t, u);
   else for (int i = 0; i < TILE; ++i) u[i] = 0.0f;
+}
+
+/* The lattice-domain values y of one tile (before the nearest point), with
+ * the range rule applied; returns the range flag. */
+static int tile_y(const ora_params *P, const uint16_t *x, int64_t t, float *y) {
+  float z[TILE], u[TILE];
+  tile_zu(P, x, t, z, u);
   float s = oracle_encode_scale(P->alpha);
   int flag = 0;
   for (int i = 0; i < TILE; ++i) {
@@ -988,6 +994,106 @@ int oracle_e8_rule_census(const ora_params *P, const uint16_t *x, int64_t n_tile
   out[0] = C.vectors;
   out[1] = C.differ;
   out[2] = C.coset_differ;
+  dist[0] = C.dist_sum;
+  dist[1] = C.max_abs;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostic, no counterpart in the method: how often the scale and the     */
+/* dither rounded once, y = fl(z s_enc + u) (the reading the codec takes),    */
+/* and rounded twice, y' = fl(fl(z s_enc) + u), lead to different lattice     */
+/* points, and which of the two points is nearer to the exact z s_enc + u.    */
+/* ------------------------------------------------------------------------ */
+/* Codes of one vector of the lattice (dim coordinates). */
+static void vector_codes(int lattice, const float *y, int32_t *v) {
+  if (lattice == ORA_E8) oracle_nearest_e8(y, v);
+  else if (lattice == ORA_D4) oracle_nearest_d4(y, v);
+  else if (lattice == ORA_A2) oracle_nearest_a2(y, v);
+  else v[0] = oracle_nearest_z(y[0]);
+}
+
+/* Squared distance (double) from the exact values ye to the point coded by
+ * v: the codes themselves, except A2's (m, n) = the point (m/2, h n). */
+static double point_dist2(int lattice, const double *ye, const int32_t *v) {
+  const int d = lattice_dim(lattice);
+  double s = 0.0;
+  for (int i = 0; i < d; ++i) {
+    double pt = (double)v[i];
+    if (lattice == ORA_A2) pt = (i == 0) ? 0.5 * v[0] : (double)oracle_a2_point_y(v[1]);
+    s += (ye[i] - pt) * (ye[i] - pt);
+  }
+  return s;
+}
+
+typedef struct {
+  const ora_params *P;
+  const uint16_t *x;
+  pthread_mutex_t mu;
+  int64_t vectors, differ, skipped;
+  double dist_sum, max_abs;
+} rnd_ctx;
+
+static void rounding_range(void *c, int64_t b, int64_t e) {
+  rnd_ctx *C = (rnd_ctx *)c;
+  const int lat = C->P->lattice, d = lattice_dim(lat);
+  const float s = oracle_encode_scale(C->P->alpha);
+  int64_t nv = 0, nd = 0, nk = 0;
+  double ds = 0.0, mx = 0.0;
+  float z[TILE], u[TILE], y1[TILE], y2[TILE];
+  for (int64_t t = b; t < e; ++t) {
+    tile_zu(C->P, C->x + t * TILE, t, z, u);
+    int out = 0;
+    for (int i = 0; i < TILE; ++i) {
+      y1[i] = fmaf(z[i], s, u[i]);
+      const float a = z[i] * s;           /* two roundings (no contraction here) */
+      y2[i] = a + u[i];
+      if (!(fabsf(y1[i]) <= RANGE_LIMIT) || !(fabsf(y2[i]) <= RANGE_LIMIT)) out = 1;
+    }
+    if (out) { ++nk; continue; }          /* the range rule decides such tiles */
+    for (int q = 0; q < TILE; q += d) {
+      int32_t v1[8], v2[8];
+      vector_codes(lat, y1 + q, v1);
+      vector_codes(lat, y2 + q, v2);
+      ++nv;
+      if (memcmp(v1, v2, sizeof(int32_t) * d) != 0) {
+        double ye[8];
+        for (int i = 0; i < d; ++i) ye[i] = (double)z[q + i] * (double)s + (double)u[q + i];
+        const double diff = point_dist2(lat, ye, v2) - point_dist2(lat, ye, v1);
+        ++nd;
+        ds += diff;
+        if (fabs(diff) > mx) mx = fabs(diff);
+      }
+    }
+  }
+  pthread_mutex_lock(&C->mu);
+  C->vectors += nv;
+  C->differ += nd;
+  C->skipped += nk;
+  C->dist_sum += ds;
+  if (mx > C->max_abs) C->max_abs = mx;
+  pthread_mutex_unlock(&C->mu);
+}
+
+/* out[0] = lattice vectors compared, out[1] = vectors whose points differ
+ * between the two roundings, out[2] = tiles left out because either reading
+ * trips the range rule; dist[0] = sum over the differing vectors of the
+ * exact squared distance from z s_enc + u to the twice-rounded reading's
+ * point minus that to the once-rounded reading's point (positive: the
+ * codec's reading is nearer), dist[1] = the largest |.| of one vector. */
+int oracle_scale_rounding_census(const ora_params *P, const uint16_t *x, int64_t n_tiles,
+                                 int64_t *out, double *dist, int nthreads) {
+  if (!params_ok(P) || n_tiles < 0) return -1;
+  rnd_ctx C;
+  memset(&C, 0, sizeof C);
+  C.P = P;
+  C.x = x;
+  pthread_mutex_init(&C.mu, NULL);
+  parallel_for(n_tiles, nthreads, rounding_range, &C);
+  pthread_mutex_destroy(&C.mu);
+  out[0] = C.vectors;
+  out[1] = C.differ;
+  out[2] = C.skipped;
   dist[0] = C.dist_sum;
   dist[1] = C.max_abs;
   return 0;

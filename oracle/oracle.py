@@ -95,6 +95,8 @@ def lib():
             L.oracle_decode_scale.argtypes = [ctypes.c_float]
             L.oracle_e8_rule_census.restype = ctypes.c_int
             L.oracle_e8_rule_census.argtypes = [vp, vp, i64, vp, vp, ctypes.c_int]
+            L.oracle_scale_rounding_census.restype = ctypes.c_int
+            L.oracle_scale_rounding_census.argtypes = [vp, vp, i64, vp, vp, ctypes.c_int]
             L.oracle_e8_plain.argtypes = [vp, vp]
             L.oracle_group_tiles.restype = ctypes.c_int
             L.oracle_range_limit.restype = ctypes.c_float
@@ -301,6 +303,21 @@ def e8_plain(y) -> np.ndarray:
     v = np.zeros(8, np.int32)
     lib().oracle_e8_plain(_p(yy), _p(v))
     return v
+
+
+def scale_rounding_census(P: Params, x_bf16_bits: np.ndarray, threads: int | None = None) -> dict:
+    """Counts, over every lattice vector the oracle codes from these tiles,
+    where the scale and dither rounded once (the codec's reading) and rounded
+    twice pick different points; dist_sum > 0 means the once-rounded points
+    are nearer to the exact values in total (diagnostic)."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16).reshape(-1, 128)
+    out = np.zeros(3, np.int64)
+    dist = np.zeros(2, np.float64)
+    if lib().oracle_scale_rounding_census(ctypes.byref(P), _p(x), x.shape[0], _p(out), _p(dist),
+                                          threads or default_threads()) != 0:
+        raise ValueError("oracle_scale_rounding_census: invalid arguments")
+    return dict(vectors=int(out[0]), differ=int(out[1]), skipped_tiles=int(out[2]),
+                dist_sum=float(dist[0]), dist_max=float(dist[1]))
 
 
 def e8_rule_census(P: Params, x_bf16_bits: np.ndarray, threads: int | None = None) -> dict:

@@ -185,6 +185,28 @@ def test_plain_e8_rule_and_census(oracle):
     assert c["differ"] <= 3 and c["dist_max"] <= 1e-4
 
 
+def test_scale_rounding_census(oracle):
+    """Diagnostic of the reading that scales and dithers in one rounding,
+    y = fl(z s_enc + u), against two roundings, fl(fl(z s_enc) + u): with a
+    power-of-two scale the product is exact and the two agree everywhere; at
+    a coarse scale (few fp32 steps per lattice cell) they pick different
+    points on a few vectors, all near-ties (the two points' squared distances
+    to the exact z s_enc + u within a few fp32 steps of each other), for
+    every lattice."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((4000, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    m = oracle.make_signs(4, 0)
+    P = oracle.make_params(8, 2, float(np.float32(64 * np.sqrt(128.0))), 1, 8, m, 1 << 40)
+    c = oracle.scale_rounding_census(P, x)
+    assert c["vectors"] == 4000 * 16 and c["differ"] == 0
+    for lat, dim in ((8, 8), (4, 4), (2, 2), (1, 1)):
+        P = oracle.make_params(lat, 2, 3000.0, 1, 8, m, 1 << 40)
+        c = oracle.scale_rounding_census(P, x)
+        assert c["vectors"] == 4000 * 128 // dim and c["skipped_tiles"] == 0
+        assert 0 < c["differ"] <= 1e-3 * c["vectors"]
+        assert c["dist_max"] <= 1e-2               # |y| ~ 10^4: fp32 steps of 10^-3
+
+
 def test_e8_ties_and_translation(oracle):
     # exact ties: equidistant from 0 and a minimal vector, or all-integer inputs
     ties = np.array([[1, 1, 0, 0, 0, 0, 0, 0], [0.5] * 8, [1] * 8, [-1, 1, -1, 1, 0, 0, 0, 0],

@@ -356,6 +356,11 @@ def test_kv_cache_8b_e8_rule_census(oracle, rate):
     assert c["vectors"] == xb.shape[0] * 16
     assert c["differ"] <= 1e-6 * c["vectors"]
     assert c["dist_max"] <= 1e-3
+    # the same inputs: scale and dither rounded once (the codec) or twice
+    r = oracle.scale_rounding_census(P, xb)
+    print(f"scale rounding census, KV cache at {rate} bps: {r}")
+    assert r["vectors"] == xb.shape[0] * 16 and r["skipped_tiles"] == 0
+    assert r["differ"] <= 1e-5 * r["vectors"]
 
 
 @pytest.mark.parametrize("rate", ["3.0", "4.0", "5.0"])
