@@ -358,6 +358,8 @@ def run_ours(args, rank, world):
     attn = run_attention(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
     gemm = run_gemm(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
     extra = run_extra_workloads(hq, I, cal, dev) if rank == 0 and not args.skip_fused else None
+    if extra is not None:
+        extra["calibration"] = run_calibration(hq, I, cal, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -699,6 +701,24 @@ def run_extra_workloads(hq, I, cal, dev):
                if f"{nm}@{rate}" in lc]
         order[rate] = {"by_distortion": [nm for _, nm in sorted(got)],
                        "E8<D4<A2<Z": [nm for _, nm in sorted(got)] == ["E8", "D4", "A2", "Z"]}
+    # the per-layer Haar rotation variant on the same layer (one 128 x 128
+    # matrix for the K half and one for the V half), E8 at 3 bps: the dense
+    # product R x runs in fixed-order fp32 FMA chains inside the codec kernels
+    c = cal["long_context"]["E8"]["3.0"]
+    rot = torch.from_numpy(I.haar_rotations(2, seed=321)).to(dev)
+    rsigns = torch.cat([lsigns, lsigns])
+    p = hq.make_params(8, c["k"], c["alpha"], 1, L["dither_seed"], rsigns, n // 2, rot=rot)
+    e, d, bps = _time_codec(hq, p, xt, n, dev)
+    flop = 2.0 * 128 * n * 128                    # one 128 x 128 matrix-vector product per tile
+    out["dense_rotation"] = {
+        "workload": "long-context layer (512 MiB bf16), per-half Haar rotation + dither, E8 3 bps",
+        "encode_ms": round(e, 4), "decode_ms": round(d, 4),
+        "encode_GBps_bf16eq": round(2.0 * n * 128 / (e * 1e-3) / 1e9, 1),
+        "decode_GBps_bf16eq": round(2.0 * n * 128 / (d * 1e-3) / 1e9, 1),
+        "encode_rotation_TFLOPs": round(flop / (e * 1e-3) / 1e12, 2),
+        "decode_rotation_TFLOPs": round(flop / (d * 1e-3) / 1e12, 2),
+        "realized_bps": round(bps, 4), "without_rotation": lc.get("E8@3.0")}
+    del rot
     out["long_context"] = {"workload": "one layer's K and V, 8 heads x 131072 tokens (512 MiB bf16), "
                                        "dither on",
                            "mse_note": "mse = alpha^2 x per-dimension mean squared error of the fp32 "
@@ -708,6 +728,45 @@ def run_extra_workloads(hq, I, cal, dev):
                                        "lattices at each rate",
                            **lc, "distortion_order": order}
     return out
+
+
+def run_calibration(hq, I, cal, dev):
+    """GPU rate calibration (hq_calibrate: bisection of log2 alpha for each
+    Rice k on the size-only encoder) on the KV cache's calibration subset --
+    the first 256 tokens of every layer's K and V slab, 131072 tiles, drawn on
+    the CPU as the frozen calibration drew them -- for 2 and 3 bps: wall time
+    of the call (a host loop that reads every rate back), the alpha and k it
+    finds and whether they are the frozen ones."""
+    import time
+    import numpy as np
+    import torch
+    C = I.KV8B
+    x = torch.cat([I.kv_slab(I.slab_seed(C["data_seed"], layer, kv), C["kv_heads"], 256)
+                   .reshape(-1, 128) for layer in range(C["layers"]) for kv in (0, 1)]).to(dev)
+    xt = x.view(torch.int16)
+    n = xt.shape[0]
+    masks = hq.kv_layer_masks(C["sign_seed"], C["layer_sign_seed"], C["layers"])
+    seg = np.array([masks[layer] for layer in range(C["layers"]) for _ in (0, 1)], np.uint32)
+    signs = torch.from_numpy(seg.view(np.int32).copy()).to(dev)
+    p = hq.make_params(8, 0, 1.0, 1, C["dither_seed"], signs, n // (2 * C["layers"]))
+    ws = torch.zeros(hq.hq_encode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    bits = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {}
+    for target in ("2.0", "3.0"):
+        hq.hq_calibrate(p, xt, n, float(target), 0.002, 0, 8, ws, bits, st)   # warm-up
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        rc, out = hq.hq_calibrate(p, xt, n, float(target), 0.002, 0, 8, ws, bits, st)
+        ms = (time.perf_counter() - t0) * 1e3
+        fz = cal["kv_cache_8b"]["E8"][target]
+        res[target] = {"ms": round(ms, 2), "size_mode_encodes": int(out.evaluations),
+                       "alpha": round(float(out.alpha), 6), "k": int(out.rice_k),
+                       "bps": round(float(out.bps), 4), "frozen": {"alpha": fz["alpha"], "k": fz["k"]},
+                       "matches_frozen": bool(rc == 0 and out.feasible == 1 and out.rice_k == fz["k"]
+                                              and abs(out.alpha - fz["alpha"]) <= 1e-3 * fz["alpha"])}
+    return {"workload": "KV-cache calibration subset: 256 tokens of each of 64 K/V slabs, "
+                        "131072 tiles, E8, dither, k in 0..8, tolerance 0.002 bps", **res}
 
 
 def run_gemm(hq, I, cal, dev):
