@@ -13,10 +13,10 @@
 
 namespace hq {
 
-// ROT: the dense-rotation variant (an instance of its own, 2 blocks per SM
-// with the registers of its 4 x 8 product tile; runtime k only).
+// ROT: the dense-rotation variant (an instance of its own, 4 blocks per SM
+// with the registers of its 4 x 4 product tile; runtime k only).
 template <int LAT, int K, bool ROT>
-__global__ void __launch_bounds__(kDecThreads, ROT ? 2 : 8)
+__global__ void __launch_bounds__(kDecThreads, ROT ? 4 : 8)
 decode_kernel(DecodeArgs a) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
@@ -35,11 +35,8 @@ decode_kernel(DecodeArgs a) {
                                        ((tid >> 3) & 1)] =
         __uint_as_float(__float_as_uint(a.s_dec) ^ (((mword >> (tid & 31)) & 1u) << 31));
   }
-  constexpr int kRS = kTile + 4;                 // row stride of the rotation's operands
-  extern __shared__ __align__(16) float s_dyn[];  // ROT: y [32][kRS], then R [128][kRS]
-  if constexpr (ROT)                             // R arrives while the group is decoded
-    rot_load_async(s_dyn + kGroupTiles * kRS, a.rot + seg0 * (int64_t)(kTile * kTile), kRS, tid,
-                   kDecThreads);
+  constexpr int kRS = kTile + 4;                 // row stride of the rotation's operand
+  extern __shared__ __align__(16) float s_dyn[];  // ROT: y [32][kRS]
   float e[16];
   const bool ok = decode_lane<LAT, K>(a, g, e, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
@@ -66,14 +63,14 @@ decode_kernel(DecodeArgs a) {
     }
   }
   if constexpr (ROT) {                           // x_hat = R^T y, chains over i
-    // [32 tiles x 128] x [128 x 128] in shared memory: y row-major [32][132]
-    // (later reused for the result) and R row-major [128][132]
+    // [32 tiles x 128] x [128 x 128]: y row-major [32][132] in shared memory
+    // (later reused for the result), the segment's R row-major through L1
+    // (every block of the segment reads the same 64 KB)
     float *s_y = s_dyn;
-    const float *s_r = s_dyn + kGroupTiles * kRS;
+    const float *Rg = a.rot + seg0 * (int64_t)(kTile * kTile);
     float4 *dy = reinterpret_cast<float4 *>(s_y + tl * kRS + 16 * r);
 #pragma unroll
     for (int c = 0; c < 4; ++c) dy[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
-    rot_wait();
     __syncthreads();
     // thread (tg, oh, l16): tiles 4 tg .. 4 tg + 3 x outputs 64 oh + 4 l16 .. +3,
     // each one fma chain over i = 0..127 from +0
@@ -91,7 +88,7 @@ decode_kernel(DecodeArgs a) {
         yv[u] = *reinterpret_cast<const float4 *>(s_y + (4 * tg + u) * kRS + i);
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii) {
-        const float4 rr = *reinterpret_cast<const float4 *>(s_r + (i + ii) * kRS + ob);
+        const float4 rr = __ldg(reinterpret_cast<const float4 *>(Rg + (i + ii) * kTile + ob));
         const float rs[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -135,7 +132,7 @@ decode_kernel(DecodeArgs a) {
   }
 }
 
-constexpr size_t kDecRotSmemBytes = (size_t)((kGroupTiles + kTile) * (kTile + 4)) * 4;
+constexpr size_t kDecRotSmemBytes = (size_t)(kGroupTiles * (kTile + 4)) * 4;
 
 template <int LAT, int K, bool ROT = false>
 static void launch_dec_one(const DecodeArgs &a, cudaStream_t st) {
