@@ -25,11 +25,30 @@ constexpr int kEncThreads = 256;                 // one group of 32 tiles
 constexpr int kStageWords = 4096;                // 16 KiB of output per window
 constexpr int kKmaxTemplated = 8;                // Rice k specialised at compile time
 // Dense rotation (optional), as a [32 tiles x 128] x [128 x 128] product in
-// shared memory: the tiles transposed [128][36] (later reused for the result
-// [32][132]) and the segment's R transposed [128][132].
+// shared memory: the group's tiles [32][132] in the staging window (unused
+// until the transform; later reused for the result), and the segment's R
+// streamed in chunks of 16 columns, [128][20] each, two in flight
+// (asynchronous copies): rows 80 bytes apart put the 16 rows a warp reads
+// per request in two bank-conflict-free halves.
 constexpr int kRotStride = kTile + 4;
 constexpr int kRotXFloats = kGroupTiles * kRotStride;               // the group's tiles, then R x
-constexpr size_t kEncRotSmemBytes = (size_t)(kRotXFloats + kTile * kRotStride) * 4;
+constexpr int kRotChunk = 16, kRotChunkStride = kRotChunk + 4;
+constexpr int kRotChunkFloats = kTile * kRotChunkStride;
+constexpr size_t kEncRotSmemBytes = (size_t)(2 * kRotChunkFloats) * 4;
+
+// Columns 16 q .. 16 q + 15 of R (row-major, 16-byte aligned) into a chunk
+// buffer, 16-byte asynchronous copies by all threads; one commit group.
+__device__ __forceinline__ void rot_chunk_async(float *dst, const float *R, int q, int tid) {
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(dst);
+  for (int idx = tid; idx < kTile * kRotChunk / 4; idx += kEncThreads) {
+    const int row = idx >> 2, c4 = idx & 3;
+    const uint32_t d = base + 4u * (uint32_t)(row * kRotChunkStride + 4 * c4);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
+                 "l"(R + row * kTile + kRotChunk * q + 4 * c4)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 constexpr uint64_t kFlagAgg = 1ull << 62;        // look-back state: [63:62] flag
 constexpr uint64_t kFlagPrefix = 2ull << 62;     //                  [61:0] words
@@ -223,10 +242,10 @@ __device__ __forceinline__ void put_unary8(BitOut &o, const uint32_t s[8], int k
   }
 }
 
-// ROT: the dense-rotation variant (an instance of its own, 2 blocks per SM
-// with the registers of its 4 x 8 product tile; runtime k only).
+// ROT: the dense-rotation variant (an instance of its own, 4 blocks per SM
+// with the registers of its 4 x 4 product tile; runtime k only).
 template <int LAT, int K, bool ROT>
-__global__ void __launch_bounds__(kEncThreads, ROT ? 2 : 6)
+__global__ void __launch_bounds__(kEncThreads, ROT ? 4 : 6)
 encode_kernel(EncodeArgs a) {
   // staging window of the group's words; before that, the tile transposes of the transform
   __shared__ __align__(16) uint32_t s_stage[kStageWords > kGroupTiles * kTrTile ? kStageWords : kGroupTiles * kTrTile];
@@ -268,10 +287,9 @@ encode_kernel(EncodeArgs a) {
   }
   // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
   const int64_t seg0 = div_by(t0, a.tiles_per_segment, a.seg_shift);
-  if constexpr (ROT) {                           // R arrives while the tiles are staged
+  if constexpr (ROT) {                           // R's first chunk arrives while the tiles are staged
     extern __shared__ __align__(16) float s_dyn_r[];   // the group is in one segment
-    rot_load_async(s_dyn_r + kRotXFloats, a.rot + seg0 * (int64_t)(kTile * kTile), kRotStride, tid,
-                   kEncThreads);
+    rot_chunk_async(s_dyn_r, a.rot + seg0 * (int64_t)(kTile * kTile), 0, tid);
   }
   if (tid < kTile / 2) {
     const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
@@ -284,9 +302,10 @@ encode_kernel(EncodeArgs a) {
   // ---- optional dense rotation R x (before the sign mask)
   float x[16];
   if constexpr (ROT) {
-    extern __shared__ __align__(16) float s_dyn[];
-    float *s_x = s_dyn;                          // [32][132]: coordinate j of tile t at [t][j]
-    const float *s_r = s_dyn + kRotXFloats;      // [128][132]: R[i][j] at [i][j]
+    extern __shared__ __align__(16) float s_dyn[];   // two chunks of R: [128][20] each
+    const float *Rg = a.rot + seg0 * (int64_t)(kTile * kTile);
+    float *s_x = reinterpret_cast<float *>(s_stage);   // [32][132]: coordinate j of tile t at [t][j]
+    static_assert(kRotXFloats <= (int)(sizeof(s_stage) / 4), "the tiles fit the staging window");
     {
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       float4 *dst = reinterpret_cast<float4 *>(s_x + tl * kRotStride + 16 * r);
@@ -296,8 +315,6 @@ encode_kernel(EncodeArgs a) {
                              __uint_as_float(w[2 * c + 1] << 16),
                              __uint_as_float(w[2 * c + 1] & 0xFFFF0000u));
     }
-    rot_wait();                                  // R was issued at the start of the block
-    __syncthreads();
     // thread (tg, oh, l16): tiles 4 tg .. 4 tg + 3 x outputs 64 oh + l16 + 16 c
     // (c = 0..3), each output one fma chain over j = 0..127 from +0
     const int tg = (tid >> 4) & 7, ob = 64 * (tid >> 7) + (tid & 15);
@@ -306,27 +323,36 @@ encode_kernel(EncodeArgs a) {
     for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-#pragma unroll 2
-    for (int j = 0; j < kTile; j += 4) {
-      float4 xv[4], rv[4];
+#pragma unroll 1
+    for (int q = 0; q < kTile / kRotChunk; ++q) {
+      // chunk q has landed (chunk q + 1 is issued once every thread is past
+      // chunk q - 1, whose buffer it reuses)
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();
+      if (q + 1 < kTile / kRotChunk) rot_chunk_async(s_dyn + ((q + 1) & 1) * kRotChunkFloats, Rg, q + 1, tid);
+      const float *s_r = s_dyn + (q & 1) * kRotChunkFloats;   // [128][20]: R[i][16 q + jj] at [i][jj]
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        xv[u] = *reinterpret_cast<const float4 *>(s_x + (4 * tg + u) * kRotStride + j);
+      for (int jj = 0; jj < kRotChunk; jj += 4) {
+        const int j = kRotChunk * q + jj;
+        float4 xv[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        rv[c] = *reinterpret_cast<const float4 *>(s_r + (ob + 16 * c) * kRotStride + j);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 4; ++u)
+          xv[u] = *reinterpret_cast<const float4 *>(s_x + (4 * tg + u) * kRotStride + j);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          acc[u][c] = __fmaf_rn(rv[c].x, xv[u].x, acc[u][c]);
-          acc[u][c] = __fmaf_rn(rv[c].y, xv[u].y, acc[u][c]);
-          acc[u][c] = __fmaf_rn(rv[c].z, xv[u].z, acc[u][c]);
-          acc[u][c] = __fmaf_rn(rv[c].w, xv[u].w, acc[u][c]);
+          const float4 rv = *reinterpret_cast<const float4 *>(s_r + (ob + 16 * c) * kRotChunkStride + jj);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[u][c] = __fmaf_rn(rv.x, xv[u].x, acc[u][c]);
+            acc[u][c] = __fmaf_rn(rv.y, xv[u].y, acc[u][c]);
+            acc[u][c] = __fmaf_rn(rv.z, xv[u].z, acc[u][c]);
+            acc[u][c] = __fmaf_rn(rv.w, xv[u].w, acc[u][c]);
+          }
         }
+      }
     }
     __syncthreads();                             // the tile area becomes the result area
-    float *s_z = s_dyn;                          // [32][132]
+    float *s_z = s_x;                            // [32][132]
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -341,6 +367,7 @@ encode_kernel(EncodeArgs a) {
       z[4 * c + 2] = q.z;
       z[4 * c + 3] = q.w;
     }
+    __syncthreads();                             // every row is read before the transposes reuse the window
     const uint4 s0 = s_signx[r], s1 = s_signx[8 + r];
     const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
