@@ -17,22 +17,6 @@ constexpr uint32_t kSymbolLimit = 1u << 22;      // no valid symbol reaches 2^22
 constexpr float kMagic1 = 12582912.0f;           // 1.5 * 2^23: round to integer
 constexpr float kMagic2 = 25165824.0f;           // 1.5 * 2^24: round to even integer
 
-// ---------------------------------------------------------------- dense rotation
-// Asynchronous copy of the 128 x 128 fp32 rotation R (row-major, 16-byte
-// aligned) into shared memory rows of `stride` floats: 16-byte cp.async per
-// element group, issued by all `nthreads` threads; rot_wait() completes this
-// thread's copies (a barrier then publishes them to the block).
-__device__ __forceinline__ void rot_load_async(float *dst, const float *R, int stride, int tid,
-                                               int nthreads) {
-  const uint32_t base = (uint32_t)__cvta_generic_to_shared(dst);
-  for (int idx = tid; idx < 128 * 128 / 4; idx += nthreads) {
-    const uint32_t d = base + 4u * (uint32_t)((idx >> 5) * stride + 4 * (idx & 31));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(R + 4 * idx) : "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void rot_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // ---------------------------------------------------------------- Philox4x32-10
 // Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
 // (SC'11): 10 rounds of the 4x32 bijection with multipliers D2511F53 and
