@@ -647,54 +647,77 @@ __global__ void rotate_x_kernel(GemmArgs a) {
   for (int k = 0; k < 128; ++k) a.xrot[i * kTile + k] = __fmul_rn(x[k], a.dec.s_dec);
 }
 
-// Each tile's share of y: lane r of tile t holds 16 lattice-domain values;
-// partial dots with 8 activation rows at a time are reduced over the tile's
-// 8 lanes by a butterfly that leaves one finished row on each lane.
-template <int LAT, int K>
-__global__ void __launch_bounds__(kDecThreads, 3) gemm_kernel(GemmArgs a) {
+// Each tile's share of y.  With PAIR (two or more activation rows) a block
+// takes two groups whose tiles fall on the same column blocks -- groups d
+// apart, d = tpr / gcd(tpr, 32) -- so each lane's slice of the rotated
+// activations serves two weight tiles and is read from L2 once for both;
+// without, one group.  Lane r of tile t holds 16 lattice-domain values of
+// each tile; partial dots with 8 activation rows at a time are reduced over
+// the tile's 8 lanes by a butterfly that leaves one finished row on each lane.
+template <int LAT, int K, bool PAIR>
+__global__ void __launch_bounds__(kDecThreads, 3) gemm_kernel(GemmArgs a, int pair_d) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
-  const int64_t g = blockIdx.x;
-  float e[16];
-  const bool ok = decode_lane<LAT, K>(a.dec, g, e, s_start, s_warp);   // barriers inside
+  const int64_t bq = PAIR ? blockIdx.x / pair_d : blockIdx.x, bm = PAIR ? blockIdx.x - bq * pair_d : 0;
+  const int64_t gA = PAIR ? 2 * pair_d * bq + bm : bq, gB = gA + pair_d;
+  if (gA >= a.dec.n_groups) return;              // uniform
+  const bool hasB = PAIR && gB < a.dec.n_groups;   // uniform
+  float eA[16], eB[16];
+  bool ok = decode_lane<LAT, K>(a.dec, gA, eA, s_start, s_warp);   // barriers inside
+  if (hasB) {
+    ok = decode_lane<LAT, K>(a.dec, gB, eB, s_start, s_warp) && ok;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) eB[i] = 0.0f;
+  }
   if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-  const int64_t tile = g * kGroupTiles + tl;
-  const bool valid = tile < a.dec.n_tiles;
-  const int64_t row = valid ? div_by(tile, a.tpr, a.tpr_shift) : 0;
-  const int64_t j = valid ? tile - row * a.tpr : 0;
+  const int64_t tileA = gA * kGroupTiles + tl, tileB = gB * kGroupTiles + tl;
+  const bool validA = tileA < a.dec.n_tiles, validB = hasB && tileB < a.dec.n_tiles;
+  const int64_t row = validA ? div_by(tileA, a.tpr, a.tpr_shift) : 0;
+  const int64_t j = validA ? tileA - row * a.tpr : 0;   // tile B's column block too
   for (int b0 = 0; b0 < a.B; b0 += 8) {
-    float p[8];
+    float pA[8], pB[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float acc = 0.0f;
+      float accA = 0.0f, accB = 0.0f;
       if (b0 + i < a.B) {
         const float4 *xr = reinterpret_cast<const float4 *>(
             a.xrot + (int64_t)(b0 + i) * a.cols + j * kTile + 16 * r);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const float4 xv = __ldg(xr + c);
-          acc = __fmaf_rn(xv.x, e[4 * c], acc);
-          acc = __fmaf_rn(xv.y, e[4 * c + 1], acc);
-          acc = __fmaf_rn(xv.z, e[4 * c + 2], acc);
-          acc = __fmaf_rn(xv.w, e[4 * c + 3], acc);
+          accA = __fmaf_rn(xv.x, eA[4 * c], accA);
+          accA = __fmaf_rn(xv.y, eA[4 * c + 1], accA);
+          accA = __fmaf_rn(xv.z, eA[4 * c + 2], accA);
+          accA = __fmaf_rn(xv.w, eA[4 * c + 3], accA);
+          accB = __fmaf_rn(xv.x, eB[4 * c], accB);
+          accB = __fmaf_rn(xv.y, eB[4 * c + 1], accB);
+          accB = __fmaf_rn(xv.z, eB[4 * c + 2], accB);
+          accB = __fmaf_rn(xv.w, eB[4 * c + 3], accB);
         }
       }
-      p[i] = acc;
+      pA[i] = accA;
+      pB[i] = accB;
     }
 #pragma unroll
     for (int m = 4; m >= 1; m >>= 1) {
 #pragma unroll
       for (int i = 0; i < m; ++i) {
         const bool upper = (r & m) != 0;
-        const float send = upper ? p[i] : p[i + m];
-        const float keep = upper ? p[i + m] : p[i];
-        const float got = __shfl_xor_sync(0xffffffffu, send, m);
-        p[i] = __fadd_rn(keep, got);
+        const float sendA = upper ? pA[i] : pA[i + m], keepA = upper ? pA[i + m] : pA[i];
+        const float sendB = upper ? pB[i] : pB[i + m], keepB = upper ? pB[i + m] : pB[i];
+        const float gotA = __shfl_xor_sync(0xffffffffu, sendA, m);
+        const float gotB = __shfl_xor_sync(0xffffffffu, sendB, m);
+        pA[i] = __fadd_rn(keepA, gotA);
+        pB[i] = __fadd_rn(keepB, gotB);
       }
     }
     const int b = b0 + r;                        // slot kept by lane r is row b0 + r
-    if (valid && b < a.B) a.partial[(int64_t)b * a.dec.n_tiles + tile] = p[0];
+    if (b < a.B) {
+      if (validA) a.partial[(int64_t)b * a.dec.n_tiles + tileA] = pA[0];
+      if (validB) a.partial[(int64_t)b * a.dec.n_tiles + tileB] = pB[0];
+    }
   }
 }
 
@@ -795,15 +818,33 @@ static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
   }
 }
 
+template <int LAT, bool PAIR>
+static void launch_gemm_k(const GemmArgs &a, int64_t blocks, int d, cudaStream_t st) {
+  dim3 grid((unsigned)blocks), block(kDecThreads);
+  switch (a.dec.rice_k) {
+    case 2: gemm_kernel<LAT, 2, PAIR><<<grid, block, 0, st>>>(a, d); break;
+    case 3: gemm_kernel<LAT, 3, PAIR><<<grid, block, 0, st>>>(a, d); break;
+    case 4: gemm_kernel<LAT, 4, PAIR><<<grid, block, 0, st>>>(a, d); break;
+    default: gemm_kernel<LAT, -1, PAIR><<<grid, block, 0, st>>>(a, d); break;
+  }
+}
+
 template <int LAT>
 static void launch_gemm_lat(const GemmArgs &a, cudaStream_t st) {
-  dim3 grid((unsigned)a.dec.n_groups), block(kDecThreads);
-  switch (a.dec.rice_k) {
-    case 2: gemm_kernel<LAT, 2><<<grid, block, 0, st>>>(a); break;
-    case 3: gemm_kernel<LAT, 3><<<grid, block, 0, st>>>(a); break;
-    case 4: gemm_kernel<LAT, 4><<<grid, block, 0, st>>>(a); break;
-    default: gemm_kernel<LAT, -1><<<grid, block, 0, st>>>(a); break;
+  // groups d apart cover the same column blocks: 32 d is the first multiple
+  // of tpr that is a multiple of 32
+  int64_t g = 32, t = a.tpr;
+  while (t != 0) {
+    const int64_t m = g % t;
+    g = t;
+    t = m;
   }
+  const int d = (int)(a.tpr / g);
+  if (a.B < 2) {                                 // one activation row: a group per block
+    launch_gemm_k<LAT, false>(a, a.dec.n_groups, d, st);
+    return;
+  }
+  launch_gemm_k<LAT, true>(a, (a.dec.n_groups + 2 * d - 1) / (2 * d) * d, d, st);
 }
 
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
