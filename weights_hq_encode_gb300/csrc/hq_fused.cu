@@ -647,76 +647,82 @@ __global__ void rotate_x_kernel(GemmArgs a) {
   for (int k = 0; k < 128; ++k) a.xrot[i * kTile + k] = __fmul_rn(x[k], a.dec.s_dec);
 }
 
-// Each tile's share of y.  With PAIR (two or more activation rows) a block
-// takes two groups whose tiles fall on the same column blocks -- groups d
-// apart, d = tpr / gcd(tpr, 32) -- so each lane's slice of the rotated
-// activations serves two weight tiles and is read from L2 once for both;
-// without, one group.  Lane r of tile t holds 16 lattice-domain values of
-// each tile; partial dots with 8 activation rows at a time are reduced over
-// the tile's 8 lanes by a butterfly that leaves one finished row on each lane.
-template <int LAT, int K, bool PAIR>
-__global__ void __launch_bounds__(kDecThreads, 3) gemm_kernel(GemmArgs a, int pair_d) {
+// Each tile's share of y.  A block decodes NG groups d apart, d = tpr /
+// gcd(tpr, 32) -- their tiles fall on the same column blocks -- so each
+// lane's slice of the rotated activations, read from L2 once, serves NG
+// weight tiles (NG = 1 for a single activation row).  Lane r of tile t holds
+// 16 lattice-domain values of each tile; partial dots with 8 activation rows
+// at a time are reduced over the tile's 8 lanes by a butterfly that leaves
+// one finished row on each lane.
+template <int LAT, int K, int NG>
+__global__ void __launch_bounds__(kDecThreads, NG > 2 ? 2 : 3) gemm_kernel(GemmArgs a, int pair_d) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
-  const int64_t bq = PAIR ? blockIdx.x / pair_d : blockIdx.x, bm = PAIR ? blockIdx.x - bq * pair_d : 0;
-  const int64_t gA = PAIR ? 2 * pair_d * bq + bm : bq, gB = gA + pair_d;
-  if (gA >= a.dec.n_groups) return;              // uniform
-  const bool hasB = PAIR && gB < a.dec.n_groups;   // uniform
-  float eA[16], eB[16];
-  bool ok = decode_lane<LAT, K>(a.dec, gA, eA, s_start, s_warp);   // barriers inside
-  if (hasB) {
-    ok = decode_lane<LAT, K>(a.dec, gB, eB, s_start, s_warp) && ok;
-  } else {
+  const int64_t bq = blockIdx.x / pair_d, bm = blockIdx.x - bq * pair_d;
+  const int64_t g0 = NG * pair_d * bq + bm;      // groups g0 + n d, n < NG
+  if (g0 >= a.dec.n_groups) return;              // uniform
+  float e[NG][16];
+  bool ok = true;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) eB[i] = 0.0f;
+  for (int n = 0; n < NG; ++n) {
+    const int64_t g = g0 + (int64_t)n * pair_d;
+    if (g < a.dec.n_groups) {                    // uniform
+      ok = decode_lane<LAT, K>(a.dec, g, e[n], s_start, s_warp) && ok;   // barriers inside
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) e[n][i] = 0.0f;
+    }
   }
   if (!ok && tid == 0) atomicOr(a.dec.status, (uint32_t)HQ_ERR_CORRUPT);
-  const int64_t tileA = gA * kGroupTiles + tl, tileB = gB * kGroupTiles + tl;
-  const bool validA = tileA < a.dec.n_tiles, validB = hasB && tileB < a.dec.n_tiles;
-  const int64_t row = validA ? div_by(tileA, a.tpr, a.tpr_shift) : 0;
-  const int64_t j = validA ? tileA - row * a.tpr : 0;   // tile B's column block too
+  const int64_t tile0 = g0 * kGroupTiles + tl;
+  const int64_t row = tile0 < a.dec.n_tiles ? div_by(tile0, a.tpr, a.tpr_shift) : 0;
+  const int64_t j = tile0 < a.dec.n_tiles ? tile0 - row * a.tpr : 0;   // every tile's column block
   for (int b0 = 0; b0 < a.B; b0 += 8) {
-    float pA[8], pB[8];
+    float p[NG][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float accA = 0.0f, accB = 0.0f;
+      float acc[NG];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) acc[n] = 0.0f;
       if (b0 + i < a.B) {
         const float4 *xr = reinterpret_cast<const float4 *>(
             a.xrot + (int64_t)(b0 + i) * a.cols + j * kTile + 16 * r);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const float4 xv = __ldg(xr + c);
-          accA = __fmaf_rn(xv.x, eA[4 * c], accA);
-          accA = __fmaf_rn(xv.y, eA[4 * c + 1], accA);
-          accA = __fmaf_rn(xv.z, eA[4 * c + 2], accA);
-          accA = __fmaf_rn(xv.w, eA[4 * c + 3], accA);
-          accB = __fmaf_rn(xv.x, eB[4 * c], accB);
-          accB = __fmaf_rn(xv.y, eB[4 * c + 1], accB);
-          accB = __fmaf_rn(xv.z, eB[4 * c + 2], accB);
-          accB = __fmaf_rn(xv.w, eB[4 * c + 3], accB);
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {
+            acc[n] = __fmaf_rn(xv.x, e[n][4 * c], acc[n]);
+            acc[n] = __fmaf_rn(xv.y, e[n][4 * c + 1], acc[n]);
+            acc[n] = __fmaf_rn(xv.z, e[n][4 * c + 2], acc[n]);
+            acc[n] = __fmaf_rn(xv.w, e[n][4 * c + 3], acc[n]);
+          }
         }
       }
-      pA[i] = accA;
-      pB[i] = accB;
+#pragma unroll
+      for (int n = 0; n < NG; ++n) p[n][i] = acc[n];
     }
 #pragma unroll
     for (int m = 4; m >= 1; m >>= 1) {
 #pragma unroll
       for (int i = 0; i < m; ++i) {
         const bool upper = (r & m) != 0;
-        const float sendA = upper ? pA[i] : pA[i + m], keepA = upper ? pA[i + m] : pA[i];
-        const float sendB = upper ? pB[i] : pB[i + m], keepB = upper ? pB[i + m] : pB[i];
-        const float gotA = __shfl_xor_sync(0xffffffffu, sendA, m);
-        const float gotB = __shfl_xor_sync(0xffffffffu, sendB, m);
-        pA[i] = __fadd_rn(keepA, gotA);
-        pB[i] = __fadd_rn(keepB, gotB);
+#pragma unroll
+        for (int n = 0; n < NG; ++n) {
+          const float send = upper ? p[n][i] : p[n][i + m], keep = upper ? p[n][i + m] : p[n][i];
+          p[n][i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+        }
       }
     }
     const int b = b0 + r;                        // slot kept by lane r is row b0 + r
     if (b < a.B) {
-      if (validA) a.partial[(int64_t)b * a.dec.n_tiles + tileA] = pA[0];
-      if (validB) a.partial[(int64_t)b * a.dec.n_tiles + tileB] = pB[0];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) {
+        const int64_t tile = tile0 + (int64_t)n * pair_d * kGroupTiles;
+        if (g0 + (int64_t)n * pair_d < a.dec.n_groups && tile < a.dec.n_tiles)
+          a.partial[(int64_t)b * a.dec.n_tiles + tile] = p[n][0];
+      }
     }
   }
 }
@@ -818,14 +824,17 @@ static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
   }
 }
 
-template <int LAT, bool PAIR>
-static void launch_gemm_k(const GemmArgs &a, int64_t blocks, int d, cudaStream_t st) {
+constexpr int kGemmFourGroupRows = 16;  // from this many activation rows on, four groups a block
+
+template <int LAT, int NG>
+static void launch_gemm_k(const GemmArgs &a, int d, cudaStream_t st) {
+  const int64_t blocks = (a.dec.n_groups + NG * d - 1) / (NG * d) * d;
   dim3 grid((unsigned)blocks), block(kDecThreads);
   switch (a.dec.rice_k) {
-    case 2: gemm_kernel<LAT, 2, PAIR><<<grid, block, 0, st>>>(a, d); break;
-    case 3: gemm_kernel<LAT, 3, PAIR><<<grid, block, 0, st>>>(a, d); break;
-    case 4: gemm_kernel<LAT, 4, PAIR><<<grid, block, 0, st>>>(a, d); break;
-    default: gemm_kernel<LAT, -1, PAIR><<<grid, block, 0, st>>>(a, d); break;
+    case 2: gemm_kernel<LAT, 2, NG><<<grid, block, 0, st>>>(a, d); break;
+    case 3: gemm_kernel<LAT, 3, NG><<<grid, block, 0, st>>>(a, d); break;
+    case 4: gemm_kernel<LAT, 4, NG><<<grid, block, 0, st>>>(a, d); break;
+    default: gemm_kernel<LAT, -1, NG><<<grid, block, 0, st>>>(a, d); break;
   }
 }
 
@@ -840,11 +849,9 @@ static void launch_gemm_lat(const GemmArgs &a, cudaStream_t st) {
     t = m;
   }
   const int d = (int)(a.tpr / g);
-  if (a.B < 2) {                                 // one activation row: a group per block
-    launch_gemm_k<LAT, false>(a, a.dec.n_groups, d, st);
-    return;
-  }
-  launch_gemm_k<LAT, true>(a, (a.dec.n_groups + 2 * d - 1) / (2 * d) * d, d, st);
+  if (a.B < 2) launch_gemm_k<LAT, 1>(a, d, st);          // one activation row: decoding bounds it
+  else if (a.B < kGemmFourGroupRows) launch_gemm_k<LAT, 2>(a, d, st);
+  else launch_gemm_k<LAT, 4>(a, d, st);
 }
 
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
