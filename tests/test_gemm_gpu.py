@@ -73,6 +73,7 @@ def _check(G, what, xb, rows, cols, y, rot=False):
 @pytest.mark.parametrize("index,rows,B,rate,lattice,dither", [
     (0, 64, 1, "4.0", 8, 0),      # 4096 columns: one row per group
     (2, 33, 5, "3.0", 8, 0),      # 14336 columns: rows straddle groups
+    (2, 33, 16, "3.0", 8, 1),     # the same with four groups a block (ragged last blocks)
     (3, 100, 17, "5.0", 8, 1),    # 4096 columns, three batch chunks, dither on
     (1, 50, 3, "4.0", 4, 0),      # D4
     (0, 20, 2, "4.0", 1, 0),      # Z
