@@ -200,7 +200,11 @@ def run_ours(args, rank, world):
     import torch.distributed as dist
 
     from weights_hq_encode_gb300 import build
+    if world > 1 and rank != 0:
+        dist.barrier()                               # rank 0 builds (or finds) the library first
     build.build()
+    if world > 1 and rank == 0:
+        dist.barrier()
     from weights_hq_encode_gb300 import hq, inputs as I
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
