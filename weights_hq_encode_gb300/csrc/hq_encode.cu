@@ -254,9 +254,10 @@ encode_kernel(EncodeArgs a) {
   __shared__ uint64_t s_base, s_words;
   __shared__ uint32_t s_ticket, s_flags;
   __shared__ int s_ok;
-  // sign XOR words of the first segment; lane r's two 16-byte blocks sit at
-  // r and 8 + r, so the 8 lanes of a tile read 128 contiguous bytes
-  __shared__ uint4 s_signx[kTile / 8];
+  // (dense rotation) sign XOR words of the segment; lane r's two 16-byte
+  // blocks sit at r and 8 + r, so the 8 lanes of a tile read 128 contiguous
+  // bytes
+  __shared__ uint4 s_signx[ROT ? kTile / 8 : 1];
 
 
   const int tid = threadIdx.x, lane = tid & 31, tl = tid >> 3, r = tid & 7;
@@ -267,37 +268,43 @@ encode_kernel(EncodeArgs a) {
   // progress whatever order the hardware starts blocks in.  (A counter set
   // ahead by the caller leaves groups unprocessed, which the bounded waits
   // turn into HQ_ERR_TIMEOUT.)
-  if (tid == 0) s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
+  if (tid == 0) {
+    s_ticket = atomicAdd(reinterpret_cast<unsigned int *>(a.ws), 1u);
+    s_flags = 0u;
+  }
   __syncthreads();
   const uint32_t g = s_ticket;
-  if (tid == 0) s_flags = 0u;
   if (g >= a.n_blocks) return;                   // only with a counter set ahead
   const int k = K >= 0 ? K : a.rice_k;
   const int64_t t0 = (int64_t)g * kGroupTiles;
   const int nt = (int)min((int64_t)kGroupTiles, a.n_tiles - t0);
   const int64_t t = t0 + tl;
   const bool valid = tl < nt;
-  // the lane's 16 bf16 coordinates, loaded before the sign table is built so
-  // that the two loads overlap
+  // the lane's 16 bf16 coordinates and (without the rotation) the 16 sign
+  // bits of its tile's mask, loaded together
   uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+  uint32_t mw = 0u;
   if (valid) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * kTile + 16 * r);
     v0 = __ldg(src);
     v1 = __ldg(src + 1);
+    if constexpr (!ROT)
+      mw = __ldg(a.signs + 4 * div_by(t, a.tiles_per_segment, a.seg_shift) + (r >> 1)) >> (16 * (r & 1));
   }
-  // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
   const int64_t seg0 = div_by(t0, a.tiles_per_segment, a.seg_shift);
   if constexpr (ROT) {                           // R's first chunk arrives while the tiles are staged
     extern __shared__ __align__(16) float s_dyn_r[];   // the group is in one segment
     rot_chunk_async(s_dyn_r, a.rot + seg0 * (int64_t)(kTile * kTile), 0, tid);
   }
-  if (tid < kTile / 2) {
-    const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
-    // word tid = pair q = tid & 7 of lane r = tid >> 3
-    reinterpret_cast<uint32_t *>(s_signx)[32 * ((tid & 7) >> 2) + 4 * (tid >> 3) + (tid & 3)] =
-        (((mword >> (2 * (tid & 15))) & 3u) * 0x40008000u) & 0x80008000u;
+  if constexpr (ROT) {                           // the rotation applies the signs after its product
+    if (tid < kTile / 2) {
+      const uint32_t mword = __ldg(a.signs + 4 * seg0 + (tid >> 4));
+      // word tid = pair q = tid & 7 of lane r = tid >> 3
+      reinterpret_cast<uint32_t *>(s_signx)[32 * ((tid & 7) >> 2) + 4 * (tid >> 3) + (tid & 3)] =
+          (((mword >> (2 * (tid & 15))) & 3u) * 0x40008000u) & 0x80008000u;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- optional dense rotation R x (before the sign mask)
   float x[16];
@@ -376,21 +383,11 @@ encode_kernel(EncodeArgs a) {
       x[2 * q + 1] = __uint_as_float(__float_as_uint(z[2 * q + 1]) ^ (sw[q] & 0x80000000u));
     }
   } else if (valid) {
-    uint32_t sw[8];
-    if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
-      const uint4 s0 = s_signx[r], s1 = s_signx[8 + r];
-      sw[0] = s0.x; sw[1] = s0.y; sw[2] = s0.z; sw[3] = s0.w;
-      sw[4] = s1.x; sw[5] = s1.y; sw[6] = s1.z; sw[7] = s1.w;
-    } else {
-      const uint32_t *mask = a.signs + 4 * (div_by(t, a.tiles_per_segment, a.seg_shift));
-      const uint32_t mw = __ldg(mask + (r >> 1)) >> (16 * (r & 1));
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sw[q] = (((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u;
-    }
+    // sign bits of coordinates 2q, 2q+1 moved to bit 15 / bit 31 of a bf16 pair
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const uint32_t ww = w[q] ^ sw[q];
+      const uint32_t ww = w[q] ^ ((((mw >> (2 * q)) & 3u) * 0x40008000u) & 0x80008000u);
       x[2 * q] = __uint_as_float(ww << 16);
       x[2 * q + 1] = __uint_as_float(ww & 0xFFFF0000u);
     }
