@@ -5,7 +5,10 @@
 // the block then inverts the transform (FWHT, x (D s_dec), optional dense
 // rotation R^T) and stores contiguous 32-byte (bf16) / 64-byte (fp32) writes
 // per lane.  A group that fails any check is written as zeros with
-// HQ_ERR_CORRUPT.
+// HQ_ERR_CORRUPT: without the rotation each lane stores what it decoded and
+// the block's verdict, taken after the stores, has every lane of a corrupt
+// group overwrite its values with zeros (so no block barrier waits for the
+// slowest lane's parse before the transform).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,13 +41,13 @@ decode_kernel(DecodeArgs a) {
   constexpr int kRS = kTile + 4;                 // row stride of the rotation's operand
   extern __shared__ __align__(16) float s_dyn[];  // ROT: y [32][kRS]
   float e[16];
-  const bool ok = decode_lane<LAT, K>(a, g, e, s_start, s_warp);
+  // ok: the group's verdict with the rotation, this lane's own without it
+  const bool ok = decode_lane<LAT, K, BlockBar, !ROT>(a, g, e, s_start, s_warp);
   const int64_t t = g * kGroupTiles + tl;
-  if (!ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
+  if (ROT && !ok && tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
   // the transform runs on every lane of the block (its transposes synchronise whole warps)
   fwht128_t8(e, s_tr + tl * kTrTile, r);
   const bool tvalid = t < a.n_tiles;
-  if (!ROT && !tvalid) return;
   if (ok && tvalid) {
     // x = D fl(z s_dec) = fl(z (D s_dec)): the sign commutes with rounding
     if (div_by(t, a.tiles_per_segment, a.seg_shift) == seg0) {
@@ -114,21 +117,34 @@ decode_kernel(DecodeArgs a) {
     }
     if (!tvalid) return;
   }
-  if (a.out_kind == HQ_OUT_F32) {
-    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + t * kTile + 16 * r);
+  if (tvalid) {
+    if (a.out_kind == HQ_OUT_F32) {
+      float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + t * kTile + 16 * r);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      dst[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
-  } else {
-    uint32_t w[8];
+      for (int c = 0; c < 4; ++c)
+        dst[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+    } else {
+      uint32_t w[8];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(e[2 * h], e[2 * h + 1]);   // RNE
-      w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      for (int h = 0; h < 8; ++h) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(e[2 * h], e[2 * h + 1]);   // RNE
+        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + t * kTile + 16 * r);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + t * kTile + 16 * r);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  if constexpr (!ROT) {
+    // every thread of the block reaches this barrier (none has returned)
+    if (__syncthreads_or(ok ? 0 : 1)) {
+      if (tid == 0) atomicOr(a.status, (uint32_t)HQ_ERR_CORRUPT);
+      if (tvalid) {                              // the same bytes, now zeros
+        const int n16 = a.out_kind == HQ_OUT_F32 ? 4 : 2;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (t * kTile + 16 * r) / 16 * n16;
+        for (int c = 0; c < n16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
   }
 }
 
