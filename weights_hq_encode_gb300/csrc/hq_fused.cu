@@ -12,28 +12,26 @@
 
 #include "hq_decode_lane.cuh"
 #include "hq_fused.h"
+#include "hq_rows.cuh"
 #include "hq_umma.cuh"
 
 namespace hq {
 
-// q'[row] = s_dec * H * (D_h q[row]) for row = b * Hq + hq, h = hq / (Hq / n_kv).
-__global__ void rotate_queries_kernel(QkArgs a) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= a.B * a.Hq) return;
-  const int hq = row % a.Hq, h = hq / (a.Hq / a.n_kv);
+// q'[row] = s_dec * H * D_h * (R_h) q[row] for row = b * Hq + hq,
+// h = hq / (Hq / n_kv), R_h the optional dense rotation of h's segment; 8
+// lanes a row.
+__global__ void __launch_bounds__(kRowThreads) rotate_queries_kernel(QkArgs a) {
+  __shared__ __align__(16) float s_tr[(kRowThreads / 8) * kTrTile];
+  const int tl = threadIdx.x >> 3, r = threadIdx.x & 7;
+  const int row = blockIdx.x * (kRowThreads / 8) + tl;
+  const bool valid = row < a.B * a.Hq;           // every lane stays for the transform
+  const int hq = (valid ? row : 0) % a.Hq, h = hq / (a.Hq / a.n_kv);
   const int64_t seg = div_by((int64_t)h * a.n_tokens, a.dec.tiles_per_segment, a.dec.seg_shift);
-  const uint32_t *mask = a.dec.signs + 4 * seg;
-  float x[128];
-  const uint16_t *q = a.q + (int64_t)row * kTile;
-#pragma unroll
-  for (int i = 0; i < 128; ++i) x[i] = __uint_as_float((uint32_t)q[i] << 16);
-  if (a.dec.rot != nullptr) rotate128(a.dec.rot + seg * (int64_t)(kTile * kTile), x);
-#pragma unroll
-  for (int i = 0; i < 128; ++i)
-    if ((mask[i >> 5] >> (i & 31)) & 1u) x[i] = -x[i];
-  fwht128(x);
-#pragma unroll
-  for (int i = 0; i < 128; ++i) a.qrot[(int64_t)row * kTile + i] = __fmul_rn(x[i], a.dec.s_dec);
+  const uint32_t mw = __ldg(a.dec.signs + 4 * seg + (r >> 1)) >> (16 * (r & 1));
+  rotate_row_t8(valid ? a.q + (int64_t)row * kTile : nullptr,
+                (reinterpret_cast<uintptr_t>(a.q) & 15) == 0,
+                a.dec.rot != nullptr ? a.dec.rot + seg * (int64_t)(kTile * kTile) : nullptr, mw,
+                a.dec.s_dec, a.qrot + (int64_t)(valid ? row : 0) * kTile, s_tr + tl * kTrTile, r);
 }
 
 // Scores of one KV head over a chunk of its token groups for one tile of
@@ -711,7 +709,7 @@ static void launch_pv_lat(const AttnArgs &a, cudaStream_t st) {
 
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st) {
   const int rows = a.B * a.Hq;
-  rotate_queries_kernel<<<(rows + 127) / 128, 128, 0, st>>>(a);
+  rotate_queries_kernel<<<(rows + kRowThreads / 8 - 1) / (kRowThreads / 8), kRowThreads, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return 1;
   switch (lattice) {
     case 8: launch_qk_lat<8>(a, st); break;

@@ -8,27 +8,21 @@
 
 #include "hq_decode_lane.cuh"
 #include "hq_fused.h"
+#include "hq_rows.cuh"
 
 namespace hq {
 
 // ---------------------------------------------------------------- weights
-// x'[b][j] = s_dec * H * (D x[b][j]) for each 128-column tile j of activation
-// row b (the whole matrix is one sign segment).
-__global__ void rotate_x_kernel(GemmArgs a) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (b, j)
-  if (i >= (int64_t)a.B * a.tpr) return;
-  const uint32_t *mask = a.dec.signs;
-  float x[128];
-  const uint16_t *src = a.x + i * kTile;
-#pragma unroll
-  for (int k = 0; k < 128; ++k) x[k] = __uint_as_float((uint32_t)src[k] << 16);
-  if (a.dec.rot != nullptr) rotate128(a.dec.rot, x);      // the matrix is one segment
-#pragma unroll
-  for (int k = 0; k < 128; ++k)
-    if ((mask[k >> 5] >> (k & 31)) & 1u) x[k] = -x[k];
-  fwht128(x);
-#pragma unroll
-  for (int k = 0; k < 128; ++k) a.xrot[i * kTile + k] = __fmul_rn(x[k], a.dec.s_dec);
+// x'[b][j] = s_dec * H * D * (R) x[b][j] for each 128-column tile j of
+// activation row b (the whole matrix is one sign segment); 8 lanes a tile.
+__global__ void __launch_bounds__(kRowThreads) rotate_x_kernel(GemmArgs a) {
+  __shared__ __align__(16) float s_tr[(kRowThreads / 8) * kTrTile];
+  const int tl = threadIdx.x >> 3, r = threadIdx.x & 7;
+  const int64_t i = (int64_t)blockIdx.x * (kRowThreads / 8) + tl;   // (b, j)
+  const bool valid = i < (int64_t)a.B * a.tpr;   // every lane stays for the transform
+  const uint32_t mw = __ldg(a.dec.signs + (r >> 1)) >> (16 * (r & 1));
+  rotate_row_t8(valid ? a.x + i * kTile : nullptr, (reinterpret_cast<uintptr_t>(a.x) & 15) == 0,
+                a.dec.rot, mw, a.dec.s_dec, a.xrot + (valid ? i : 0) * kTile, s_tr + tl * kTrTile, r);
 }
 
 // Each tile's share of y.  A block decodes NG groups d apart, d = tpr /
@@ -160,7 +154,7 @@ static void launch_gemm_lat(const GemmArgs &a, cudaStream_t st) {
 
 int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {
   const int64_t xt = (int64_t)a.B * a.tpr;
-  rotate_x_kernel<<<(unsigned)((xt + 127) / 128), 128, 0, st>>>(a);
+  rotate_x_kernel<<<(unsigned)((xt + kRowThreads / 8 - 1) / (kRowThreads / 8)), kRowThreads, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return 1;
   switch (lattice) {
     case 8: launch_gemm_lat<8>(a, st); break;
