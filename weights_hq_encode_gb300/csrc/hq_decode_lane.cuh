@@ -71,21 +71,33 @@ __device__ __forceinline__ uint64_t read_bits(const uint32_t *W, uint64_t pos, i
   return nb >= 64 ? v : (v >> (64 - nb));
 }
 
-// MSB-first position (0..31) of the n-th (1-based, n <= popc(x)) set bit of
-// x: a branch-free binary search on population counts.
-__device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
-  int p = 0;
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const int c = __popc(x >> (32 - w));        // ones among the top w bits
-    const bool skip = c < n;
-    n -= skip ? c : 0;
-    x = skip ? (x << w) : x;
-    p += skip ? w : 0;
+// MSB-first place (0..7) of each set bit of a byte: nibble k - 1 of
+// entry b is the place of b's k-th set bit.
+struct NthBitInByte {
+  uint32_t v[256];
+  constexpr NthBitInByte() : v() {
+    for (int b = 0; b < 256; ++b) {
+      uint32_t t = 0u;
+      int k = 0;
+      for (int i = 7; i >= 0; --i)
+        if ((b >> i) & 1) t |= (uint32_t)(7 - i) << (4 * k++);
+      v[b] = t;
+    }
   }
-  return p;
-}
+};
+__device__ const NthBitInByte kNthBitInByte = NthBitInByte();
 
+// MSB-first position (0..31) of the n-th (1-based, n <= popc(x)) set bit of
+// x: the byte holding it from the population counts of x's top 8, 16 and 24
+// bits, its place inside the byte from the table.
+__device__ __forceinline__ int nth_set_bit_msb(uint32_t x, int n) {
+  const int c1 = __popc(x >> 24), c2 = __popc(x >> 16), c3 = __popc(x >> 8);
+  const int k = (n > c1 ? 1 : 0) + (n > c2 ? 1 : 0) + (n > c3 ? 1 : 0);   // c1 <= c2 <= c3
+  const int before = n > c3 ? c3 : n > c2 ? c2 : n > c1 ? c1 : 0;
+  const uint32_t byte = (x >> (24 - 8 * k)) & 0xFFu;
+  const uint32_t t = __ldg(&kNthBitInByte.v[byte]);
+  return 8 * k + (int)((t >> (4 * (n - before - 1))) & 7u);
+}
 
 // Quotients of 8 unary codes from bit pos in the general case (a code longer
 // than the lane's 64-bit window, or a quotient of 32 or more): one 32-bit view
@@ -171,16 +183,12 @@ __device__ __forceinline__ bool decode_lane_p(const DecodeArgs &a, int64_t g, in
       }
       if (lane == 31) s_warp[par][warp] = incl;
       Bar::sync();
-      static_assert(kDecThreads / 32 == 8, "two 16-byte reads of the warp totals");
-      const uint4 q0 = reinterpret_cast<const uint4 *>(s_warp[par])[0];
-      const uint4 q1 = reinterpret_cast<const uint4 *>(s_warp[par])[1];
-      const uint32_t ws[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      uint32_t before_w = 0, total = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        before_w += i < warp ? ws[i] : 0u;
-        total += ws[i];
-      }
+      // lane i < 8 takes warp i's total: two warp reductions give the ones
+      // before this warp and the window's total (at most 8192: no wrap)
+      static_assert(kDecThreads / 32 == 8, "one warp total per lane 0..7");
+      const uint32_t wt = lane < kDecThreads / 32 ? s_warp[par][lane] : 0u;
+      const uint32_t before_w = __reduce_add_sync(0xffffffffu, lane < warp ? wt : 0u);
+      const uint32_t total = __reduce_add_sync(0xffffffffu, wt);
       if (wact) {
         const P before = ones + (P)(before_w + incl - pc);
         P m = (before / 16 + 1) * 16;             // at most two boundaries per word
