@@ -96,6 +96,25 @@ def test_gemm_against_oracle(hq, oracle, index, rows, B, rate, lattice, dither):
     assert np.array_equal(y, y2)                                 # deterministic
 
 
+@pytest.mark.parametrize("cols,rows,B", [(128, 37, 1), (512, 19, 9), (2048, 21, 16)])
+def test_gemm_narrow_matrices(hq, oracle, cols, rows, B):
+    """Matrices of 1, 4 and 16 tiles a row (the first columns of a
+    Llama-shaped weight): a group of 32 tiles holds whole rows, so the
+    product kernel sums each row's tile shares itself.  The row counts leave
+    the last group partial; the batch sizes take one, two and four groups a
+    block and a ragged chunk of activation rows."""
+    from oracle import gemm as G
+    from weights_hq_encode_gb300 import inputs as I
+    c = calibration()["weights_8b"]["E8"]["4.0"][0]
+    wb = np.ascontiguousarray(_bits(I.weight_matrix(0, "cpu", rows=rows))[:, :cols])
+    p, stream, words, offsets, what, _s = _weights(oracle, hq, wb, rows, cols, 8, c["k"],
+                                                   c["alpha"], 1, 5)
+    xb = _bits(I.activations(B, cols, device="cpu"))
+    y, st = _run(hq, p, stream, words, offsets, rows, cols, xb)
+    assert st == 0
+    _check(G, what, xb, rows, cols, y)
+
+
 def test_gemm_with_dense_rotation(hq, oracle):
     """Weights coded with a Haar (QJL) rotation: each activation tile is
     rotated by R before the transform."""

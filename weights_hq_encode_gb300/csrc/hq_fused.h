@@ -45,6 +45,8 @@ struct GemmArgs {
   float *xrot;              // [B][cols] fp32: s_dec * H * D * x, per 128-column tile
   float *partial;           // [B][n_tiles] fp32: one tile's share of y
   float *y;                 // [B][rows] fp32
+  int fold_rows = 0;        // set by the launcher: tpr divides 32, so a row's tiles lie in
+                            // one group and the product kernel sums them itself
 };
 
 int launch_decode_qk(const QkArgs &a, int lattice, cudaStream_t st);

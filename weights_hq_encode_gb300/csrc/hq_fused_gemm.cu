@@ -31,11 +31,16 @@ __global__ void __launch_bounds__(kRowThreads) rotate_x_kernel(GemmArgs a) {
 // weight tiles (NG = 1 for a single activation row).  Lane r of tile t holds
 // 16 lattice-domain values of each tile; partial dots with 8 activation rows
 // at a time are reduced over the tile's 8 lanes by a butterfly that leaves
-// one finished row on each lane.
+// one finished row on each lane.  When a weight row's tiles lie in one group
+// (tpr divides 32, so d = 1) the block also sums each row's tile shares and
+// writes y itself, in the order of gemm_reduce_kernel (one warp a row, lane
+// l holding tile l, a fixed butterfly); otherwise the shares go to the
+// workspace for that kernel.
 template <int LAT, int K, int NG>
 __global__ void __launch_bounds__(kDecThreads, NG > 2 ? 2 : 3) gemm_kernel(GemmArgs a, int pair_d) {
   __shared__ uint64_t s_start[kDecThreads + 1];
   __shared__ __align__(16) uint32_t s_warp[2][kDecThreads / 32];
+  __shared__ float s_share[NG][8][kGroupTiles];  // (group, activation row of the chunk, tile)
   const int tid = threadIdx.x, tl = tid >> 3, r = tid & 7;
   const int64_t bq = blockIdx.x / pair_d, bm = blockIdx.x - bq * pair_d;
   const int64_t g0 = NG * pair_d * bq + bm;      // groups g0 + n d, n < NG
@@ -94,7 +99,23 @@ __global__ void __launch_bounds__(kDecThreads, NG > 2 ? 2 : 3) gemm_kernel(GemmA
       }
     }
     const int b = b0 + r;                        // slot kept by lane r is row b0 + r
-    if (b < a.B) {
+    if (a.fold_rows) {                           // uniform: pair_d = 1, rows within groups
+#pragma unroll
+      for (int n = 0; n < NG; ++n) s_share[n][r][tl] = p[n][0];
+      __syncthreads();
+      const int lane = tid & 31, rpg = kGroupTiles / (int)a.tpr, nb = min(8, a.B - b0);
+      const int per_n = 8 * rpg;
+      for (int o = tid >> 5; o < NG * per_n; o += kDecThreads / 32) {   // (n, chunk row, weight row)
+        const int n = o / per_n, bi = (o - n * per_n) / rpg, ol = o - n * per_n - bi * rpg;
+        const int64_t g = g0 + n, orow = g * (kGroupTiles / a.tpr) + ol;
+        if (bi >= nb || g >= a.dec.n_groups || orow >= a.rows) continue;   // warp-uniform
+        float sum = lane < a.tpr ? __fadd_rn(0.0f, s_share[n][bi][ol * (int)a.tpr + lane]) : 0.0f;
+#pragma unroll
+        for (int dd = 16; dd >= 1; dd >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, dd));
+        if (lane == 0) a.y[(int64_t)(b0 + bi) * a.rows + orow] = sum;
+      }
+      __syncthreads();                           // the next chunk rewrites the shares
+    } else if (b < a.B) {
 #pragma unroll
       for (int n = 0; n < NG; ++n) {
         const int64_t tile = tile0 + (int64_t)n * pair_d * kGroupTiles;
@@ -152,7 +173,9 @@ static void launch_gemm_lat(const GemmArgs &a, cudaStream_t st) {
   else launch_gemm_k<LAT, 4>(a, d, st);
 }
 
-int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {
+int launch_decode_gemm(const GemmArgs &args, int lattice, cudaStream_t st) {
+  GemmArgs a = args;
+  a.fold_rows = kGroupTiles % a.tpr == 0 ? 1 : 0;
   const int64_t xt = (int64_t)a.B * a.tpr;
   rotate_x_kernel<<<(unsigned)((xt + kRowThreads / 8 - 1) / (kRowThreads / 8)), kRowThreads, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return 1;
@@ -163,6 +186,7 @@ int launch_decode_gemm(const GemmArgs &a, int lattice, cudaStream_t st) {
     default: launch_gemm_lat<1>(a, st); break;
   }
   if (cudaGetLastError() != cudaSuccess) return 1;
+  if (a.fold_rows) return 0;                     // y written by the product kernel
   const int64_t warps = (int64_t)a.B * a.rows;
   gemm_reduce_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
