@@ -62,41 +62,8 @@ constexpr float kGrid16 = -0.5f + 0x1p-17f;
 
 // ---------------------------------------------------------------- FWHT-128
 // Unnormalised Walsh-Hadamard transform, natural (Sylvester) order, stages
-// h = 1, 2, ..., 64 in that order (Method 1).
-__device__ __forceinline__ void fwht128(float x[128]) {
-#pragma unroll
-  for (int h = 1; h < 128; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      if (i & h) continue;
-      float a = x[i], b = x[i + h];
-      x[i] = __fadd_rn(a, b);
-      x[i + h] = __fsub_rn(a, b);
-    }
-  }
-}
-
-// x <- R x for one 128-vector held by one thread (R row-major, global): one
-// fused multiply-add chain over j = 0..127 per output, from +0.
-__device__ __forceinline__ void rotate128(const float *R, float x[128]) {
-  float z[128];
-#pragma unroll 1
-  for (int i = 0; i < 128; ++i) {
-    float acc = 0.0f;
-    const float4 *row = reinterpret_cast<const float4 *>(R + i * 128);
-#pragma unroll
-    for (int j4 = 0; j4 < 32; ++j4) {
-      const float4 q = __ldg(row + j4);
-      acc = __fmaf_rn(q.x, x[4 * j4], acc);
-      acc = __fmaf_rn(q.y, x[4 * j4 + 1], acc);
-      acc = __fmaf_rn(q.z, x[4 * j4 + 2], acc);
-      acc = __fmaf_rn(q.w, x[4 * j4 + 3], acc);
-    }
-    z[i] = acc;
-  }
-#pragma unroll
-  for (int i = 0; i < 128; ++i) x[i] = z[i];
-}
+// h = 1, 2, ..., 64 in that order, each butterfly (a, b) -> (a + b, a - b)
+// rounded once (Method 1): fwht128_t8 below.
 
 // ---------------------------------------------------------------- packed fp32 pairs
 // sm_100+ executes add / sub / mul / fma on a pair of fp32 values in one
@@ -146,8 +113,8 @@ __device__ __forceinline__ void bfly2(float &a0, float &a1, float &b0, float &b1
 // kTrRow floats apart), lane c reads row c back (coordinates c + 8m,
 // m = 0..15) and runs stages 16, 32, 64 on pairs of adjacent columns, then
 // writes the row back: the result stays in the table.  Every coordinate goes
-// through the same additions in the same stage order as the single-thread
-// form.  `tile` is the tile's table (kTrTile floats, 16-byte aligned), private
+// through the additions of the definition above, stage by stage in order,
+// whichever lane makes them.  `tile` is the tile's table (kTrTile floats, 16-byte aligned), private
 // to its 8 lanes; with rows of 20 floats and tables 176 floats apart, the
 // pair stores (16 lanes = two tiles) and the 16-byte row loads and stores
 // (8 lanes = one tile) of a warp are free of bank conflicts.  All 32 lanes of

@@ -4,10 +4,9 @@
 //
 // A row is spread over 8 consecutive lanes like a codec tile (lane r holds
 // dimensions 16 r .. 16 r + 15), so the transform is the tiled one.  The
-// roundings are those of the single-thread form: the optional dense rotation
-// is one fused multiply-add chain over j = 0..127 from +0 per output, the
-// sign flips are exact and the transform makes the same additions in the same
-// stage order.
+// optional dense rotation is one fused multiply-add chain over j = 0..127
+// from +0 per output, the sign flips are exact and the transform rounds each
+// butterfly once, stage by stage in order, as its definition states.
 #pragma once
 #include <cuda_runtime.h>
 
