@@ -79,6 +79,11 @@ def test_sign_masks_are_philox_words(oracle):
     # masks of different segments/seeds differ and are balanced on average
     bits = np.unpackbits(np.stack([oracle.make_signs(3, s) for s in range(256)]).view(np.uint8))
     assert abs(bits.mean() - 0.5) < 0.01
+    # segments past 2^32 put their high half in the second counter word
+    seg = (1 << 32) + 5
+    m = oracle.make_signs(0x0123456789ABCDEF, seg)
+    ref = oracle.philox([5, 1, 0, 0x5349474E], [0x89ABCDEF, 0x01234567])
+    assert (m == ref).all()
 
 
 # ------------------------------------------------------------------ FWHT
@@ -312,6 +317,100 @@ def test_dither_in_voronoi_cell_with_right_second_moment(oracle, lat):
     assert not (oracle.dither(lat, 99, 5) == oracle.dither(lat, 99, 6)).all()
 
 
+# The dither rebuilt outside the oracle from its stated reading: the Philox
+# words of (tile, j) (pinned above by known answers and Triton), the grid
+# midpoints of each lattice's box, then the nearest lattice point found by
+# enumeration; u = u0 - Q(u0) in fp32.
+_DITHER_TAG = 0x44495448                                       # 'DITH'
+
+
+def _dither_halves(oracle, seed, tile, j):
+    w = oracle.philox([tile & 0xFFFFFFFF, tile >> 32, j, _DITHER_TAG],
+                      [seed & 0xFFFFFFFF, seed >> 32])
+    b = []
+    for m in range(4):
+        b += [int(w[m]) & 0xFFFF, int(w[m]) >> 16]
+    return np.array(b, np.float64)
+
+
+def _brute_argmin(pts, ok, y):
+    """Nearest admissible candidate of each row and its margin over the next."""
+    d = ((pts - y[:, None, :]) ** 2).sum(-1)
+    d[~ok] = np.inf
+    order = np.argsort(d, axis=1, kind="stable")
+    i = np.arange(y.shape[0])
+    return pts[i, order[:, 0]], d[i, order[:, 1]] - d[i, order[:, 0]]
+
+
+def _brute_e8(y):
+    pe, oke = _brute_coset(y, False)
+    po, oko = _brute_coset(y, True)
+    return _brute_argmin(np.concatenate([pe, po], 1), np.concatenate([oke, oko], 1), y)
+
+
+def _brute_d4(y):
+    combos = ((np.arange(16)[:, None] >> np.arange(4)[None, :]) & 1).astype(np.float64)
+    pts = np.floor(y)[:, None, :] + combos[None, :, :]
+    ok = (np.round(pts.sum(-1)).astype(np.int64) % 2) == 0
+    return _brute_argmin(pts, ok, y)
+
+
+def _brute_a2(y):
+    """Points (m / 2, fl32(h n)) with m = n mod 2 around each (x, y)."""
+    h = np.float32(np.sqrt(3.0) / 2.0)
+    n0, m0 = np.floor(y[:, 1] / float(h)), np.floor(2.0 * y[:, 0])
+    dn, dm = np.arange(-1, 3), np.arange(-2, 4)
+    N = (n0[:, None, None] + dn[None, :, None] + 0 * dm[None, None, :]).reshape(len(y), -1)
+    M = (m0[:, None, None] + dm[None, None, :] + 0 * dn[None, :, None]).reshape(len(y), -1)
+    ok = ((M - N) % 2) == 0
+    pts = np.stack([M / 2.0, (h * N.astype(np.float32)).astype(np.float64)], -1)
+    return _brute_argmin(pts, ok, y)
+
+
+@pytest.mark.parametrize("lat", [8, 4, 2, 1])
+def test_dither_is_a_grid_midpoint_minus_its_nearest_lattice_point(oracle, lat):
+    """Method 4 ("Bias correction": U uniform on the Voronoi cell, drawn afresh
+    per vector from the seed), rebuilt outside the oracle: the 16-bit halves
+    b of the Philox words of counter (tile lo, tile hi, j, 'DITH') under the
+    64-bit seed give the midpoints u0 of a 2^16-step grid on each lattice's
+    box (E8: (-1, 1)^7 x (-2, 2); D4: (-1/2, 1/2)^3 x (-1, 1); A2: [-1/2,
+    1/2) x h[-1, 1); Z: (-1/2, 1/2)), and u = u0 - Q(u0) with Q found by
+    enumeration.  Tiles past 2^32 and 2^40 exercise the counter's high word."""
+    seed = 0x9E3779B97F4A7C15
+    checked = 0
+    for t in (0, 1, 77, (1 << 32) + 7, (1 << 40) + 3):
+        u = oracle.dither(lat, seed, t)
+        for j in range(16):
+            b = _dither_halves(oracle, seed, t, j)
+            got = u[8 * j:8 * j + 8]
+            if lat == 8:
+                u0 = -1.0 + (b + 0.5) * 2.0**-15
+                u0[7] = -2.0 + (b[7] + 0.5) * 2.0**-14
+                q, margin = _brute_e8(u0[None, :])
+                exp = (u0 - q[0]).astype(np.float32)                 # exact
+            elif lat == 4:
+                u0 = -0.5 + (b + 0.5) * 2.0**-16
+                u0[[3, 7]] = -1.0 + (b[[3, 7]] + 0.5) * 2.0**-15
+                q, margin = _brute_d4(u0.reshape(2, 4))
+                exp = (u0 - q.reshape(8)).astype(np.float32)
+            elif lat == 2:
+                h = np.float32(np.sqrt(3.0) / 2.0)
+                ux = (-0.5 + (b[0::2] + 0.5) * 2.0**-16).astype(np.float32)
+                uy = h * (-1.0 + (b[1::2] + 0.5) * 2.0**-15).astype(np.float32)
+                pts, margin = _brute_a2(np.stack([ux, uy], -1).astype(np.float64))
+                exp = np.empty(8, np.float32)
+                exp[0::2] = ux - pts[:, 0].astype(np.float32)
+                exp[1::2] = uy - pts[:, 1].astype(np.float32)
+            else:
+                exp = (-0.5 + (b + 0.5) * 2.0**-16).astype(np.float32)
+                margin = np.ones(1)
+            if (margin < 1e-9).any():
+                continue                                  # a tie: either point is nearest
+            assert (got == exp).all(), (t, j, got, exp)
+            checked += 1
+    assert checked >= 75
+
+
 @pytest.mark.parametrize("lat,name", [(8, "E8"), (4, "D4"), (2, "A2"), (1, "Z")])
 def test_dithered_error_second_moment(oracle, lat, name):
     """With subtractive dither the error v - u - y is uniform on the Voronoi
@@ -521,6 +620,81 @@ def test_range_guard(oracle):
     assert enc["status"] & oracle.ERR_RANGE
     zero = oracle.encode(P, np.zeros((3, 128), np.uint16), want_codes=True)
     assert (enc["codes"] == zero["codes"]).all()
+
+
+def test_range_rule_boundary(oracle):
+    """The range rule's limit on |y| is 2^20, inclusive, checked where it
+    bites: alpha = fl32(sqrt 128) makes s_enc = 1, so a tile holding c at one
+    coordinate (no sign flips, no dither) has y = c at every coordinate."""
+    alpha = float(np.float32(np.sqrt(128.0)))
+    assert oracle.encode_scale(alpha) == 1.0
+    P = oracle.make_params(8, 15, alpha, 0, 0, np.zeros(4, np.uint32), 1 << 40)
+    cases = [  # (coordinate: bf16 bits, in range, code of every coordinate if in range)
+        ({0: 0x4980}, True, 1 << 20),                 # 2^20
+        ({0: 0xC980}, True, -(1 << 20)),              # -2^20
+        ({0: 0x4981}, False, 0),                      # 2^20 (1 + 2^-7)
+        ({0: 0x4980, 77: 0x3F80}, False, 0),          # y = 2^20 +- 1: half the coordinates out
+    ]
+    for vals, inside, code in cases:
+        x = np.zeros((1, 128), np.uint16)
+        for i, b in vals.items():
+            x[0, i] = b
+        enc = oracle.encode(P, x, want_codes=True)
+        assert bool(enc["status"] & oracle.ERR_RANGE) == (not inside), vals
+        assert (enc["codes"] == code).all(), vals
+
+
+def test_scale_and_dither_round_once(oracle):
+    """y = fl(z s_enc + u) with a single rounding (the codec's reading of the
+    scale and the subtractive dither, Method 1 and 4), against exact
+    arithmetic: a tile with c at coordinate 0 (no sign flips) has z = c at
+    every coordinate; c s_enc + u is exact in float64 and is rounded to fp32
+    once.  With |y| near 2^16 one fp32 step is 2^-7, so rounding c s_enc
+    first moves some 8-vectors across a Voronoi boundary of 2E8: the oracle's
+    codes must be the enumerated nearest points of the once-rounded y, and
+    the twice-rounded y must give other codes for some vectors of the sample
+    (so that the check can tell the two readings apart)."""
+    alpha, seed, n = 3.3, 2024, 400
+    s = float(np.float32(alpha / np.sqrt(128.0)))
+    assert oracle.encode_scale(alpha) == s
+    # c = 1.5546875 * 2^17 (exact in bf16): c s_enc lies 0.49 fp32 steps off
+    # the fp32 grid, so the two readings round differently for about half the
+    # values of u
+    c = 203776.0
+    assert abs(c * s - float(np.float32(c * s))) > 0.45 * 2.0**-8
+    x = np.zeros((n, 128), np.uint16)
+    x[:, 0] = np.array([c], np.float32).view(np.uint32)[0] >> 16
+    P = oracle.make_params(8, 15, alpha, 1, seed, np.zeros(4, np.uint32), 1 << 40)
+    enc = oracle.encode(P, x, want_codes=True)
+    assert enc["status"] == 0
+    u = np.stack([oracle.dither(8, seed, t) for t in range(n)]).astype(np.float64)
+    y1 = (c * s + u).astype(np.float32).astype(np.float64)    # exact sum, one rounding
+    y2 = (np.float32(c * s) + u.astype(np.float32)).astype(np.float64)
+    y1, y2 = y1.reshape(-1, 8), y2.reshape(-1, 8)
+    codes = enc["codes"].reshape(-1, 8)
+    q1, m1 = _brute_e8(y1)
+    q2, m2 = _brute_e8(y2)
+    sure = (m1 > 1e-6) & (m2 > 1e-6)
+    assert sure.mean() > 0.99
+    assert (codes[sure] == q1[sure]).all()
+    assert ((q1 != q2).any(-1) & sure).sum() >= 5
+
+
+def test_scores_query_heads_read_their_kv_head(oracle):
+    """Grouped-query attention as in the fused-scores workload (group 4):
+    query head hq reads KV head hq // (Hq / n_kv).  Every token of K head h
+    holds 1000 h + d at dimension d and query head hq is the unit vector of
+    dimension hq, so each score names the head it read."""
+    n_kv, Hq, B, T = 2, 8, 2, 3
+    khat = np.zeros((n_kv * T, 128), np.float32)
+    for h in range(n_kv):
+        khat[h * T:(h + 1) * T] = 1000.0 * h + np.arange(128)
+    q = np.zeros((B, Hq, 128), np.uint16)
+    for hq in range(Hq):
+        q[:, hq, hq] = 0x3F80                                  # bf16 1.0
+    sc = oracle.scores(khat, n_kv, T, q.reshape(B * Hq, 128), B, Hq)
+    exp = np.array([1000.0 * (hq // (Hq // n_kv)) + hq for hq in range(Hq)])
+    assert (sc == exp[None, :, None]).all()
 
 
 def test_scalar_special_case_is_textbook_uniform_quantizer(oracle):
