@@ -35,7 +35,11 @@
  *
  * Parity status: every function here is pinned by a CPU test (known-answer
  * vectors, brute-force nearest point, exhaustive round trips, closed forms,
- * measured second moments); none is "parity unpinned".
+ * measured second moments, exact-arithmetic references); none is "parity
+ * unpinned".  One convention inside a pinned function has no outside fact to
+ * pin it: the order of the FWHT's stages (h = 1, 2, ..., 64).  Other orders
+ * give the same transform up to rounding, so the tests pin the transform
+ * (Sylvester H, per-stage error bound) and the order is a stated reading.
  */
 #include <math.h>
 #include <pthread.h>
