@@ -6,7 +6,10 @@ imports, links or calls anything here, and this module imports nothing from
 the product package.
 
 The C source is compiled on first use with the host compiler (gcc, ``-O2
--ffp-contract=off``, no fast-math) into ``oracle/_build/``.
+-ffp-contract=off``, no fast-math) into ``oracle/_build/``.  With the
+environment variable ``HQ_ORACLE_SRC`` set to another C file (a copy of
+``hq_oracle.c`` with a mistake planted by ``tests/oracle_mutations.py``),
+that file is compiled instead, into a library beside it.
 """
 from __future__ import annotations
 
@@ -18,8 +21,9 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "hq_oracle.c")
-_BUILD = os.path.join(_HERE, "_build")
+_ALT = os.environ.get("HQ_ORACLE_SRC")
+_SRC = os.path.abspath(_ALT) if _ALT else os.path.join(_HERE, "hq_oracle.c")
+_BUILD = os.path.dirname(_SRC) if _ALT else os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "libhq_oracle.so")
 _lock = threading.Lock()
 _lib = None
